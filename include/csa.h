@@ -1,0 +1,304 @@
+/*
+ * csa.h -- C ABI of the CSA2 compressed-sparse-attention library for B300 (sm_103a).
+ *
+ * The library implements one data path: a shared FP4 global KV cache built by pair-merging adjacent
+ * token latents, a block indexer with Top-K selection (flat or hierarchical), and sparse attention
+ * over the selected cache blocks merged with each layer's own sliding-window KV.
+ *
+ * Sources the operations follow (web pages about the DeepSeek-V4.1-Flash technical report):
+ *   [digest] "DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression" (paper-digest.app),
+ *            sections "Core Mechanics" and "Terminology".
+ *   [abstract] "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" (thelatestinai.com),
+ *            section "Abstract".
+ *   [card]   "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" (observer.broadside card),
+ *            section "Key ideas".
+ *   [news]   "DeepSeek Releases V4.1 Flash with 4x KV Cache Compression for Long-Context Agent
+ *            Workflows" (promptgoblins), section "Details".
+ * The pages fix the structure only (one 512-d latent shared by K and V across heads, 2 positions merged
+ * per entry, FP4 storage, blocks of 8, Top-K, hierarchical indexing up to 2,048 blocks, a 128-token
+ * sliding window, Full/Reindex/Reuse layers). Every numeric format and rounding rule below is this
+ * library's own definition; each is stated where it is used.
+ *
+ * Conventions shared by every call
+ *   - All pointers marked "device" are CUDA device pointers on the current device. The caller owns every
+ *     buffer; the library never allocates or frees device memory.
+ *   - Every call is stream-ordered and asynchronous on `stream`. The returned csa_status reports host-side
+ *     validation only; when it is not CSA_OK nothing was launched.
+ *   - Problems only the device can see (an out-of-range block id, an entry count beyond capacity) never
+ *     trap: the kernel skips the offending item and records a code in the workspace header, which
+ *     csa_get_device_status() returns. The header must be zeroed once (csa_workspace_reset) before first
+ *     use; csa_get_device_status() clears it again after reading.
+ *   - Only sm_103 devices are accepted (CSA_ERR_UNSUPPORTED_DEVICE otherwise). There is no CPU fallback.
+ *   - Calls are safe from several host threads as long as they use different workspaces. Calls that share
+ *     a workspace must be ordered on one stream.
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA_ABI_VERSION 1
+
+/* Width of the shared latent that serves as key and value for every head ([digest] Core Mechanics,
+   "Channel"). */
+#define CSA_LATENT_DIM 512
+/* Cache entries per selectable block ([card] Key ideas, "blocks of 8"). */
+#define CSA_BLOCK_ENTRIES 8
+/* Elements that share one E4M3 scale byte (format of this library). */
+#define CSA_SCALE_GROUP 16
+/* Blocks per super-block of the hierarchical indexer (reading of [card] Key ideas, "hierarchical
+   sparse indexer (up to 2,048 blocks of 8 positions)"). */
+#define CSA_SUPER_BLOCK 64
+/* Largest Top-K (in blocks) accepted by csa_index_topk and the attention calls. */
+#define CSA_MAX_TOP_K 2048
+/* Bytes at the start of every workspace reserved for the device status word. */
+#define CSA_WS_HEADER_BYTES 256
+
+typedef enum csa_status {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,        /* null pointer, bad size, unsupported shape or flag */
+  CSA_ERR_ALIGNMENT = 2,          /* a pointer or stride breaks the alignment stated for it */
+  CSA_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not sm_103 */
+  CSA_ERR_WORKSPACE_TOO_SMALL = 4,
+  CSA_ERR_CUDA = 5,               /* a CUDA runtime call failed (launch, attribute query) */
+  CSA_ERR_DEVICE_CHECK = 6,       /* a kernel found invalid data; see the conventions above */
+  CSA_ERR_TIMEOUT = 7             /* a bounded device-side wait gave up */
+} csa_status;
+
+enum { CSA_DTYPE_BF16 = 0, CSA_DTYPE_F32 = 1 };
+
+/* Scale rule of the FP4 quantiser (format of this library):
+ *   CSA_SCALE_AMAX: s = E4M3_rne_satfinite(amax / 6), the usual rule for latents.
+ *   CSA_SCALE_POW2: s = smallest power of two >= amax / 6, clamped to [2^-9, 256]; exact for index keys
+ *                   whose values are integers in [-4, 4]. */
+enum { CSA_SCALE_AMAX = 0, CSA_SCALE_POW2 = 1 };
+
+/* Indexer flags. CSA_IDX_RELU: score = sum_h w_h * max(0, q_h . k). Without it the ReLU is dropped.
+   CSA_IDX_HIER: two-stage (super-block, then block) selection; decode only. */
+enum { CSA_IDX_RELU = 1, CSA_IDX_HIER = 2 };
+
+int csa_abi_version(void);
+const char* csa_status_string(csa_status status);
+
+/* Bytes of one packed entry of width `dim` (dim/2 code bytes + dim/16 scale bytes), and of one block
+   of 8 entries. dim = 512 gives 288 and 2,304. Returns 0 for a dim that is not a positive multiple of 16. */
+size_t csa_entry_bytes(int dim);
+size_t csa_block_bytes(int dim);
+
+/* Zeroes the workspace header (status word). Async on `stream`. */
+csa_status csa_workspace_reset(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronizes `stream`, reads the workspace status word, clears it, and returns CSA_OK,
+   CSA_ERR_DEVICE_CHECK or CSA_ERR_TIMEOUT (or CSA_ERR_CUDA if the synchronize failed). */
+csa_status csa_get_device_status(void* ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * csa_pack_fp4 -- pair-merge and FP4-pack token rows into cache entries.
+ *
+ * Follows [digest] Core Mechanics ("Sequence: the Encoder merges 2 adjacent positions into 1 cache
+ * entry"), [digest] Terminology / [abstract] Abstract / [card] Key ideas ("FP4 global KV").
+ *
+ * For every sequence b and new entry i in [0, n_tokens / merge):
+ *   m = merge == 2 ? fl32(fl32(x[2i] + x[2i+1]) * 0.5)  :  x[i]        (fp32, IEEE round-to-nearest)
+ * then per group of 16 elements: amax = max |m|, scale s by `scale_rule`, code_j = E2M1_rne_satfinite(
+ * fl32(m_j / s)) (sign kept, so a negative value that rounds to zero is code 0x8; s == 0 gives all-zero
+ * codes). An odd trailing token (merge == 2) is not packed.
+ *
+ * Entry e = first_entry[b] + i is written to block e / 8, slot e % 8 of sequence b:
+ *   block = [8 x dim/2 code bytes, slot-major][8 x dim/16 E4M3 scale bytes, slot-major]
+ *   code byte j of an entry holds element 2j in its low nibble and 2j+1 in its high nibble.
+ *
+ * If coarse_sum is not NULL, after packing every super-block (64 blocks = 512 entries) that received a
+ * new entry is recomputed: coarse_sum[b][g][d] = sum, in ascending entry order in fp32, of the dequantized
+ * element d over entries [512 g, min(512 (g+1), first_entry[b] + n_new)). This assumes entries are appended
+ * in order, so that [0, first_entry[b] + n_new) is the valid prefix. The sums are exact when the dequantized
+ * values are integers (index keys under CSA_SCALE_POW2 with integer inputs).
+ *
+ * Arguments (all strides in elements unless stated):
+ *   x            device, [batch][n_tokens][dim] rows of x_dtype; each row contiguous; 16-byte aligned rows.
+ *   dim          512 for latents; any multiple of 64 up to 1024 for index keys.
+ *   first_entry  device int32 [batch], or NULL for 0. first_entry[b] + n_new must be <= max_entries
+ *                (else the sequence is skipped and CSA_ERR_DEVICE_CHECK recorded).
+ *   cache        device, 16-byte aligned; sequence b starts at cache + b * cache_stride_b (bytes, a multiple
+ *                of 16, >= ceil(max_entries / 8) * csa_block_bytes(dim)).
+ *   coarse_sum   device fp32 [batch][ceil(max_entries / 512)][dim] with stride coarse_stride_b, or NULL.
+ *   ws           workspace of at least CSA_WS_HEADER_BYTES (status word only).
+ * ------------------------------------------------------------------------------------------------ */
+typedef struct csa_pack_args {
+  const void* x;
+  int32_t x_dtype;
+  int32_t dim;
+  int64_t x_stride_b;
+  int64_t x_stride_t;
+  int64_t n_tokens;
+  int32_t merge;
+  int32_t scale_rule;
+  const int32_t* first_entry;
+  int64_t max_entries;
+  uint8_t* cache;
+  int64_t cache_stride_b;
+  float* coarse_sum;
+  int64_t coarse_stride_b;
+} csa_pack_args;
+
+csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* args, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * csa_index_topk -- score cache blocks with an indexer query and select the Top-K blocks.
+ *
+ * Follows [card] Key ideas ("Reindex ... rescore with its own indexer query", "Reuse (reuse both KV and
+ * Top-K indices)", "a hierarchical sparse indexer (up to 2,048 blocks of 8 positions) trims decoder
+ * indexing") and [news] Details ("block-based approach").
+ *
+ * Per query u = (b, j):
+ *   entry score   s_e = sum over h = 0..H-1, in that order, of fl32(w_h * r_{h,e}),
+ *                 r_{h,e} = max(0, q_h . k_e) (plain q_h . k_e without CSA_IDX_RELU),
+ *                 k_e the dequantized index key; the dot product is exact when q and k are integers with
+ *                 |partial sums| <= 2048 (the kernels multiply in fp16 and accumulate in fp32).
+ *   eligible      e < n_entries[b], and 2e + 1 <= q_pos[b][j] when q_pos is given (prefill causality).
+ *   block score   S_blk = max of s_e over eligible entries of the block; blocks with none are not
+ *                 candidates.
+ *   Top-K         the min(top_k, #candidates) candidates with the largest S, ties to the lower block id,
+ *                 written in ascending block id and padded with -1.
+ *   CSA_IDX_HIER  (q_pos must be NULL) super-block g (blocks [64 g, 64 g + 64)) is first scored with the
+ *                 same score function applied to coarse_sum[b][g]; the keep_blocks / 64 best super-blocks
+ *                 (ties to the lower id) are kept and the block Top-K runs over their blocks only.
+ *
+ * Arguments:
+ *   q_idx     device fp32 [batch][n_query][heads][dim], contiguous; 16-byte aligned.
+ *   heads     1, 2, 4 or 8.   dim: 64, 128 or 256.
+ *   head_w    device fp32 [heads] or NULL for all ones.
+ *   keys      device packed index keys (csa_pack_fp4 layout with width dim), 16-byte aligned; sequence b
+ *             at keys + b * keys_stride_b bytes (a multiple of 16).
+ *   n_entries device int32 [batch]; each in [0, max_entries].
+ *   q_pos     device int32 [batch][n_query] token positions (prefill) or NULL (decode: every entry
+ *             below n_entries is eligible).
+ *   coarse_sum, coarse_stride_b   CSA_IDX_HIER only: as written by csa_pack_fp4.
+ *   keep_blocks CSA_IDX_HIER only: a multiple of 64, at most 4096 (the pages' figure is 2,048).
+ *   top_k     1..CSA_MAX_TOP_K.
+ *   out_idx   device int32 [batch][n_query][top_k].
+ *   out_block_scores  optional device fp32 [batch][n_query][ceil(max_entries / 8)] (flat mode only):
+ *             the block scores, -inf for non-candidates.
+ *   ws        at least csa_index_topk_workspace_size(batch, args) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------------------------------ */
+typedef struct csa_index_args {
+  int64_t n_query;
+  int32_t heads;
+  int32_t dim;
+  const float* q_idx;
+  const float* head_w;
+  int32_t flags;
+  int32_t top_k;
+  const uint8_t* keys;
+  int64_t keys_stride_b;
+  const int32_t* n_entries;
+  int64_t max_entries;
+  const int32_t* q_pos;
+  const float* coarse_sum;
+  int64_t coarse_stride_b;
+  int32_t keep_blocks;
+  int32_t reserved0;
+  int32_t* out_idx;
+  float* out_block_scores;
+} csa_index_args;
+
+size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* args);
+csa_status csa_index_topk(int64_t batch, const csa_index_args* args, void* ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * csa_sparse_attn_decode / csa_sparse_attn_prefill -- attention over the selected blocks of the shared
+ * FP4 cache merged with the layer's own sliding-window KV.
+ *
+ * Follows [digest] Core Mechanics ("one 512-dim latent shares keys and values across all attention
+ * heads"), [digest] Terminology ("SWA ... each token sees only a recent window (128 here)") and [card]
+ * Key ideas ("Every layer keeps its own query and sliding-window KV").
+ *
+ * Per query u = (b, j) and head h, the rows are
+ *   R = { dequantized entry e of every block listed in idx[u] (id >= 0), e eligible }  U  W_u
+ * where eligibility is as for csa_index_topk and W_u is the window:
+ *   decode : rows 0 .. swa_len[b]-1 of swa[b]
+ *   prefill: the rows of tokens max(p - window + 1, swa_first_pos[b]) .. p, p = q_pos[b][j]; the row of
+ *            token t is t - swa_first_pos[b].
+ * A row c (512 values) is both key and value:
+ *   z_c = scale * (q_h . c),  out[u][h] = sum_c softmax(z)_c * c,  out_lse[u][h] = log sum_c exp(z_c).
+ * Duplicates between the cache and the window are not removed. A query with no rows gets out = 0 and
+ * lse = -inf.
+ *
+ * Precision (library choice): cache rows are dequantized exactly (E2M1 x E4M3 products fit fp16); q and
+ * window rows are converted from bf16 to fp16 (exact for 2^-14 <= |x| <= 65504; smaller magnitudes lose
+ * at most 2^-25 absolute; larger ones overflow, so |q|, |window| must stay below 65504); products are
+ * accumulated in fp32, probabilities are rounded to fp16 for the value product, sums are fp32.
+ *
+ * Arguments:
+ *   n_query   queries per sequence (decode may use more than one; all see the whole cache prefix).
+ *   heads     16, 32, 48 or 64.   scale: softmax scale (1/sqrt(512) for the pages' latent).
+ *   q         device bf16 [batch][n_query][heads][512], contiguous, 16-byte aligned.
+ *   cache     device packed latent cache (csa_pack_fp4, dim 512), 16-byte aligned; stride in bytes,
+ *             a multiple of 16.
+ *   n_entries device int32 [batch]; max_entries bounds it and the block ids.
+ *   idx       device int32 [batch][n_query][top_k] block ids (ascending not required; -1 = empty slot).
+ *   window    sliding-window length in rows, 0..1024 (the pages use 128).
+ *   swa       device bf16 [batch][swa_rows][512] (stride swa_stride_b elements, rows contiguous).
+ *   swa_len   decode: device int32 [batch], each in [0, min(window, swa_rows)].
+ *   swa_first_pos, q_pos  prefill: device int32 [batch] and [batch][n_query].
+ *   out       device fp32 [batch][n_query][heads][512].   out_lse: device fp32 [batch][n_query][heads]
+ *             or NULL.
+ *   ws        at least csa_sparse_attn_workspace_size(batch, args) bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------------------------------ */
+typedef struct csa_attn_args {
+  int64_t n_query;
+  int32_t heads;
+  float scale;
+  const void* q;
+  const uint8_t* cache;
+  int64_t cache_stride_b;
+  const int32_t* n_entries;
+  int64_t max_entries;
+  const int32_t* idx;
+  int32_t top_k;
+  int32_t window;
+  const int32_t* q_pos;
+  const void* swa;
+  int64_t swa_stride_b;
+  int64_t swa_rows;
+  const int32_t* swa_len;
+  const int32_t* swa_first_pos;
+  float* out;
+  float* out_lse;
+} csa_attn_args;
+
+size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* args);
+csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Kernel timing (opt-in, not thread-safe). Between csa_profile_begin and csa_profile_end every kernel
+ * this library launches is bracketed by two CUDA timing events recorded on its launch stream (also
+ * inside stream capture, as external event nodes). csa_profile_end synchronizes the device and reports,
+ * per kernel name, the number of launches and their summed device time. Launches beyond max_launches
+ * are counted in *dropped but not timed.
+ * ------------------------------------------------------------------------------------------------ */
+typedef struct csa_kernel_time {
+  char name[48];
+  int64_t launches;
+  double total_ms;
+} csa_kernel_time;
+
+csa_status csa_profile_begin(int max_launches);
+csa_status csa_profile_end(csa_kernel_time* out, int max_out, int* n_out, int64_t* dropped);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */
