@@ -1,0 +1,426 @@
+// C ABI of the CSA2 library: host-side validation, workspace layout, launch configuration, the device
+// status word and opt-in kernel timing. Every compute step runs in the kernels of this directory; the
+// host code only checks arguments and launches. Nothing here allocates device memory.
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "csa_internal.cuh"
+
+using namespace csa;
+
+namespace {
+
+struct DeviceInfo {
+  int checked = 0;     // 0 unknown, 1 ok, -1 unsupported
+  int num_sms = 0;
+};
+DeviceInfo g_dev[64];
+
+// Validates the current device (sm_103) and caches its SM count.
+csa_status current_device(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return CSA_ERR_UNSUPPORTED_DEVICE;
+  DeviceInfo& d = g_dev[dev];
+  if (d.checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    d.num_sms = sms;
+    d.checked = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (d.checked < 0) return CSA_ERR_UNSUPPORTED_DEVICE;
+  if (num_sms) *num_sms = d.num_sms;
+  return CSA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------------------------
+// Index workspace: [header][block scores][coarse scores][kept super-blocks]
+// ---------------------------------------------------------------------------------------------
+struct IndexLayout {
+  int64_t units, n_b_cap, n_slots, n_super, keep_super;
+  size_t scores_off, coarse_off, kept_off, total;
+};
+
+IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
+  IndexLayout L{};
+  const bool hier = (a->flags & CSA_IDX_HIER) != 0;
+  L.units = batch * a->n_query;
+  L.n_b_cap = ceil_div(a->max_entries, kBlockEntries);
+  L.n_super = ceil_div(L.n_b_cap, kSuper);
+  L.keep_super = hier ? a->keep_blocks / kSuper : 0;
+  L.n_slots = hier ? (int64_t)a->keep_blocks : L.n_b_cap;
+  L.scores_off = CSA_WS_HEADER_BYTES;
+  L.coarse_off = round_up(L.scores_off + (size_t)L.units * L.n_slots * 4, 256);
+  L.kept_off = round_up(L.coarse_off + (hier ? (size_t)L.units * L.n_super * 4 : 0), 256);
+  L.total = round_up(L.kept_off + (size_t)L.units * L.keep_super * 4, 256);
+  return L;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Attention workspace: [header][partial o][partial (m, l)]
+// ---------------------------------------------------------------------------------------------
+struct AttnLayout {
+  int64_t units;
+  int tiles, splits;
+  size_t o_off, ml_off, total;
+};
+
+AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
+  AttnLayout L{};
+  L.units = batch * a->n_query;
+  L.tiles = (int)(ceil_div(a->top_k, kBlockEntries) + ceil_div(a->window, 64));
+  // one CTA per SM: split the row list so that the grid covers the SMs about once
+  int64_t splits = L.units > 0 ? num_sms / L.units : 1;
+  if (splits > L.tiles) splits = L.tiles;
+  if (splits < 1) splits = 1;
+  L.splits = (int)splits;
+  L.o_off = CSA_WS_HEADER_BYTES;
+  const size_t parts = L.splits > 1 ? (size_t)L.units * L.splits * a->heads : 0;
+  L.ml_off = round_up(L.o_off + parts * kLatent * 4, 256);
+  L.total = round_up(L.ml_off + parts * 2 * 4, 256);
+  return L;
+}
+
+csa_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr) return CSA_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return CSA_ERR_ALIGNMENT;
+  if (ws_bytes < need) return CSA_ERR_WORKSPACE_TOO_SMALL;
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Kernel timing
+// ---------------------------------------------------------------------------------------------
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<ProfRecord> recs;
+  size_t max_records = 0;
+  int64_t dropped = 0;
+  bool pending = false;
+  ProfRecord cur{};
+};
+Profiler g_prof;
+
+}  // namespace
+
+namespace csa {
+
+void prof_begin(const char* name, cudaStream_t s) {
+  if (!g_prof.on) return;
+  if (g_prof.recs.size() >= g_prof.max_records) { ++g_prof.dropped; g_prof.pending = false; return; }
+  const size_t i = g_prof.recs.size();
+  g_prof.cur = ProfRecord{name, g_prof.pool[2 * i], g_prof.pool[2 * i + 1]};
+  cudaEventRecordWithFlags(g_prof.cur.start, s, cudaEventRecordExternal);
+  g_prof.pending = true;
+}
+
+void prof_end(cudaStream_t s) {
+  if (!g_prof.on || !g_prof.pending) return;
+  cudaEventRecordWithFlags(g_prof.cur.stop, s, cudaEventRecordExternal);
+  g_prof.recs.push_back(g_prof.cur);
+  g_prof.pending = false;
+}
+
+}  // namespace csa
+
+extern "C" {
+
+int csa_abi_version(void) { return CSA_ABI_VERSION; }
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case CSA_ERR_UNSUPPORTED_DEVICE: return "unsupported device (sm_103 required)";
+    case CSA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case CSA_ERR_CUDA: return "CUDA runtime error";
+    case CSA_ERR_DEVICE_CHECK: return "device-side check failed (invalid index or size in device data)";
+    case CSA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t csa_entry_bytes(int dim) { return (dim > 0 && dim % kGroup == 0) ? (size_t)entry_bytes(dim) : 0; }
+size_t csa_block_bytes(int dim) { return (dim > 0 && dim % kGroup == 0) ? (size_t)block_bytes(dim) : 0; }
+
+csa_status csa_workspace_reset(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  return cudaMemsetAsync(ws, 0, CSA_WS_HEADER_BYTES, stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+csa_status csa_get_device_status(void* ws, cudaStream_t stream) {
+  if (ws == nullptr) return CSA_ERR_INVALID_ARG;
+  uint32_t hdr[4] = {0, 0, 0, 0};
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaMemcpy(hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (hdr[0] != 0u) {
+    if (cudaMemset(ws, 0, CSA_WS_HEADER_BYTES) != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  switch (hdr[0]) {
+    case 0: return CSA_OK;
+    case CSA_ERR_TIMEOUT: return CSA_ERR_TIMEOUT;
+    default: return CSA_ERR_DEVICE_CHECK;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (a == nullptr || batch < 0) return CSA_ERR_INVALID_ARG;
+  if (a->x_dtype != CSA_DTYPE_BF16 && a->x_dtype != CSA_DTYPE_F32) return CSA_ERR_INVALID_ARG;
+  if (a->merge != 1 && a->merge != 2) return CSA_ERR_INVALID_ARG;
+  if (a->scale_rule != CSA_SCALE_AMAX && a->scale_rule != CSA_SCALE_POW2) return CSA_ERR_INVALID_ARG;
+  if (a->dim <= 0 || a->dim % 64 != 0 || a->dim > 1024) return CSA_ERR_INVALID_ARG;
+  if (a->n_tokens < 0 || a->max_entries < 0) return CSA_ERR_INVALID_ARG;
+  if (batch > 65535) return CSA_ERR_INVALID_ARG;
+  csa_status st = current_device(nullptr);
+  if (st != CSA_OK) return st;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  const int64_t n_new = a->n_tokens / a->merge;
+  if (batch == 0 || n_new == 0) return CSA_OK;
+  if (a->x == nullptr || a->cache == nullptr) return CSA_ERR_INVALID_ARG;
+  const int esz = a->x_dtype == CSA_DTYPE_BF16 ? 2 : 4;
+  if (!aligned(a->x, 16) || !aligned(a->cache, 16)) return CSA_ERR_ALIGNMENT;
+  if ((a->x_stride_t * esz) % 16 != 0 || (a->x_stride_b * esz) % 16 != 0 || a->cache_stride_b % 16 != 0)
+    return CSA_ERR_ALIGNMENT;
+  if (a->x_stride_t < a->dim) return CSA_ERR_INVALID_ARG;
+  const int64_t cap_bytes = ceil_div(a->max_entries, kBlockEntries) * block_bytes(a->dim);
+  if (batch > 1 && a->cache_stride_b < cap_bytes) return CSA_ERR_INVALID_ARG;
+  const int64_t per_super = (int64_t)kSuper * kBlockEntries;
+  const int64_t n_super = ceil_div(a->max_entries, per_super);
+  if (a->coarse_sum != nullptr) {
+    if (!aligned(a->coarse_sum, 16)) return CSA_ERR_ALIGNMENT;
+    if (batch > 1 && a->coarse_stride_b < n_super * a->dim) return CSA_ERR_INVALID_ARG;
+    if (ceil_div(n_new, per_super) + 1 > 65535) return CSA_ERR_INVALID_ARG;
+  }
+
+  PackParams p{};
+  p.x = a->x; p.x_dtype = a->x_dtype; p.dim = a->dim; p.merge = a->merge; p.scale_rule = a->scale_rule;
+  p.x_stride_b = a->x_stride_b; p.x_stride_t = a->x_stride_t; p.n_new = n_new; p.batch = batch;
+  p.max_entries = a->max_entries; p.first_entry = a->first_entry;
+  p.cache = a->cache; p.cache_stride_b = a->cache_stride_b;
+  p.coarse_sum = a->coarse_sum; p.coarse_stride_b = a->coarse_stride_b;
+  p.hdr = static_cast<uint32_t*>(ws);
+  if (launch_pack(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (launch_coarse_sum(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+static csa_status validate_index(int64_t batch, const csa_index_args* a) {
+  if (a == nullptr || batch < 0) return CSA_ERR_INVALID_ARG;
+  if (a->n_query < 1 || a->max_entries < 0) return CSA_ERR_INVALID_ARG;
+  if (a->heads != 1 && a->heads != 2 && a->heads != 4 && a->heads != 8) return CSA_ERR_INVALID_ARG;
+  if (a->dim != 64 && a->dim != 128 && a->dim != 256) return CSA_ERR_INVALID_ARG;
+  if (a->top_k < 1 || a->top_k > CSA_MAX_TOP_K) return CSA_ERR_INVALID_ARG;
+  if ((a->flags & ~(CSA_IDX_RELU | CSA_IDX_HIER)) != 0) return CSA_ERR_INVALID_ARG;
+  const bool hier = (a->flags & CSA_IDX_HIER) != 0;
+  if (hier) {
+    if (a->q_pos != nullptr || a->coarse_sum == nullptr) return CSA_ERR_INVALID_ARG;
+    if (a->keep_blocks < kSuper || a->keep_blocks % kSuper != 0 || a->keep_blocks > 4096) return CSA_ERR_INVALID_ARG;
+    if (!aligned(a->coarse_sum, 16)) return CSA_ERR_ALIGNMENT;
+  }
+  const int64_t units_y = hier ? batch * a->n_query : batch;
+  if (units_y > 65535) return CSA_ERR_INVALID_ARG;
+  if (batch == 0) return CSA_OK;
+  if (a->q_idx == nullptr || a->keys == nullptr || a->n_entries == nullptr || a->out_idx == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned(a->q_idx, 16) || !aligned(a->keys, 16) || a->keys_stride_b % 16 != 0) return CSA_ERR_ALIGNMENT;
+  if (batch > 1 && a->keys_stride_b < ceil_div(a->max_entries, kBlockEntries) * block_bytes(a->dim))
+    return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* a) {
+  if (a == nullptr || batch < 0) return 0;
+  return index_layout(batch, a).total;
+}
+
+csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  csa_status st = validate_index(batch, a);
+  if (st != CSA_OK) return st;
+  int num_sms = 0;
+  st = current_device(&num_sms);
+  if (st != CSA_OK) return st;
+  const IndexLayout L = index_layout(batch, a);
+  st = check_ws(ws, ws_bytes, L.total);
+  if (st != CSA_OK) return st;
+  if (batch == 0) return CSA_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint32_t* hdr = reinterpret_cast<uint32_t*>(w);
+  const bool hier = (a->flags & CSA_IDX_HIER) != 0;
+  const bool relu = (a->flags & CSA_IDX_RELU) != 0;
+  float* scores = reinterpret_cast<float*>(w + L.scores_off);
+  int32_t* kept = reinterpret_cast<int32_t*>(w + L.kept_off);
+
+  if (hier) {
+    CoarseScoreParams cp{};
+    cp.q_idx = a->q_idx; cp.head_w = a->head_w; cp.n_query = a->n_query; cp.heads = a->heads; cp.dim = a->dim;
+    cp.relu = relu; cp.coarse = a->coarse_sum; cp.coarse_stride_b = a->coarse_stride_b;
+    cp.n_entries = a->n_entries; cp.n_super = L.n_super;
+    cp.scores = reinterpret_cast<float*>(w + L.coarse_off); cp.batch = batch;
+    if (launch_coarse_score(cp, stream) != cudaSuccess) return CSA_ERR_CUDA;
+    TopkParams tk{};
+    tk.scores = cp.scores; tk.score_stride = L.n_super; tk.n = L.n_super; tk.k = (int)L.keep_super;
+    tk.out = kept; tk.out_stride = L.keep_super; tk.units = L.units; tk.hdr = hdr;
+    if (launch_topk(tk, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  }
+
+  ScoreParams sp{};
+  sp.q_idx = a->q_idx; sp.head_w = a->head_w; sp.n_query = a->n_query; sp.heads = a->heads; sp.dim = a->dim;
+  sp.relu = relu; sp.keys = a->keys; sp.keys_stride_b = a->keys_stride_b; sp.n_entries = a->n_entries;
+  sp.max_entries = a->max_entries; sp.q_pos = a->q_pos;
+  sp.kept = hier ? kept : nullptr; sp.keep_super = (int)L.keep_super;
+  sp.scores = scores; sp.score_stride = L.n_slots; sp.n_slots = L.n_slots; sp.batch = batch; sp.hdr = hdr;
+  if (launch_index_score(sp, num_sms, stream) != cudaSuccess) return CSA_ERR_CUDA;
+
+  TopkParams tk{};
+  tk.scores = scores; tk.score_stride = L.n_slots; tk.n = L.n_slots; tk.k = a->top_k;
+  tk.out = a->out_idx; tk.out_stride = a->top_k; tk.units = L.units; tk.hdr = hdr;
+  if (hier) { tk.map_super = kept; tk.map_stride = (int)L.keep_super; }
+  if (launch_topk(tk, stream) != cudaSuccess) return CSA_ERR_CUDA;
+
+  if (a->out_block_scores != nullptr && !hier) {
+    if (cudaMemcpyAsync(a->out_block_scores, scores, (size_t)L.units * L.n_slots * 4, cudaMemcpyDeviceToDevice,
+                        stream) != cudaSuccess)
+      return CSA_ERR_CUDA;
+  }
+  return CSA_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
+static csa_status validate_attn(int64_t batch, const csa_attn_args* a, bool prefill) {
+  if (a == nullptr || batch < 0) return CSA_ERR_INVALID_ARG;
+  if (a->n_query < 1 || a->max_entries < 0) return CSA_ERR_INVALID_ARG;
+  if (a->heads != 16 && a->heads != 32 && a->heads != 48 && a->heads != 64) return CSA_ERR_INVALID_ARG;
+  if (a->top_k < 1 || a->top_k > CSA_MAX_TOP_K) return CSA_ERR_INVALID_ARG;
+  if (a->window < 0 || a->window > 1024) return CSA_ERR_INVALID_ARG;
+  if (!(a->scale > 0.0f) || a->scale != a->scale) return CSA_ERR_INVALID_ARG;
+  if (batch * a->n_query > 65535) return CSA_ERR_INVALID_ARG;
+  if (batch == 0) return CSA_OK;
+  if (a->q == nullptr || a->cache == nullptr || a->n_entries == nullptr || a->idx == nullptr || a->out == nullptr)
+    return CSA_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->cache, 16) || a->cache_stride_b % 16 != 0 || !aligned(a->out, 16))
+    return CSA_ERR_ALIGNMENT;
+  if (batch > 1 && a->cache_stride_b < ceil_div(a->max_entries, kBlockEntries) * block_bytes(kLatent))
+    return CSA_ERR_INVALID_ARG;
+  if (a->window > 0) {
+    if (a->swa == nullptr || a->swa_rows < 0) return CSA_ERR_INVALID_ARG;
+    if (!aligned(a->swa, 16) || (a->swa_stride_b * 2) % 16 != 0) return CSA_ERR_ALIGNMENT;
+    if (batch > 1 && a->swa_stride_b < a->swa_rows * kLatent) return CSA_ERR_INVALID_ARG;
+    if (prefill ? a->swa_first_pos == nullptr : a->swa_len == nullptr) return CSA_ERR_INVALID_ARG;
+  }
+  if (prefill && a->q_pos == nullptr) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* a) {
+  if (a == nullptr || batch < 0) return 0;
+  int num_sms = 0;
+  if (current_device(&num_sms) != CSA_OK) num_sms = 148;
+  return attn_layout(batch, a, num_sms).total;
+}
+
+static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream,
+                              bool prefill) {
+  csa_status st = validate_attn(batch, a, prefill);
+  if (st != CSA_OK) return st;
+  int num_sms = 0;
+  st = current_device(&num_sms);
+  if (st != CSA_OK) return st;
+  const AttnLayout L = attn_layout(batch, a, num_sms);
+  st = check_ws(ws, ws_bytes, L.total);
+  if (st != CSA_OK) return st;
+  if (batch == 0) return CSA_OK;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  AttnParams p{};
+  p.units = L.units; p.n_query = a->n_query; p.heads = a->heads;
+  p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.q = static_cast<const __nv_bfloat16*>(a->q);
+  p.cache = a->cache; p.cache_stride_b = a->cache_stride_b; p.n_entries = a->n_entries;
+  p.max_entries = a->max_entries; p.idx = a->idx; p.top_k = a->top_k; p.window = a->window;
+  p.q_pos = prefill ? a->q_pos : nullptr;
+  p.swa = static_cast<const __nv_bfloat16*>(a->swa); p.swa_stride_b = a->swa_stride_b; p.swa_rows = a->swa_rows;
+  p.swa_len = a->swa_len; p.swa_first_pos = a->swa_first_pos;
+  p.splits = L.splits; p.tiles = L.tiles;
+  p.part_o = reinterpret_cast<float*>(w + L.o_off);
+  p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
+  p.out = a->out; p.out_lse = a->out_lse;
+  p.hdr = reinterpret_cast<uint32_t*>(w);
+  if (launch_attn(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (launch_combine(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  return sparse_attn(batch, a, ws, ws_bytes, stream, false);
+}
+
+csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream) {
+  return sparse_attn(batch, a, ws, ws_bytes, stream, true);
+}
+
+// ------------------------------------------------------------------------------------------------
+csa_status csa_profile_begin(int max_launches) {
+  if (max_launches < 1 || max_launches > (1 << 20)) return CSA_ERR_INVALID_ARG;
+  if (g_prof.on) return CSA_ERR_INVALID_ARG;
+  for (auto e : g_prof.pool) cudaEventDestroy(e);
+  g_prof.pool.assign(2 * (size_t)max_launches, nullptr);
+  for (auto& e : g_prof.pool)
+    if (cudaEventCreate(&e) != cudaSuccess) return CSA_ERR_CUDA;
+  g_prof.recs.clear();
+  g_prof.recs.reserve(max_launches);
+  g_prof.max_records = max_launches;
+  g_prof.dropped = 0;
+  g_prof.pending = false;
+  g_prof.on = true;
+  return CSA_OK;
+}
+
+csa_status csa_profile_end(csa_kernel_time* out, int max_out, int* n_out, int64_t* dropped) {
+  if (!g_prof.on) return CSA_ERR_INVALID_ARG;
+  g_prof.on = false;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CSA_ERR_CUDA;
+  std::vector<csa_kernel_time> agg;
+  for (const auto& r : g_prof.recs) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) return CSA_ERR_CUDA;
+    size_t i = 0;
+    for (; i < agg.size(); ++i)
+      if (std::strncmp(agg[i].name, r.name, sizeof(agg[i].name)) == 0) break;
+    if (i == agg.size()) {
+      csa_kernel_time t{};
+      std::strncpy(t.name, r.name, sizeof(t.name) - 1);
+      agg.push_back(t);
+    }
+    agg[i].launches += 1;
+    agg[i].total_ms += ms;
+  }
+  const int n = (int)agg.size() < max_out ? (int)agg.size() : max_out;
+  for (int i = 0; i < n; ++i) out[i] = agg[i];
+  if (n_out) *n_out = n;
+  if (dropped) *dropped = g_prof.dropped;
+  g_prof.recs.clear();
+  return CSA_OK;
+}
+
+}  // extern "C"

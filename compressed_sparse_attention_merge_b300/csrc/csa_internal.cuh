@@ -1,0 +1,189 @@
+// Internal declarations shared by the kernels and the C-ABI layer of the CSA2 library.
+// Device helpers here implement the cache format stated in include/csa.h (E2M1 codes, one E4M3
+// scale per 16 elements, block-major layout) from the format definitions themselves.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+// ------------------------------------------------------------------------------------------------
+// Workspace header: word 0 = first status code recorded, 1 = kernel id, 2 = detail, 3 = count.
+// ------------------------------------------------------------------------------------------------
+enum KernelId : uint32_t {
+  KID_PACK = 1,
+  KID_COARSE_SUM = 2,
+  KID_INDEX_SCORE = 3,
+  KID_COARSE_SCORE = 4,
+  KID_TOPK = 5,
+  KID_ATTN = 6,
+  KID_COMBINE = 7,
+};
+
+__device__ __forceinline__ void report(uint32_t* hdr, uint32_t code, uint32_t kernel, uint32_t detail) {
+  if (atomicCAS(hdr, 0u, code) == 0u) {
+    hdr[1] = kernel;
+    hdr[2] = detail;
+  }
+  atomicAdd(hdr + 3, 1u);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Format helpers
+// ------------------------------------------------------------------------------------------------
+constexpr int kBlockEntries = CSA_BLOCK_ENTRIES;
+constexpr int kGroup = CSA_SCALE_GROUP;
+constexpr int kLatent = CSA_LATENT_DIM;
+constexpr int kSuper = CSA_SUPER_BLOCK;
+
+__host__ __device__ constexpr int entry_bytes(int dim) { return dim / 2 + dim / kGroup; }
+__host__ __device__ constexpr int block_bytes(int dim) { return kBlockEntries * entry_bytes(dim); }
+
+// Two E2M1 codes (low nibble = first element) -> f16x2 (first element in the low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(byte));
+  return out;
+}
+
+// One E4M3 byte -> f16x2 holding the value twice (every E4M3 value is exact in fp16).
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
+  uint32_t out;
+  const uint16_t pair = (uint16_t)((byte & 0xFFu) | ((byte & 0xFFu) << 8));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(pair));
+  return out;
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  const uint32_t h2 = e4m3_to_f16x2_bcast(byte);
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// Non-negative fp32 -> E4M3 byte, round to nearest even, saturating at 448. Both halves of the
+// converted pair receive x, so the low byte is the result whichever half the instruction fills first.
+__device__ __forceinline__ uint32_t float_to_e4m3_satfinite(float x) {
+  uint16_t out;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(out) : "f"(x));
+  return out & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch parameter blocks (host -> kernel launchers)
+// ------------------------------------------------------------------------------------------------
+struct PackParams {
+  const void* x;
+  int x_dtype, dim, merge, scale_rule;
+  int64_t x_stride_b, x_stride_t, n_new, batch, max_entries;
+  const int32_t* first_entry;
+  uint8_t* cache;
+  int64_t cache_stride_b;
+  float* coarse_sum;
+  int64_t coarse_stride_b;
+  uint32_t* hdr;
+};
+
+struct ScoreParams {
+  // queries
+  const float* q_idx;          // [batch][n_query][heads][dim]
+  const float* head_w;         // [heads] or null
+  int64_t n_query;
+  int heads, dim, relu;
+  // keys
+  const uint8_t* keys;
+  int64_t keys_stride_b;
+  const int32_t* n_entries;
+  int64_t max_entries;
+  const int32_t* q_pos;        // [batch][n_query] or null
+  // hierarchical restriction: per unit list of kept super-blocks (null in flat mode)
+  const int32_t* kept;         // [units][keep_super]
+  int keep_super;
+  // output: per unit block scores
+  float* scores;               // [units][score_stride]
+  int64_t score_stride;
+  int64_t n_slots;             // blocks (flat) or compact slots (hierarchical) per unit
+  int64_t batch;
+  uint32_t* hdr;
+};
+
+struct CoarseScoreParams {
+  const float* q_idx;
+  const float* head_w;
+  int64_t n_query;
+  int heads, dim, relu;
+  const float* coarse;
+  int64_t coarse_stride_b;
+  const int32_t* n_entries;
+  int64_t n_super;
+  float* scores;               // [units][n_super]
+  int64_t batch;
+};
+
+struct TopkParams {
+  const float* scores;         // [units][score_stride]
+  int64_t score_stride;
+  int64_t n;                   // candidates per unit
+  int k;
+  int32_t* out;                // [units][out_stride]
+  int64_t out_stride;
+  const int32_t* map_super;    // hierarchical: slot s -> map_super[unit][s / 64] * 64 + s % 64
+  int map_stride;
+  int64_t units;
+  uint32_t* hdr;
+};
+
+struct AttnParams {
+  int64_t units, n_query;
+  int heads;
+  float scale_log2;            // softmax scale * log2(e)
+  const __nv_bfloat16* q;      // [units][heads][512]
+  const uint8_t* cache;
+  int64_t cache_stride_b;
+  const int32_t* n_entries;
+  int64_t max_entries;
+  const int32_t* idx;          // [units][top_k]
+  int top_k, window;
+  const int32_t* q_pos;        // [units] or null (decode)
+  const __nv_bfloat16* swa;
+  int64_t swa_stride_b, swa_rows;
+  const int32_t* swa_len;
+  const int32_t* swa_first_pos;
+  int splits, tiles;           // tiles = ceil(top_k/8) + ceil(window/64)
+  float* part_o;               // [units][splits][heads][512]
+  float* part_ml;              // [units][splits][heads][2]
+  float* out;                  // used when splits == 1
+  float* out_lse;
+  uint32_t* hdr;
+};
+
+// ------------------------------------------------------------------------------------------------
+// Launchers (one per kernel file). Each returns the launch error, if any.
+// ------------------------------------------------------------------------------------------------
+cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
+cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s);
+cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+
+// Kernel timing hooks (defined in csa_api.cu); no-ops unless profiling is on.
+void prof_begin(const char* name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+struct ProfScope {
+  cudaStream_t s;
+  ProfScope(const char* name, cudaStream_t st) : s(st) { prof_begin(name, st); }
+  ~ProfScope() { prof_end(s); }
+};
+
+}  // namespace csa

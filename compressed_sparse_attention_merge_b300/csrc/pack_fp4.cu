@@ -1,0 +1,174 @@
+// Pair-merge + FP4 quantiser + block-major store, and the super-block coarse-key sums.
+//
+// Follows "DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression" (paper-digest), Core
+// Mechanics ("Sequence: the Encoder merges 2 adjacent positions into 1 cache entry") and the FP4 global
+// KV of "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" (card), Key ideas. The numeric
+// format (E2M1 codes, E4M3 scale per 16 elements, amax/6 or power-of-two scale) is this library's own and
+// is stated in include/csa.h; every fp32 step uses an explicit round-to-nearest intrinsic so that the
+// bytes do not depend on contraction or fast-math choices.
+//
+// One thread quantises one 16-element group: a warp covers 32 consecutive groups (a whole 512-d entry),
+// so loads (2 x 32 B or 1 x 32 B per thread) and stores (8 code bytes + 1 scale byte per thread) are
+// contiguous across the warp. The kernel is HBM-bound.
+#include "csa_internal.cuh"
+
+namespace csa {
+namespace {
+
+__device__ __forceinline__ void load16(const void* base, int dtype, int64_t elem_off, float* v) {
+  if (dtype == CSA_DTYPE_BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem_off);
+    uint4 a = __ldg(p), b = __ldg(p + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float4 f = __ldg(p + i);
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+  }
+}
+
+// E2M1 code of y: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 to |y|, ties to the even code (the thresholds
+// alternate between strict and non-strict at the midpoints 0.25, 0.75, ..., 5), saturating at 6; the
+// sign bit copies the sign bit of y.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
+               (a > 5.0f);
+  return c | ((__float_as_uint(y) >> 31) << 3);
+}
+
+// Smallest power of two >= sf (sf > 0), clamped to [2^-9, 256]; returns the E4M3 byte and the value.
+__device__ __forceinline__ uint32_t pow2_scale(float sf, float* value) {
+  const uint32_t bits = __float_as_uint(sf);
+  const int e = (int)((bits >> 23) & 0xFFu);
+  const uint32_t mant = bits & 0x7FFFFFu;
+  int k = (e == 0) ? -126 : (mant == 0u ? e - 127 : e - 126);
+  k = k < -9 ? -9 : (k > 8 ? 8 : k);
+  *value = __uint_as_float((uint32_t)(k + 127) << 23);
+  return k >= -6 ? (uint32_t)(k + 7) << 3 : (0x08u >> (-6 - k));
+}
+
+__global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
+  const int groups = p.dim / kGroup;
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = p.batch * p.n_new * groups;
+  if (t >= total) return;
+  const int g = (int)(t % groups);
+  const int64_t i = (t / groups) % p.n_new;
+  const int64_t b = t / ((int64_t)groups * p.n_new);
+
+  const int64_t first = p.first_entry ? (int64_t)p.first_entry[b] : 0;
+  if (first < 0 || first + p.n_new > p.max_entries) {
+    if (i == 0 && g == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_PACK, (uint32_t)b);
+    return;
+  }
+
+  float m[16];
+  const int64_t row0 = b * p.x_stride_b + (int64_t)g * kGroup;
+  if (p.merge == 2) {
+    float a[16], c[16];
+    load16(p.x, p.x_dtype, row0 + (2 * i) * p.x_stride_t, a);
+    load16(p.x, p.x_dtype, row0 + (2 * i + 1) * p.x_stride_t, c);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m[j] = __fmul_rn(__fadd_rn(a[j], c[j]), 0.5f);
+  } else {
+    load16(p.x, p.x_dtype, row0 + i * p.x_stride_t, m);
+  }
+
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(m[j]));
+  const float sf = __fdiv_rn(amax, 6.0f);
+
+  uint32_t sbyte = 0;
+  float s = 0.0f;
+  if (sf > 0.0f) {
+    if (p.scale_rule == CSA_SCALE_AMAX) {
+      sbyte = float_to_e4m3_satfinite(sf);
+      s = e4m3_to_float(sbyte);
+    } else {
+      sbyte = pow2_scale(sf, &s);
+    }
+  }
+
+  uint32_t lo = 0, hi = 0;
+  if (s > 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t c0 = e2m1_code(__fdiv_rn(m[2 * j], s));
+      const uint32_t c1 = e2m1_code(__fdiv_rn(m[2 * j + 1], s));
+      const uint32_t byte = c0 | (c1 << 4);
+      if (j < 4) lo |= byte << (8 * j); else hi |= byte << (8 * (j - 4));
+    }
+  }
+
+  const int64_t e = first + i;
+  uint8_t* blk = p.cache + b * p.cache_stride_b + (e / kBlockEntries) * (int64_t)block_bytes(p.dim);
+  const int slot = (int)(e % kBlockEntries);
+  *reinterpret_cast<uint2*>(blk + slot * (p.dim / 2) + g * 8) = make_uint2(lo, hi);
+  blk[kBlockEntries * (p.dim / 2) + slot * groups + g] = (uint8_t)sbyte;
+}
+
+// coarse_sum[b][g][d] = fp32 sum, ascending entry order, of the dequantised element d of entries
+// [512 g, min(512 (g + 1), first + n_new)), for every super-block g touched by this call.
+__global__ void __launch_bounds__(128) coarse_sum_kernel(PackParams p, int touched) {
+  const int d = blockIdx.x * blockDim.x + threadIdx.x;
+  const int gl = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  if (d >= p.dim) return;
+  const int64_t first = p.first_entry ? (int64_t)p.first_entry[b] : 0;
+  if (first < 0 || first + p.n_new > p.max_entries || p.n_new == 0) return;
+  const int64_t end = first + p.n_new;
+  const int64_t per_super = (int64_t)kSuper * kBlockEntries;
+  const int64_t g = first / per_super + gl;
+  if (gl >= touched || g * per_super >= end) return;
+  const int64_t e_hi = (g + 1) * per_super < end ? (g + 1) * per_super : end;
+
+  const uint8_t* seq = p.cache + b * p.cache_stride_b;
+  const int bb = block_bytes(p.dim);
+  const int half = p.dim / 2, groups = p.dim / kGroup;
+  const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+  float acc = 0.0f;
+  for (int64_t e = g * per_super; e < e_hi; ++e) {
+    const uint8_t* blk = seq + (e / kBlockEntries) * bb;
+    const int slot = (int)(e % kBlockEntries);
+    const uint32_t byte = blk[slot * half + d / 2];
+    const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 0xFu);
+    const float sc = e4m3_to_float(blk[kBlockEntries * half + slot * groups + d / kGroup]);
+    const float v = __fmul_rn((code & 8u) ? -mag[code & 7u] : mag[code & 7u], sc);
+    acc = __fadd_rn(acc, v);
+  }
+  p.coarse_sum[b * p.coarse_stride_b + g * p.dim + d] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
+  const int64_t total = p.batch * p.n_new * (p.dim / kGroup);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  ProfScope prof("pack_fp4", s);
+  pack_fp4_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s) {
+  if (p.coarse_sum == nullptr || p.n_new == 0 || p.batch == 0) return cudaSuccess;
+  const int64_t per_super = (int64_t)kSuper * kBlockEntries;
+  const int touched = (int)((p.n_new + per_super - 1) / per_super) + 1;
+  dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)touched, (unsigned)p.batch);
+  ProfScope prof("coarse_sum", s);
+  coarse_sum_kernel<<<grid, 128, 0, s>>>(p, touched);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -123,13 +123,17 @@ def scale_bytes(amax, rule):
     return np.where(sf == 0, 0, out).astype(np.uint8)
 
 
-def quantize(m, rule):
+def quantize(m, rule, rows_per_chunk=4096):
     """Quantise rows m (float32 [n, dim], dim % 16 == 0). Returns (codes uint8 [n, dim] one code per
-    element, scales uint8 [n, dim // 16])."""
+    element, scales uint8 [n, dim // 16]). Rows are independent; large inputs are processed a chunk of
+    rows at a time only to bound the temporary memory of the brute-force search."""
     m = np.asarray(m, dtype=np.float32)
     n, dim = m.shape
     if dim % GROUP:
         raise ValueError("dim must be a multiple of 16")
+    if n > rows_per_chunk:
+        parts = [quantize(m[i:i + rows_per_chunk], rule, rows_per_chunk) for i in range(0, n, rows_per_chunk)]
+        return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
     g = m.reshape(n, dim // GROUP, GROUP)
     amax = np.abs(g).max(axis=-1)
     sb = scale_bytes(amax, rule)
@@ -159,13 +163,13 @@ def layout(codes, scales, first_entry=0, n_blocks=None, base=None):
     if n_blocks is None:
         n_blocks = -(-last // BLOCK)
     out = np.zeros((n_blocks, block_bytes(dim)), np.uint8) if base is None else base.copy()
-    packed = (codes[:, 0::2] & 0xF) | ((codes[:, 1::2] & 0xF) << 4)
-    for i in range(n):
-        e = first_entry + i
-        blk, slot = divmod(e, BLOCK)
-        out[blk, slot * half:(slot + 1) * half] = packed[i]
-        off = BLOCK * half + slot * nsc
-        out[blk, off:off + nsc] = scales[i]
+    packed = ((codes[:, 0::2] & 0xF) | ((codes[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+    e = first_entry + np.arange(n)
+    blk, slot = e // BLOCK, e % BLOCK
+    code_cols = slot[:, None] * half + np.arange(half)[None, :]
+    out[blk[:, None], code_cols] = packed
+    scale_cols = BLOCK * half + slot[:, None] * nsc + np.arange(nsc)[None, :]
+    out[blk[:, None], scale_cols] = scales
     return out
 
 
@@ -180,16 +184,14 @@ def pack(x, merge, rule, first_entry=0, n_blocks=None, base=None):
 def unpack(blocks, dim, n_entries):
     """Inverse of layout: returns (codes [n_entries, dim], scales [n_entries, dim // 16])."""
     half, nsc = dim // 2, dim // GROUP
+    e = np.arange(n_entries)
+    blk, slot = e // BLOCK, e % BLOCK
+    packed = blocks[blk[:, None], slot[:, None] * half + np.arange(half)[None, :]]
     codes = np.zeros((n_entries, dim), np.uint8)
-    scales = np.zeros((n_entries, nsc), np.uint8)
-    for e in range(n_entries):
-        blk, slot = divmod(e, BLOCK)
-        packed = blocks[blk, slot * half:(slot + 1) * half]
-        codes[e, 0::2] = packed & 0xF
-        codes[e, 1::2] = packed >> 4
-        off = BLOCK * half + slot * nsc
-        scales[e] = blocks[blk, off:off + nsc]
-    return codes, scales
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    scales = blocks[blk[:, None], BLOCK * half + slot[:, None] * nsc + np.arange(nsc)[None, :]]
+    return codes, scales.astype(np.uint8)
 
 
 def dequantize(blocks, dim, n_entries):

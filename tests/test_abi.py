@@ -1,0 +1,87 @@
+"""The C-ABI library loads and exports every symbol include/csa.h declares; host-side validation that
+needs no GPU rejects bad arguments before touching the device. No compute call runs here."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from compressed_sparse_attention_merge_b300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(csa_[a-z0-9_]+)\s*\(", text))
+    return sorted(n for n in names if not n.endswith("_t"))
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("csa_pack_fp4", "csa_index_topk", "csa_sparse_attn_decode", "csa_sparse_attn_prefill"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    path = lib._name
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (csa_[a-z0-9_]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_constants_and_strings(lib):
+    assert lib.csa_abi_version() == 1
+    assert lib.csa_entry_bytes(512) == 288 and lib.csa_block_bytes(512) == 2304
+    assert lib.csa_block_bytes(128) == 576 and lib.csa_block_bytes(64) == 288
+    assert lib.csa_entry_bytes(10) == 0
+    for s in range(8):
+        assert lib.csa_status_string(s)
+    assert b"unknown" in lib.csa_status_string(99)
+
+
+def test_validation_rejects_before_any_device_call(lib):
+    from compressed_sparse_attention_merge_b300 import binding as b
+    # null argument blocks
+    assert lib.csa_pack_fp4(1, None, None, 0, None) == b.ERR_INVALID_ARG
+    assert lib.csa_index_topk(1, None, None, 0, None) == b.ERR_INVALID_ARG
+    assert lib.csa_sparse_attn_decode(1, None, None, 0, None) == b.ERR_INVALID_ARG
+    pa = b.PackArgs()
+    pa.x_dtype, pa.dim, pa.merge, pa.scale_rule = 0, 100, 2, 0       # dim not a multiple of 64
+    assert lib.csa_pack_fp4(1, ctypes.byref(pa), None, 0, None) == b.ERR_INVALID_ARG
+    # unsupported indexer shape / attention head count
+    ia = b.IndexArgs()
+    ia.n_query, ia.heads, ia.dim, ia.top_k, ia.flags = 1, 3, 128, 8, b.IDX_RELU
+    assert lib.csa_index_topk(1, ctypes.byref(ia), None, 0, None) == b.ERR_INVALID_ARG
+    ia.heads, ia.top_k = 4, 5000
+    assert lib.csa_index_topk(1, ctypes.byref(ia), None, 0, None) == b.ERR_INVALID_ARG
+    ia.top_k, ia.flags = 8, b.IDX_RELU | b.IDX_HIER      # hierarchical without coarse keys
+    assert lib.csa_index_topk(1, ctypes.byref(ia), None, 0, None) == b.ERR_INVALID_ARG
+    aa = b.AttnArgs()
+    aa.n_query, aa.heads, aa.top_k, aa.window, aa.scale = 1, 20, 8, 128, 0.04
+    assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
+    aa.heads, aa.scale = 64, -1.0
+    assert lib.csa_sparse_attn_prefill(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
+
+
+def test_workspace_sizes_are_host_only(lib):
+    from compressed_sparse_attention_merge_b300 import binding as b
+    ia = b.IndexArgs()
+    ia.n_query, ia.heads, ia.dim, ia.top_k, ia.flags, ia.max_entries = 1, 4, 128, 256, b.IDX_RELU, 32768
+    n = lib.csa_index_topk_workspace_size(32, ctypes.byref(ia))
+    assert n >= 256 + 32 * 4096 * 4 and n % 256 == 0
+    ia.flags, ia.keep_blocks, ia.max_entries = b.IDX_RELU | b.IDX_HIER, 2048, 1 << 19
+    n = lib.csa_index_topk_workspace_size(4, ctypes.byref(ia))
+    assert n >= 256 + 4 * 2048 * 4 + 4 * 1024 * 4 + 4 * 32 * 4
