@@ -1,0 +1,196 @@
+"""csa_sparse_attn_decode / csa_sparse_attn_prefill against the fp64 oracle (max-abs 2e-3, max-rel 1e-2),
+split-K against no split, empty and invalid inputs."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as o_attn
+from oracle import fp4 as o_fp4
+
+from _pipeline import (SCALE, assert_attn_close, assert_lse_close, gpu_decode_attn, gpu_pack_sequences,
+                       gpu_prefill_attn, to_np)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def csa():
+    from compressed_sparse_attention_merge_b300 import binding
+    binding.lib()
+    return binding
+
+
+def _latents(g, B, T, outliers=0.01):
+    x = torch.randn(B, T, 512, generator=g, device=DEV)
+    x = torch.where(torch.rand(B, T, 512, generator=g, device=DEV) < outliers, x * 8, x)
+    return x.to(torch.bfloat16)
+
+
+def _random_idx(rng, n_b_list, B, Q, K, cap_blocks):
+    idx = np.full((B, Q, K), -1, np.int32)
+    for b in range(B):
+        for j in range(Q):
+            nb = n_b_list[b]
+            k = min(K, nb)
+            take = rng.choice(max(nb, 1), size=k, replace=False) if nb else np.zeros(0, np.int64)
+            idx[b, j, :k] = take
+            # a legal id past this sequence's valid blocks (inside capacity): must be ignored
+            if k < K and nb < cap_blocks:
+                idx[b, j, k] = cap_blocks - 1
+    return idx
+
+
+@pytest.mark.parametrize("heads,top_k,batch", [(64, 24, 3), (16, 64, 3), (32, 40, 2), (64, 16, 150)])
+def test_decode_matches_oracle(csa, heads, top_k, batch):
+    g = torch.Generator(device=DEV).manual_seed(100 + heads + top_k + batch)
+    rng = np.random.default_rng(heads * 1000 + top_k + batch)
+    base = [2000, 74, 1401, 1]
+    tokens = [base[i % 4] + (i // 4) * 2 for i in range(batch)]
+    B, T = batch, max(tokens)
+    E = T // 2
+    W = 128
+    x = _latents(g, B, T)
+    q = torch.randn(B, 1, heads, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa = torch.randn(B, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa_len = torch.tensor([[128, 5, 0, 77][i % 4] for i in range(B)], dtype=torch.int32, device=DEV)
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, tokens, E, 512, 2, csa.SCALE_AMAX, ws)
+    n_e = [t // 2 for t in tokens]
+    n_entries = torch.tensor(n_e, dtype=torch.int32, device=DEV)
+    idx_np = _random_idx(rng, [-(-n // 8) for n in n_e], B, 1, top_k, -(-E // 8))
+    idx = torch.from_numpy(idx_np).to(DEV)
+    out, lse = gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, E, W)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    xf, qf, sf = to_np(x), to_np(q), to_np(swa)
+    check = range(B) if B <= 8 else list(range(4)) + [B - 1]
+    for b in check:
+        entries = o_fp4.dequantize(o_fp4.pack(xf[b, :tokens[b]], 2, "amax", n_blocks=-(-E // 8)), 512, E)
+        ref, ref_lse = o_attn.decode_attention(qf[b, 0].astype(np.float64), entries, n_e[b], idx_np[b, 0],
+                                               sf[b, :int(swa_len[b])], SCALE)
+        assert_attn_close(out[b, 0], ref, f"seq {b}")
+        assert_lse_close(lse[b, 0], ref_lse, f"seq {b}")
+
+
+def test_split_and_unsplit_agree(csa):
+    # the same query attended once as a lone sequence (many splits) and inside a batch of 148 (no split)
+    g = torch.Generator(device=DEV).manual_seed(7)
+    B, T, W, K = 148, 1200, 128, 64
+    E = T // 2
+    x = _latents(g, 1, T).expand(B, T, 512).contiguous()
+    q = torch.randn(1, 1, 64, 512, generator=g, device=DEV).to(torch.bfloat16).expand(B, 1, 64, 512).contiguous()
+    swa = torch.randn(1, W, 512, generator=g, device=DEV).to(torch.bfloat16).expand(B, W, 512).contiguous()
+    swa_len = torch.full((B,), W, dtype=torch.int32, device=DEV)
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T] * B, E, 512, 2, csa.SCALE_AMAX, ws)
+    n_entries = torch.full((B,), E, dtype=torch.int32, device=DEV)
+    idx = torch.arange(K, dtype=torch.int32, device=DEV).view(1, 1, K).expand(B, 1, K).contiguous()
+    many, lse_many = gpu_decode_attn(csa, q[:1], cache[:1], n_entries[:1], idx[:1], swa[:1], swa_len[:1], E, W)
+    one, lse_one = gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, E, W)
+    assert torch.allclose(many[0], one[0], atol=1e-5, rtol=0)
+    assert torch.allclose(lse_many[0], lse_one[0], atol=1e-5, rtol=0)
+    assert torch.equal(one[0], one[B - 1])
+
+
+def test_topk_covering_everything_equals_dense(csa):
+    g = torch.Generator(device=DEV).manual_seed(8)
+    T, W = 2 * 203, 128
+    E = T // 2
+    x = _latents(g, 1, T)
+    q = torch.randn(1, 1, 64, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa = torch.randn(1, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T], E, 512, 2, csa.SCALE_AMAX, ws)
+    nb = -(-E // 8)
+    idx = torch.tensor(list(range(nb - 1, -1, -1)) + [-1] * 3, dtype=torch.int32, device=DEV).view(1, 1, -1)
+    out, lse = gpu_decode_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV), idx, swa,
+                               torch.tensor([W], dtype=torch.int32, device=DEV), E, W)
+    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    ref, ref_lse = o_attn.dense_attention(to_np(q)[0, 0].astype(np.float64), entries, E, to_np(swa)[0], SCALE)
+    assert_attn_close(out[0, 0].cpu().numpy(), ref)
+    assert_lse_close(lse[0, 0].cpu().numpy(), ref_lse)
+
+
+def test_zero_query_is_mean_of_rows(csa):
+    g = torch.Generator(device=DEV).manual_seed(9)
+    T, W = 2 * 64, 128
+    E = T // 2
+    x = _latents(g, 1, T)
+    q = torch.zeros(1, 1, 16, 512, dtype=torch.bfloat16, device=DEV)
+    swa = torch.randn(1, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T], E, 512, 2, csa.SCALE_AMAX, ws)
+    idx = torch.arange(8, dtype=torch.int32, device=DEV).view(1, 1, 8)
+    out, lse = gpu_decode_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV), idx, swa,
+                               torch.tensor([10], dtype=torch.int32, device=DEV), E, W)
+    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    rows = np.concatenate([entries, to_np(swa)[0, :10]])
+    np.testing.assert_allclose(out[0, 0].cpu().numpy(), np.broadcast_to(rows.mean(0), (16, 512)), atol=2e-3)
+    np.testing.assert_allclose(lse[0, 0].cpu().numpy(), math.log(rows.shape[0]), atol=1e-4)
+
+
+def test_no_rows_gives_zero_and_neg_inf(csa):
+    E = 64
+    cache = csa.empty_cache(1, E, 512, DEV)
+    q = torch.ones(1, 1, 16, 512, dtype=torch.bfloat16, device=DEV)
+    swa = torch.ones(1, 128, 512, dtype=torch.bfloat16, device=DEV)
+    idx = torch.full((1, 1, 8), -1, dtype=torch.int32, device=DEV)
+    out, lse = gpu_decode_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV), idx, swa,
+                               torch.tensor([0], dtype=torch.int32, device=DEV), E, 128)
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_out_of_capacity_block_id_is_reported(csa):
+    g = torch.Generator(device=DEV).manual_seed(10)
+    T, W = 2 * 80, 128
+    E = T // 2
+    x = _latents(g, 1, T)
+    q = torch.randn(1, 1, 16, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa = torch.randn(1, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    ws0 = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T], E, 512, 2, csa.SCALE_AMAX, ws0)
+    idx = torch.tensor([[[3, 1000000, 0, -7]]], dtype=torch.int32, device=DEV)
+    out = torch.empty(1, 1, 16, 512, device=DEV)
+    n_entries = torch.tensor([E], dtype=torch.int32, device=DEV)
+    swa_len = torch.tensor([W], dtype=torch.int32, device=DEV)
+    args = csa.attn_args(q, cache, n_entries, idx, out, max_entries=E, window=W, scale=SCALE, swa=swa,
+                         swa_len=swa_len)
+    ws = csa.workspace(csa.sparse_attn_workspace_size(1, args), DEV)
+    csa.sparse_attn_decode(q, cache, n_entries, idx, out, max_entries=E, window=W, scale=SCALE, ws=ws, swa=swa,
+                           swa_len=swa_len)
+    assert csa.device_status(ws) == csa.ERR_DEVICE_CHECK
+    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    ref, _ = o_attn.decode_attention(to_np(q)[0, 0].astype(np.float64), entries, E, [3, 0], to_np(swa)[0], SCALE)
+    assert_attn_close(out[0, 0].cpu().numpy(), ref)
+
+
+def test_prefill_matches_oracle(csa):
+    g = torch.Generator(device=DEV).manual_seed(11)
+    rng = np.random.default_rng(11)
+    context, chunk_start, W, K, H = 1200, 1100, 128, 24, 64
+    E = context // 2
+    x = _latents(g, 1, context)
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [context], E, 512, 2, csa.SCALE_AMAX, ws)
+    pos = np.concatenate([[0, 1, 5, 200, 973, 1100, 1101], rng.integers(chunk_start, context, 26)]).astype(np.int32)
+    Q = pos.size
+    first = chunk_start - W + 1
+    swa = torch.randn(1, context - first, 512, generator=g, device=DEV).to(torch.bfloat16)
+    q = torch.randn(1, Q, H, 512, generator=g, device=DEV).to(torch.bfloat16)
+    nb = -(-E // 8)
+    idx_np = np.stack([rng.choice(nb, K, replace=False) for _ in range(Q)]).astype(np.int32)[None]
+    idx_np[0, 0, -2:] = -1
+    out, lse = gpu_prefill_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV),
+                                torch.from_numpy(idx_np).to(DEV), torch.from_numpy(pos)[None].to(DEV), swa,
+                                torch.tensor([first], dtype=torch.int32, device=DEV), E, W)
+    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    qf, sf = to_np(q)[0], to_np(swa)[0]
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    for j in range(Q):
+        ref, ref_lse = o_attn.prefill_attention(qf[j].astype(np.float64), entries, E, idx_np[0, j], sf, first,
+                                                int(pos[j]), W, SCALE)
+        assert_attn_close(out[0, j], ref, f"position {pos[j]}")
+        assert_lse_close(lse[0, j], ref_lse, f"position {pos[j]}")
