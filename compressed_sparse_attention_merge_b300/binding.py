@@ -28,7 +28,10 @@ IDX_RELU, IDX_HIER = 1, 2
 class CsaError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
-        super().__init__(f"{where}: {lib().csa_status_string(status).decode()} (status {status})")
+        detail = ""
+        if status == ERR_CUDA:
+            detail = " [" + lib().csa_last_error().decode() + "]"
+        super().__init__(f"{where}: {lib().csa_status_string(status).decode()} (status {status}){detail}")
 
 
 class PackArgs(ctypes.Structure):
@@ -75,6 +78,8 @@ def lib():
         L.csa_abi_version.restype = I32
         L.csa_status_string.restype = ctypes.c_char_p
         L.csa_status_string.argtypes = [I32]
+        L.csa_last_error.restype = ctypes.c_char_p
+        L.csa_last_error.argtypes = []
         L.csa_entry_bytes.restype = SZ
         L.csa_entry_bytes.argtypes = [I32]
         L.csa_block_bytes.restype = SZ

@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
 template <int HG>
 cudaError_t launch_attn_t(const AttnParams& p, cudaStream_t s) {
   const int bytes = Smem<HG>::bytes;
+  clear_stale_error();
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.splits, (unsigned)p.units);
@@ -407,6 +408,7 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
   if (p.units == 0 || p.splits == 1) return cudaSuccess;
   ProfScope prof("attn_combine", s);
+  clear_stale_error();
   combine_kernel<<<(unsigned)(p.units * p.heads), 128, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -20,15 +20,15 @@ DeviceInfo g_dev[64];
 // Validates the current device (sm_103) and caches its SM count.
 csa_status current_device(int* num_sms) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = cudaGetDevice(&dev)) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return CSA_ERR_UNSUPPORTED_DEVICE;
   DeviceInfo& d = g_dev[dev];
   if (d.checked == 0) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return CSA_ERR_CUDA;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
     d.num_sms = sms;
     d.checked = (major == 10 && minor == 3) ? 1 : -1;
   }
@@ -120,25 +120,45 @@ Profiler g_prof;
 
 namespace csa {
 
+// Records a timing event on s; inside stream capture the event becomes an external event node of the graph.
+static cudaError_t prof_record(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  e = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                          : cudaEventRecord(ev, s);
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e;
+}
+
 void prof_begin(const char* name, cudaStream_t s) {
   if (!g_prof.on) return;
   if (g_prof.recs.size() >= g_prof.max_records) { ++g_prof.dropped; g_prof.pending = false; return; }
   const size_t i = g_prof.recs.size();
   g_prof.cur = ProfRecord{name, g_prof.pool[2 * i], g_prof.pool[2 * i + 1]};
-  cudaEventRecordWithFlags(g_prof.cur.start, s, cudaEventRecordExternal);
+  if (prof_record(g_prof.cur.start, s) != cudaSuccess) { ++g_prof.dropped; g_prof.pending = false; return; }
   g_prof.pending = true;
 }
 
 void prof_end(cudaStream_t s) {
   if (!g_prof.on || !g_prof.pending) return;
-  cudaEventRecordWithFlags(g_prof.cur.stop, s, cudaEventRecordExternal);
-  g_prof.recs.push_back(g_prof.cur);
   g_prof.pending = false;
+  if (prof_record(g_prof.cur.stop, s) != cudaSuccess) { ++g_prof.dropped; return; }
+  g_prof.recs.push_back(g_prof.cur);
+}
+
+thread_local char g_last_error[192] = "";
+
+csa_status cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return CSA_ERR_CUDA;
 }
 
 }  // namespace csa
 
 extern "C" {
+
+const char* csa_last_error(void) { return csa::g_last_error; }
 
 int csa_abi_version(void) { return CSA_ABI_VERSION; }
 
@@ -162,16 +182,17 @@ size_t csa_block_bytes(int dim) { return (dim > 0 && dim % kGroup == 0) ? (size_
 csa_status csa_workspace_reset(void* ws, size_t ws_bytes, cudaStream_t stream) {
   csa_status st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
   if (st != CSA_OK) return st;
-  return cudaMemsetAsync(ws, 0, CSA_WS_HEADER_BYTES, stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+  if (cudaError_t e = cudaMemsetAsync(ws, 0, CSA_WS_HEADER_BYTES, stream)) return cuda_fail(e, "workspace reset");
+  return CSA_OK;
 }
 
 csa_status csa_get_device_status(void* ws, cudaStream_t stream) {
   if (ws == nullptr) return CSA_ERR_INVALID_ARG;
   uint32_t hdr[4] = {0, 0, 0, 0};
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CSA_ERR_CUDA;
-  if (cudaMemcpy(hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = cudaStreamSynchronize(stream)) return cuda_fail(e, "stream synchronize");
+  if (cudaError_t e = cudaMemcpy(hdr, ws, sizeof(hdr), cudaMemcpyDeviceToHost)) return cuda_fail(e, "status read");
   if (hdr[0] != 0u) {
-    if (cudaMemset(ws, 0, CSA_WS_HEADER_BYTES) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaError_t e = cudaMemset(ws, 0, CSA_WS_HEADER_BYTES)) return cuda_fail(e, "status clear");
   }
   switch (hdr[0]) {
     case 0: return CSA_OK;
@@ -218,8 +239,8 @@ csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* a, void* ws, size_t 
   p.cache = a->cache; p.cache_stride_b = a->cache_stride_b;
   p.coarse_sum = a->coarse_sum; p.coarse_stride_b = a->coarse_stride_b;
   p.hdr = static_cast<uint32_t*>(ws);
-  if (launch_pack(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
-  if (launch_coarse_sum(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = launch_pack(p, stream)) return cuda_fail(e, "pack");
+  if (cudaError_t e = launch_coarse_sum(p, stream)) return cuda_fail(e, "coarse_sum");
   return CSA_OK;
 }
 
@@ -276,11 +297,11 @@ csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size
     cp.relu = relu; cp.coarse = a->coarse_sum; cp.coarse_stride_b = a->coarse_stride_b;
     cp.n_entries = a->n_entries; cp.n_super = L.n_super;
     cp.scores = reinterpret_cast<float*>(w + L.coarse_off); cp.batch = batch;
-    if (launch_coarse_score(cp, stream) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaError_t e = launch_coarse_score(cp, stream)) return cuda_fail(e, "coarse_score");
     TopkParams tk{};
     tk.scores = cp.scores; tk.score_stride = L.n_super; tk.n = L.n_super; tk.k = (int)L.keep_super;
     tk.out = kept; tk.out_stride = L.keep_super; tk.units = L.units; tk.hdr = hdr;
-    if (launch_topk(tk, stream) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaError_t e = launch_topk(tk, stream)) return cuda_fail(e, "topk");
   }
 
   ScoreParams sp{};
@@ -289,18 +310,18 @@ csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size
   sp.max_entries = a->max_entries; sp.q_pos = a->q_pos;
   sp.kept = hier ? kept : nullptr; sp.keep_super = (int)L.keep_super;
   sp.scores = scores; sp.score_stride = L.n_slots; sp.n_slots = L.n_slots; sp.batch = batch; sp.hdr = hdr;
-  if (launch_index_score(sp, num_sms, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = launch_index_score(sp, num_sms, stream)) return cuda_fail(e, "index_score");
 
   TopkParams tk{};
   tk.scores = scores; tk.score_stride = L.n_slots; tk.n = L.n_slots; tk.k = a->top_k;
   tk.out = a->out_idx; tk.out_stride = a->top_k; tk.units = L.units; tk.hdr = hdr;
   if (hier) { tk.map_super = kept; tk.map_stride = (int)L.keep_super; }
-  if (launch_topk(tk, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = launch_topk(tk, stream)) return cuda_fail(e, "topk");
 
   if (a->out_block_scores != nullptr && !hier) {
-    if (cudaMemcpyAsync(a->out_block_scores, scores, (size_t)L.units * L.n_slots * 4, cudaMemcpyDeviceToDevice,
-                        stream) != cudaSuccess)
-      return CSA_ERR_CUDA;
+    if (cudaError_t e = cudaMemcpyAsync(a->out_block_scores, scores, (size_t)L.units * L.n_slots * 4,
+                                        cudaMemcpyDeviceToDevice, stream))
+      return cuda_fail(e, "block score copy");
   }
   return CSA_OK;
 }
@@ -364,8 +385,8 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
   p.out = a->out; p.out_lse = a->out_lse;
   p.hdr = reinterpret_cast<uint32_t*>(w);
-  if (launch_attn(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
-  if (launch_combine(p, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = launch_attn(p, stream)) return cuda_fail(e, "attn");
+  if (cudaError_t e = launch_combine(p, stream)) return cuda_fail(e, "combine");
   return CSA_OK;
 }
 
@@ -386,7 +407,7 @@ csa_status csa_profile_begin(int max_launches) {
   for (auto e : g_prof.pool) cudaEventDestroy(e);
   g_prof.pool.assign(2 * (size_t)max_launches, nullptr);
   for (auto& e : g_prof.pool)
-    if (cudaEventCreate(&e) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaError_t err = cudaEventCreate(&e)) return cuda_fail(err, "cudaEventCreate");
   g_prof.recs.clear();
   g_prof.recs.reserve(max_launches);
   g_prof.max_records = max_launches;
@@ -399,11 +420,11 @@ csa_status csa_profile_begin(int max_launches) {
 csa_status csa_profile_end(csa_kernel_time* out, int max_out, int* n_out, int64_t* dropped) {
   if (!g_prof.on) return CSA_ERR_INVALID_ARG;
   g_prof.on = false;
-  if (cudaDeviceSynchronize() != cudaSuccess) return CSA_ERR_CUDA;
+  if (cudaError_t e = cudaDeviceSynchronize()) return cuda_fail(e, "device synchronize");
   std::vector<csa_kernel_time> agg;
   for (const auto& r : g_prof.recs) {
     float ms = 0.0f;
-    if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) return CSA_ERR_CUDA;
+    if (cudaError_t e = cudaEventElapsedTime(&ms, r.start, r.stop)) return cuda_fail(e, "cudaEventElapsedTime");
     size_t i = 0;
     for (; i < agg.size(); ++i)
       if (std::strncmp(agg[i].name, r.name, sizeof(agg[i].name)) == 0) break;

@@ -176,6 +176,14 @@ cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
 
+// Clears an error that an earlier runtime call of another component left in this thread's last-error
+// slot without checking it, so that the check after a launch reports that launch alone. A sticky error
+// (a faulted context) is not cleared by this and still fails the launch.
+inline void clear_stale_error() { (void)cudaGetLastError(); }
+
+// Records the text of a CUDA runtime failure for csa_last_error() and returns CSA_ERR_CUDA.
+csa_status cuda_fail(cudaError_t e, const char* where);
+
 // Kernel timing hooks (defined in csa_api.cu); no-ops unless profiling is on.
 void prof_begin(const char* name, cudaStream_t s);
 void prof_end(cudaStream_t s);

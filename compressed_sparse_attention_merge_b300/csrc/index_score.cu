@@ -287,6 +287,7 @@ cudaError_t launch_score_t(const ScoreParams& p, int num_sms, cudaStream_t s) {
   int64_t bx = want < need ? want : need;
   if (bx < 1) bx = 1;
   dim3 grid((unsigned)bx, (unsigned)units_y);
+  clear_stale_error();
   index_score_kernel<DI, HI><<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
@@ -320,6 +321,7 @@ cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s) {
   if (warps == 0) return cudaSuccess;
   ProfScope prof("coarse_score", s);
   const int64_t blocks = (warps + 7) / 8;
+  clear_stale_error();
   coarse_score_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -157,6 +157,7 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
   ProfScope prof("pack_fp4", s);
+  clear_stale_error();
   pack_fp4_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
@@ -167,6 +168,7 @@ cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s) {
   const int touched = (int)((p.n_new + per_super - 1) / per_super) + 1;
   dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)touched, (unsigned)p.batch);
   ProfScope prof("coarse_sum", s);
+  clear_stale_error();
   coarse_sum_kernel<<<grid, 128, 0, s>>>(p, touched);
   return cudaGetLastError();
 }

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.units == 0) return cudaSuccess;
   ProfScope prof("topk", s);
+  clear_stale_error();
   topk_kernel<<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

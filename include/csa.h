@@ -86,6 +86,11 @@ enum { CSA_IDX_RELU = 1, CSA_IDX_HIER = 2 };
 int csa_abi_version(void);
 const char* csa_status_string(csa_status status);
 
+/* Text of the most recent CUDA runtime failure that made a csa_* call of this thread return
+   CSA_ERR_CUDA ("<step>: <CUDA error string> (<code>)"), or "" if there was none. The string is owned by
+   the library and stays valid until the thread's next failing call. */
+const char* csa_last_error(void);
+
 /* Bytes of one packed entry of width `dim` (dim/2 code bytes + dim/16 scale bytes), and of one block
    of 8 entries. dim = 512 gives 288 and 2,304. Returns 0 for a dim that is not a positive multiple of 16. */
 size_t csa_entry_bytes(int dim);

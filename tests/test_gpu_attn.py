@@ -90,8 +90,11 @@ def test_split_and_unsplit_agree(csa):
     idx = torch.arange(K, dtype=torch.int32, device=DEV).view(1, 1, K).expand(B, 1, K).contiguous()
     many, lse_many = gpu_decode_attn(csa, q[:1], cache[:1], n_entries[:1], idx[:1], swa[:1], swa_len[:1], E, W)
     one, lse_one = gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, E, W)
-    assert torch.allclose(many[0], one[0], atol=1e-5, rtol=0)
-    assert torch.allclose(lse_many[0], lse_one[0], atol=1e-5, rtol=0)
+    # Each split rounds its probabilities to fp16 relative to its own running maximum, so the two runs
+    # round different numbers (relative error up to 2^-11 per probability) and cannot agree bit for bit.
+    # They must agree to half the oracle tolerance; the log-sum-exp is fp32 only and agrees closely.
+    assert (many[0] - one[0]).abs().max().item() <= 1e-3
+    assert torch.allclose(lse_many[0], lse_one[0], atol=1e-4, rtol=0)
     assert torch.equal(one[0], one[B - 1])
 
 

@@ -98,7 +98,7 @@ def test_prefill_causal_positions(csa):
     np.testing.assert_array_equal(scores[0].cpu().numpy()[:, :ref_S.shape[1]], ref_S)
 
 
-@pytest.mark.parametrize("keep_blocks,top_k", [(192, 50), (64, 64), (128 * 64, 40)])
+@pytest.mark.parametrize("keep_blocks,top_k", [(192, 50), (64, 64), (4096, 40)])
 def test_hierarchical_bit_exact(csa, keep_blocks, top_k):
     g = torch.Generator(device=DEV).manual_seed(41 + keep_blocks)
     lengths = [512 * 9 + 100, 512 * 2 + 3]
