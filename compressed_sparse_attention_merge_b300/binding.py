@@ -29,7 +29,7 @@ class CsaError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
         detail = ""
-        if status == ERR_CUDA:
+        if status == ERR_CUDA or (status == ERR_WORKSPACE_TOO_SMALL and where == "csa_index_topk_static"):
             detail = " [" + lib().csa_last_error().decode() + "]"
         super().__init__(f"{where}: {lib().csa_status_string(status).decode()} (status {status}){detail}")
 
@@ -94,6 +94,8 @@ def lib():
         L.csa_index_topk_workspace_size.argtypes = [I64, ctypes.POINTER(IndexArgs)]
         L.csa_index_topk.restype = I32
         L.csa_index_topk.argtypes = [I64, ctypes.POINTER(IndexArgs), P, SZ, P]
+        L.csa_index_topk_static.restype = I32
+        L.csa_index_topk_static.argtypes = [I64, ctypes.POINTER(IndexArgs), P, P]
         L.csa_sparse_attn_workspace_size.restype = SZ
         L.csa_sparse_attn_workspace_size.argtypes = [I64, ctypes.POINTER(AttnArgs)]
         for name in ("csa_sparse_attn_decode", "csa_sparse_attn_prefill"):
@@ -255,6 +257,22 @@ def index_topk(q_idx, keys, n_entries, out_idx, *, max_entries, top_k, ws, head_
                    out_block_scores=out_block_scores)
     _check(lib().csa_index_topk(q_idx.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)),
            "csa_index_topk")
+
+
+STATIC_INDEX_SCRATCH_BYTES = 4 << 20
+
+
+def index_topk_static(q_idx, keys, n_entries, out_idx, *, max_entries, top_k, head_w=None, relu=True, q_pos=None,
+                      coarse_sum=None, keep_blocks=0, status_out=None, stream=None):
+    """csa_index_topk_static: the same selection as index_topk, for callers that cannot allocate device
+    memory; the scratch is the library's own fixed 4 MiB device array (calls on one device must not
+    overlap on the GPU). status_out: optional int32 CUDA tensor of one element that receives the device
+    status word."""
+    a = index_args(q_idx, keys, n_entries, out_idx, max_entries=max_entries, top_k=top_k, head_w=head_w,
+                   relu=relu, q_pos=q_pos, coarse_sum=coarse_sum, keep_blocks=keep_blocks)
+    st = None if status_out is None else _need(status_out, "status_out", torch.int32)
+    _check(lib().csa_index_topk_static(q_idx.shape[0], ctypes.byref(a), _ptr(st), _stream(stream)),
+           "csa_index_topk_static")
 
 
 def attn_args(q, cache, n_entries, idx, out, *, max_entries, window, scale, swa=None, swa_len=None,

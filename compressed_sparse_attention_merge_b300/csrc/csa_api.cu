@@ -1,6 +1,7 @@
 // C ABI of the CSA2 library: host-side validation, workspace layout, launch configuration, the device
 // status word and opt-in kernel timing. Every compute step runs in the kernels of this directory; the
 // host code only checks arguments and launches. Nothing here allocates device memory.
+#include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -147,11 +148,18 @@ void prof_end(cudaStream_t s) {
   g_prof.recs.push_back(g_prof.cur);
 }
 
-thread_local char g_last_error[192] = "";
+thread_local char g_last_error[256] = "";
 
 csa_status cuda_fail(cudaError_t e, const char* where) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
   return CSA_ERR_CUDA;
+}
+
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
 }
 
 }  // namespace csa

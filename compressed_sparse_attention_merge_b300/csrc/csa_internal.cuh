@@ -183,6 +183,8 @@ inline void clear_stale_error() { (void)cudaGetLastError(); }
 
 // Records the text of a CUDA runtime failure for csa_last_error() and returns CSA_ERR_CUDA.
 csa_status cuda_fail(cudaError_t e, const char* where);
+// Records a printf-style message for csa_last_error().
+void set_last_error(const char* fmt, ...);
 
 // Kernel timing hooks (defined in csa_api.cu); no-ops unless profiling is on.
 void prof_begin(const char* name, cudaStream_t s);

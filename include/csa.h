@@ -86,9 +86,10 @@ enum { CSA_IDX_RELU = 1, CSA_IDX_HIER = 2 };
 int csa_abi_version(void);
 const char* csa_status_string(csa_status status);
 
-/* Text of the most recent CUDA runtime failure that made a csa_* call of this thread return
-   CSA_ERR_CUDA ("<step>: <CUDA error string> (<code>)"), or "" if there was none. The string is owned by
-   the library and stays valid until the thread's next failing call. */
+/* Text describing the most recent failure of a csa_* call of this thread that had more to say than its
+   status code: a CUDA runtime failure behind CSA_ERR_CUDA ("<step>: <CUDA error string> (<code>)"), or
+   the sizes behind a CSA_ERR_WORKSPACE_TOO_SMALL of csa_index_topk_static; "" if there was none. The
+   string is owned by the library and stays valid until the thread's next failing call. */
 const char* csa_last_error(void);
 
 /* Bytes of one packed entry of width `dim` (dim/2 code bytes + dim/16 scale bytes), and of one block
@@ -217,6 +218,34 @@ typedef struct csa_index_args {
 size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* args);
 csa_status csa_index_topk(int64_t batch, const csa_index_args* args, void* ws, size_t ws_bytes,
                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * csa_index_topk_static -- csa_index_topk for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call: it exists for callers of this library that have no way to
+ * hand csa_index_topk a workspace, such as code inside a host framework whose allocator owns all device
+ * memory and forbids raw cudaMalloc, plug-ins that may only use the buffers they are given, or serving
+ * loops that must not allocate once running. It computes exactly what csa_index_topk computes, with the
+ * same arguments and validation, but takes its scratch from a fixed array that the library places in
+ * device memory when it is loaded. It never calls cudaMalloc, cudaFree or any other allocating routine.
+ *
+ *   - The array holds CSA_STATIC_INDEX_SCRATCH_BYTES (4 MiB). A call whose csa_index_topk_workspace_size
+ *     is larger is rejected with CSA_ERR_WORKSPACE_TOO_SMALL before anything is launched, and
+ *     csa_last_error() gives both sizes. Every GPU that loads the library holds the array until exit.
+ *   - The first call on a device (with that device current) looks up the array's device address; make
+ *     that first call before capturing any stream on that device.
+ *   - Every call on a device shares the one array, and it keeps the previous call's contents; each call
+ *     clears the status word itself. Calls whose work overlaps on the GPU (different streams, or
+ *     different host threads, without ordering between them) race on the array and give undefined
+ *     results: order them on one stream.
+ *   - status_out: optional device int32. When given, it receives the call's device status word after
+ *     the kernels finish (stream-ordered): 0, or CSA_ERR_DEVICE_CHECK / CSA_ERR_TIMEOUT as
+ *     csa_get_device_status() would report for a workspace.
+ * ------------------------------------------------------------------------------------------------ */
+#define CSA_STATIC_INDEX_SCRATCH_BYTES (4u << 20)
+
+csa_status csa_index_topk_static(int64_t batch, const csa_index_args* args, int32_t* status_out,
+                                 cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------------
  * csa_sparse_attn_decode / csa_sparse_attn_prefill -- attention over the selected blocks of the shared
