@@ -371,12 +371,22 @@ def run_ours(args):
     R = args.replicas
     stream = torch.cuda.current_stream(device)
 
-    # warm-up
+    # eager warm-up: the first launches on the device set kernel attributes outside any capture
     for i in range(args.warmup):
         w.step(i % R)
     torch.cuda.synchronize(device)
 
-    # timed region (device resident inputs)
+    # one CUDA graph per cache replica holds a whole step; the timed loop replays them in rotation
+    graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            w.step(r)
+        graphs.append(g)
+    for i in range(args.warmup):
+        graphs[i % R].replay()
+    torch.cuda.synchronize(device)
+
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -386,7 +396,7 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     start.record(stream)
     for i in range(args.steps):
-        w.step(i % R)
+        graphs[i % R].replay()
     stop.record(stream)
     torch.cuda.synchronize(device)
     _barrier(world)
@@ -395,43 +405,59 @@ def run_ours(args):
     ms = _max_over_ranks(ms, world, device)
     value = world * w.queries_per_step / (ms * 1e-3)
 
-    # per-kernel times: the same steps again with the library's event hooks on the launch stream
-    for i in range(2):
-        w.step(i % R)
-    torch.cuda.synchronize(device)
+    # per-kernel device times: the same K steps captured with the library's event hooks (event nodes on
+    # the launch stream around every kernel), replayed once
     csa.profile_begin(64 * args.steps * max(1, len(w.modes)) + 64)
-    for i in range(args.steps):
-        w.step(i % R)
+    gp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gp):
+        for i in range(args.steps):
+            w.step(i % R)
+    gp.replay()
+    torch.cuda.synchronize(device)
     kt, dropped = csa.profile_end()
     launches = sum(n for n, _ in kt.values())
+    del gp
 
-    # end to end: per step, H2D of the step's inputs from pinned memory, the path, D2H of the output
+    # end to end through the binding: per step, H2D of the step's inputs from pinned host memory, the
+    # path, D2H of the attention output; captured per replica like the device-resident steps, and also
+    # run eagerly (one Python call per entry point) for comparison
     host_in = {k: v.to("cpu").pin_memory() for k, v in w.h2d_inputs().items()}
     dev_in = {k: torch.empty_like(v) for k, v in w.h2d_inputs().items()}
     host_out = torch.empty(w.out.shape, dtype=w.out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
 
-    def e2e_step(i):
+    def e2e_step(r):
         for k in host_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        out = w.step(i % R, q=dev_in["q"], q_idx=dev_in["q_idx"], new_tokens=dev_in["new_tokens"],
+        out = w.step(r, q=dev_in["q"], q_idx=dev_in["q_idx"], new_tokens=dev_in["new_tokens"],
                      new_keys=dev_in["new_keys"])
         host_out.copy_(out, non_blocking=True)
 
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize(device)
-    _barrier(world)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    t1.record(stream)
-    torch.cuda.synchronize(device)
-    _barrier(world)
-    e2e_ms = _max_over_ranks(t0.elapsed_time(t1) / args.steps, world, device)
+    def timed(fn):
+        for i in range(args.warmup):
+            fn(i % R)
+        torch.cuda.synchronize(device)
+        _barrier(world)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            fn(i % R)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        _barrier(world)
+        return _max_over_ranks(t0.elapsed_time(t1) / args.steps, world, device)
+
+    e2e_graphs = []
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            e2e_step(r)
+        e2e_graphs.append(g)
+    e2e_ms = timed(lambda r: e2e_graphs[r].replay())
+    e2e_eager_ms = timed(e2e_step)
+    del e2e_graphs, graphs
 
     peaks = _peaks()
     kernels = {}
@@ -470,7 +496,7 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp4-e2m1/e4m3 cache, fp16 mma f32 accumulate", "data": "synthetic",
-        "config": {"workload": args.workload, "batch_per_gpu": w.case.batch if hasattr(w.case, "batch") else 1,
+        "config": {"workload": args.workload, "launch": "CUDA graph per step", "batch_per_gpu": w.case.batch if hasattr(w.case, "batch") else 1,
                    "queries_per_step_per_gpu": w.queries_per_step, "layers": len(w.modes),
                    "l2": f"{R} cache replicas in rotation, {round(R * touched_bytes(w) / 1e6, 1)} MB touched "
                          f"per rotation > 126 MB L2",
@@ -478,7 +504,10 @@ def run_ours(args):
         "alg_bytes_per_step": w.step_bytes(),
         "achieved_step_gbs": round(w.step_bytes() / (ms * 1e-3) / 1e9, 1),
         "e2e": {"value": round(world * w.queries_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT,
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "launch": "CUDA graph per step (copies, entry points, copy back)",
+                "eager_value": round(world * w.queries_per_step / (e2e_eager_ms * 1e-3), 1),
+                "eager_ms_per_step": round(e2e_eager_ms, 5)},
         "gpu_launches": launches, "kernels": kernels, "roofline": roof, "clocks": clocks,
         "cpu_baseline": cpu, "impl": "ours",
     }
@@ -644,7 +673,7 @@ def run_reference(args):
     line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample": what},
+            "config": {"workload": args.workload, "launch": "CUDA graph per step", "sample": what},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": what},

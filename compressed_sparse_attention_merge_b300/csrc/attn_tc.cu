@@ -1,0 +1,681 @@
+// Sparse attention over selected FP4 cache blocks merged with the sliding window, on the fifth-generation
+// tensor cores (tcgen05), split over the row list, plus the fixed-order log-sum-exp combine of the splits.
+//
+// Follows "DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression" (paper-digest), Core
+// Mechanics ("one 512-dim latent shares keys and values across all attention heads") and Terminology
+// (sliding window of 128), and "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" (card),
+// Key ideas ("Every layer keeps its own query and sliding-window KV").
+//
+// Design. A CTA owns one query (all heads) and some 128-row tiles of its row list: a range of cache
+// tiles (16 selected blocks each) and/or the window tiles. Because one latent row c is both key and
+// value, both products are taken with the rows as the 128-wide M side and the heads as N:
+//   S^T [rows x heads]  = C [rows x 512] . Q^T                   (C K-major, Q K-major)
+//   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (C and P MN-major)
+// C lives in shared memory as fp16 panels of 64 latent columns in the 128-byte-swizzled layout; the same
+// bytes are the K-major operand of the first product and the MN-major operand of the second.
+//   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk; the tile is
+//   dequantised twice, panel by panel, through a ring of four panel buffers (once per product).
+//   Window tiles: a tensor-map copy (TMA, 128-byte swizzle) lands the 128 bf16 rows directly in panel
+//   layout; they are converted to fp16 in place and serve both products.
+// The row sums l come from a fifth product whose A operand is a 1 KB atom of ones repeated over every
+// row (stride 0). S, O and l accumulate in tensor memory (64 + 256 + 64 columns of fp32).
+//
+// Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-11 dequantisation, 12 gather, 13 MMA issue
+// and tensor-memory allocation. The softmax keeps, per head, a reference maximum that is raised only
+// when a tile's maximum exceeds it by more than 8 (in log2 units), so the probabilities stay below 2^8
+// and the accumulators are rescaled rarely. Splits write unnormalised partials (o, m, l); the combine
+// kernel merges them in split order.
+#include <cuda.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "csa_internal.cuh"
+#include "tc.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kRows = 128;                                 // rows per tile: M of both products
+constexpr int kTileBlocks = kRows / kBlockEntries;         // 16 cache blocks per tile
+constexpr int kHeadsPad = 64;                              // N of both products (heads, zero-padded)
+constexpr int kPanels = kLatent / 64;                      // 8 panels of 64 latent columns
+constexpr int kRing = 4;
+constexpr int kLatBlk = block_bytes(kLatent);              // 2304
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleSlack = 8.0f;                      // log2 headroom before the reference max moves
+
+// shared-memory map (bytes); the operand regions start on 1024-byte boundaries
+constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB
+constexpr int kQOff = 0;
+constexpr int kRawStage = kTileBlocks * kLatBlk;           // 36,864
+constexpr int kRawOff = kQOff + kPanels * kQPanel;         // 65,536
+constexpr int kPanelBytes = kRows * 128;                   // 16 KB
+constexpr int kRingOff = kRawOff + 2 * kRawStage;          // 139,264
+constexpr int kWinOff = kRawOff;                           // window tile: 8 panels over the raw and ring areas
+constexpr int kPOff = kRingOff + kRing * kPanelBytes;      // 204,800
+constexpr int kOnesOff = kPOff + kRows * 128;              // 221,184
+constexpr int kBarOff = kOnesOff + 1024;                   // 222,208
+constexpr int kNumBars = 20;
+constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
+constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort
+constexpr int kMOff = kFlagOff + 16;                       // float m[64]
+constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[64]
+constexpr int kRedOff = kAlphaOff + 64 * 4;                // float red[4][64]
+constexpr int kSmemBytes = kRedOff + 4 * 64 * 4;
+static_assert(kWinOff + kPanels * kPanelBytes <= kPOff, "window panels must fit below P");
+
+enum Bar { RAW_FULL = 0, RAW_EMPTY = 2, RING_FULL = 4, RING_EMPTY = 8, S_FULL = 12, P_FULL = 13, O_DONE = 14,
+           FIN = 15, WIN_FULL = 16, WIN_CVT = 17, WIN_EMPTY = 18 };
+
+constexpr int kDqWarp0 = 4, kDqWarps = 8;
+constexpr int kGatherWarp = 12, kMmaWarp = 13;
+constexpr int kThreads = 14 * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 64, kColL = 320;
+
+constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
+constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
+constexpr uint32_t kIdescL = tc::idesc_f16_f32(128, kHeadsPad, 0, 1);   // ones K-major, P^T MN-major
+
+// Bounded wait that also gives up as soon as another role of the CTA has given up.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         uint32_t* hdr, uint32_t detail) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  report(hdr, CSA_ERR_TIMEOUT, KID_ATTN, detail);
+  return false;
+}
+
+// Bounded wait that ignores the abort flag (draining copies that must land before the CTA exits).
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return;
+  }
+}
+
+// AND of v over the 128 softmax threads (named barrier 1), so that they all take the same branch.
+__device__ __forceinline__ bool all_softmax(bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.and.pred p, 1, 128, q;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(r) : "r"((uint32_t)v) : "memory");
+  return r != 0;
+}
+
+// Tensor-map copy of a [1 x 128 x 64] box (batch, row, latent column) into shared memory.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+                  "r"(smem_addr(bar)) : "memory");
+}
+
+struct UnitCtx {
+  int64_t unit, b, n_e, n_b, nb_cap, pos, swa_first, swa_len;
+  bool prefill;
+};
+
+// Cache row r of cache tile t: block id (or -1) and whether the row's entry is attended.
+__device__ __forceinline__ bool cache_row(const AttnParams& p, const UnitCtx& u, int t, int r, int64_t* id_out) {
+  const int slot = t * kTileBlocks + (r >> 3);
+  int64_t id = -1;
+  if (slot < p.top_k) id = __ldg(p.idx + u.unit * p.top_k + slot);
+  const bool ok = id >= 0 && id < u.n_b;
+  *id_out = ok ? id : -1;
+  if (!ok) return false;
+  const int64_t e = id * kBlockEntries + (r & 7);
+  return e < u.n_e && 2 * e + 1 <= u.pos;
+}
+
+// First window-buffer row of window tile tw (may be negative or past the buffer: those rows are filled
+// with zeros by the tensor copy and are never attended).
+__device__ __forceinline__ int64_t window_row0(const AttnParams& p, const UnitCtx& u, int tw) {
+  return u.prefill ? u.pos - p.window + 1 + (int64_t)tw * kRows - u.swa_first : (int64_t)tw * kRows;
+}
+
+// Whether row r of window tile tw is attended; *oob reports a row the caller declared present but that
+// lies outside the window buffer.
+__device__ __forceinline__ bool window_row(const AttnParams& p, const UnitCtx& u, int tw, int r, bool* oob) {
+  const int slot = tw * kRows + r;
+  *oob = false;
+  if (slot >= p.window) return false;
+  const bool declared = u.prefill ? (u.pos - p.window + 1 + slot >= u.swa_first) : (slot < u.swa_len);
+  const int64_t s = window_row0(p, u, tw) + r;
+  if (declared && (s < 0 || s >= p.swa_rows)) { *oob = true; return false; }
+  return declared;
+}
+
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
+  return f2_to_h2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+
+// Four code bytes (eight E2M1 elements, low nibble first) -> four f16x2, exact.
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* h) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p,
+                                                               const __grid_constant__ CUtensorMap swa_map) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + kTmemPtrOff);
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
+  volatile int* abort_flag = flag + 2;
+  float* msh = reinterpret_cast<float*>(smem + kMOff);
+  float* alpha = reinterpret_cast<float*>(smem + kAlphaOff);
+  float* red = reinterpret_cast<float*>(smem + kRedOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x;
+  const int H = p.heads;
+
+  UnitCtx u;
+  u.unit = blockIdx.y;
+  u.b = u.unit / p.n_query;
+  u.n_e = __ldg(p.n_entries + u.b);
+  if (u.n_e < 0 || u.n_e > p.max_entries) {
+    if (tid == 0 && split == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.b);
+    u.n_e = u.n_e < 0 ? 0 : p.max_entries;
+  }
+  u.n_b = (u.n_e + kBlockEntries - 1) / kBlockEntries;
+  u.nb_cap = (p.max_entries + kBlockEntries - 1) / kBlockEntries;
+  u.prefill = p.q_pos != nullptr;
+  u.pos = u.prefill ? (int64_t)__ldg(p.q_pos + u.unit) : INT64_MAX;
+  u.swa_first = (u.prefill && p.window > 0) ? (int64_t)__ldg(p.swa_first_pos + u.b) : 0;
+  u.swa_len = (!u.prefill && p.window > 0) ? (int64_t)__ldg(p.swa_len + u.b) : 0;
+
+  // this CTA's tiles: cache tiles [c0, c1), then nw window tiles
+  const bool win_only = p.win_split && split == p.splits - 1;
+  const int c0 = win_only ? 0 : (int)((int64_t)split * p.n_ct / p.cache_splits);
+  const int c1 = win_only ? 0 : (int)((int64_t)(split + 1) * p.n_ct / p.cache_splits);
+  const int nw = (win_only || (!p.win_split && split == p.cache_splits - 1)) ? p.n_wt : 0;
+  const int n_cache = c1 - c0;
+  const int n_tiles = n_cache + nw;
+  const uint8_t* seq = p.cache + u.b * p.cache_stride_b;
+
+  // ---------------- setup ----------------
+  if (warp == kMmaWarp) tc::alloc(tmem_ptr, kTmemCols);
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) { mbar_init(&bars[RAW_FULL + i], 1); mbar_init(&bars[RAW_EMPTY + i], kDqWarps); }
+    for (int i = 0; i < kRing; ++i) { mbar_init(&bars[RING_FULL + i], kDqWarps); mbar_init(&bars[RING_EMPTY + i], 1); }
+    mbar_init(&bars[S_FULL], 1);
+    mbar_init(&bars[P_FULL], 4);
+    mbar_init(&bars[O_DONE], 1);
+    mbar_init(&bars[FIN], 1);
+    mbar_init(&bars[WIN_FULL], 1);
+    mbar_init(&bars[WIN_CVT], kDqWarps);
+    mbar_init(&bars[WIN_EMPTY], 1);
+    fence_mbar_init();
+    flag[0] = 0; flag[1] = 0; *abort_flag = 0;
+  }
+  {
+    // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero
+    const __nv_bfloat16* qg = p.q + u.unit * (int64_t)H * kLatent;
+    for (int i = tid; i < kHeadsPad * 64; i += kThreads) {
+      const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (h < H) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(qg + (int64_t)h * kLatent + ch * 8));
+        v = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
+      }
+      *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = v;
+    }
+    for (int i = tid; i < 64; i += kThreads)
+      *reinterpret_cast<uint4*>(smem + kOnesOff + i * 16) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+    for (int i = tid; i < 64; i += kThreads) msh[i] = -INFINITY;
+  }
+  tc::fence_proxy_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tmem_ptr;
+  const uint32_t s_base = smem_addr(smem);
+
+  if (warp == kGatherWarp) {
+    // ---------------- gather: cache blocks (cp.async.bulk), window rows (tensor map) ----------------
+    if (lane == 0) {
+      int issued = 0, win_issued = 0;
+      for (int it = 0; it < n_cache; ++it) {
+        const int stage = it & 1;
+        if (it >= 2 && !wait_bar(&bars[RAW_EMPTY + stage], ((it >> 1) - 1) & 1, abort_flag, p.hdr, 1)) break;
+        const int t = c0 + it;
+        uint8_t* dst = smem + kRawOff + stage * kRawStage;
+        uint32_t bytes = 0;
+        int64_t ids[kTileBlocks];
+#pragma unroll
+        for (int j = 0; j < kTileBlocks; ++j) {
+          const int slot = t * kTileBlocks + j;
+          int64_t id = -1;
+          if (slot < p.top_k) id = __ldg(p.idx + u.unit * p.top_k + slot);
+          if (id < -1 || id >= u.nb_cap) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
+          ids[j] = (id >= 0 && id < u.n_b) ? id : -1;
+          if (ids[j] >= 0) bytes += kLatBlk;
+        }
+        if (bytes) {
+          mbar_arrive_expect_tx(&bars[RAW_FULL + stage], bytes);
+#pragma unroll
+          for (int j = 0; j < kTileBlocks; ++j)
+            if (ids[j] >= 0) bulk_g2s(dst + j * kLatBlk, seq + ids[j] * kLatBlk, kLatBlk, &bars[RAW_FULL + stage]);
+        } else {
+          mbar_arrive(&bars[RAW_FULL + stage]);
+        }
+        ++issued;
+      }
+      if (issued == n_cache) {
+        for (int tw = 0; tw < nw; ++tw) {
+          // the window panels overlay the raw and ring buffers: wait until every earlier product is done
+          const int need = tw + (n_cache > 0 ? 1 : 0);
+          if (need > 0 && !wait_bar(&bars[WIN_EMPTY], (need - 1) & 1, abort_flag, p.hdr, 9)) break;
+          const int64_t y0 = window_row0(p, u, tw);
+          const int y = (int)(y0 < -(int64_t)kRows ? -kRows : (y0 > p.swa_rows ? p.swa_rows : y0));
+          mbar_arrive_expect_tx(&bars[WIN_FULL], kPanels * kPanelBytes);
+#pragma unroll
+          for (int pp = 0; pp < kPanels; ++pp)
+            tma_load_3d(smem + kWinOff + pp * kPanelBytes, &swa_map, pp * 64, y, (int)u.b, &bars[WIN_FULL]);
+          ++win_issued;
+        }
+      }
+      // no copy into this CTA's shared memory may still be in flight when it exits
+      for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it) drain_bar(&bars[RAW_FULL + (it & 1)], (it >> 1) & 1);
+      if (win_issued > 0) drain_bar(&bars[WIN_FULL], (win_issued - 1) & 1);
+    }
+  } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
+    // ---------------- dequantisation ----------------
+    const int dt = tid - kDqWarp0 * 32;        // 0..255
+    const int cp = dt & 3;                     // 16-element scale group within a panel
+    uint32_t ring_k = 0;
+    bool stop = false;
+    for (int it = 0; it < n_cache && !stop; ++it) {
+      const int stage = it & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
+      const uint8_t* raw = smem + kRawOff + stage * kRawStage;
+      // this thread's rows r = dt / 4 + 64 j and the offsets of their codes and scales in the raw stage
+      bool vr[2];
+      uint32_t code_off[2], sc_off[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = (dt >> 2) + 64 * j;
+        int64_t id;
+        vr[j] = cache_row(p, u, c0 + it, r, &id);
+        const uint32_t blk = (uint32_t)(r >> 3) * kLatBlk, sl = (uint32_t)(r & 7);
+        code_off[j] = vr[j] ? blk + sl * 256 + cp * 8 : 0u;
+        sc_off[j] = vr[j] ? blk + 2048 + sl * 32 + cp : 0u;
+      }
+      for (int pass = 0; pass < 2 && !stop; ++pass) {
+        for (int pp = 0; pp < kPanels; ++pp) {
+          const uint32_t slot = ring_k % kRing, n = ring_k / kRing;
+          if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[RING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
+            stop = true;
+            break;
+          }
+          uint8_t* panel = smem + kRingOff + slot * kPanelBytes;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int r = (dt >> 2) + 64 * j;
+            const uint2 cw = *reinterpret_cast<const uint2*>(raw + code_off[j] + pp * 32);
+            const uint32_t sc = e4m3_to_f16x2_bcast(raw[sc_off[j] + pp * 4]);
+            uint32_t h[8];
+            e2m1x8_to_f16x8(cw.x, h);
+            e2m1x8_to_f16x8(cw.y, h + 4);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[k] = vr[j] ? hmul2_u32(h[k], sc) : 0u;
+            *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp) ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          tc::fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[RING_FULL + slot]);
+          ++ring_k;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
+    }
+    for (int tw = 0; tw < nw && !stop; ++tw) {
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], tw & 1, abort_flag, p.hdr, 10))) break;
+      // in place: bf16 -> fp16, rows that are not attended -> 0; this thread's rows are (k & 3) * 32 + dt / 8
+      bool vr[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        bool oob;
+        vr[k] = window_row(p, u, tw, k * 32 + (dt >> 3), &oob);
+        if (oob && (dt & 7) == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
+      }
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const int q = k * 256 + dt;
+        const int pp = q >> 10, row = (q & 1023) >> 3, c = q & 7;
+        uint4* a = reinterpret_cast<uint4*>(smem + kWinOff + pp * kPanelBytes + row * 128 + ((c ^ (row & 7)) << 4));
+        const uint4 x = *a;
+        const bool v = vr[k & 3];
+        *a = v ? make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w)) : make_uint4(0, 0, 0, 0);
+      }
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[WIN_CVT]);
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue ----------------
+    if (lane == 0) {
+      uint32_t ring_k = 0;
+      const uint32_t q_addr = s_base + kQOff, ring_addr = s_base + kRingOff, p_addr = s_base + kPOff;
+      const uint32_t ones_addr = s_base + kOnesOff, win_addr = s_base + kWinOff;
+      bool ok = true;
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const bool is_cache = it < n_cache;
+        if (!is_cache && !wait_bar(&bars[WIN_CVT], (it - n_cache) & 1, abort_flag, p.hdr, 11)) { ok = false; break; }
+        // S^T = C . Q^T over the 8 panels
+        for (int pp = 0; pp < kPanels && ok; ++pp) {
+          uint32_t c_addr;
+          uint32_t slot = 0;
+          if (is_cache) {
+            slot = ring_k % kRing;
+            if (!wait_bar(&bars[RING_FULL + slot], (ring_k / kRing) & 1u, abort_flag, p.hdr, 4)) { ok = false; break; }
+            c_addr = ring_addr + slot * kPanelBytes;
+          } else {
+            c_addr = win_addr + pp * kPanelBytes;
+          }
+          tc::fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = tc::smem_desc(c_addr + ks * 32, 16, 1024, tc::kSwizzle128B);
+            const uint64_t bq = tc::smem_desc(q_addr + pp * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
+            tc::mma_f16(tbase + kColS, a, bq, kIdescS, (pp | ks) != 0);
+          }
+          if (is_cache) { tc::commit(&bars[RING_EMPTY + slot]); ++ring_k; }
+        }
+        if (!ok) break;
+        tc::commit(&bars[S_FULL]);
+        if (!wait_bar(&bars[P_FULL], it & 1, abort_flag, p.hdr, 5)) { ok = false; break; }
+        tc::fence_after();
+        // O^T += C^T . P^T, four chunks of 128 latent columns (two adjacent panels each)
+        for (int ch = 0; ch < 4 && ok; ++ch) {
+          uint32_t c_addr;
+          uint32_t slot = 0;
+          if (is_cache) {
+            slot = ring_k % kRing;
+            const uint32_t n = ring_k / kRing;
+            if (!wait_bar(&bars[RING_FULL + slot], n & 1u, abort_flag, p.hdr, 6) ||
+                !wait_bar(&bars[RING_FULL + slot + 1], n & 1u, abort_flag, p.hdr, 6)) { ok = false; break; }
+            c_addr = ring_addr + slot * kPanelBytes;
+          } else {
+            c_addr = win_addr + 2 * ch * kPanelBytes;
+          }
+          tc::fence_after();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint64_t a = tc::smem_desc(c_addr + j * 2048, kPanelBytes, 1024, tc::kSwizzle128B);
+            const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
+            tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || j > 0) ? 1u : 0u);
+          }
+          if (is_cache) {
+            tc::commit(&bars[RING_EMPTY + slot]);
+            tc::commit(&bars[RING_EMPTY + slot + 1]);
+            ring_k += 2;
+          }
+        }
+        if (!ok) break;
+        // l += ones . P^T
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t a = tc::smem_desc(ones_addr + (j & 3) * 32, 16, 0, tc::kSwizzle128B);
+          const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
+          tc::mma_f16(tbase + kColL, a, bp, kIdescL, (it > 0 || j > 0) ? 1u : 0u);
+        }
+        // the window panels overlay the raw and ring buffers: free them after the last cache tile and
+        // after every window tile
+        if ((is_cache && it == n_cache - 1 && nw > 0) || !is_cache) tc::commit(&bars[WIN_EMPTY]);
+      }
+      if (ok && n_tiles > 0) tc::commit(&bars[O_DONE]);
+      // every MMA issued must be complete before the tensor memory is released
+      tc::commit(&bars[FIN]);
+      drain_bar(&bars[FIN], 0);
+    }
+  } else {
+    // ---------------- softmax (warps 0-3, thread = tile row) ----------------
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_tiles; ++it) {
+      if (tid == 0) flag[it & 1] = 0;
+      bool valid;
+      if (it < n_cache) {
+        int64_t id;
+        valid = cache_row(p, u, c0 + it, tid, &id);
+      } else {
+        bool oob;
+        valid = window_row(p, u, it - n_cache, tid, &oob);
+      }
+      if (!all_softmax(wait_bar(&bars[S_FULL], it & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
+      tc::fence_after();
+      {
+        // per-head maximum over the warp's 32 rows: reduce-scatter, lane ends with heads 2 lane, 2 lane + 1
+        uint32_t sr[64];
+        tc::ld_32x64(tbase + lane_base + kColS, sr);
+        tc::wait_ld();
+        float m[64];
+#pragma unroll
+        for (int h = 0; h < 64; ++h) m[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+          const int o = 16 >> k, half = 32 >> k;
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < half; ++i) {
+            const float send = up ? m[i] : m[i + half];
+            const float keep = up ? m[i + half] : m[i];
+            m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+          }
+        }
+        red[warp * 64 + 2 * lane] = m[0];
+        red[warp * 64 + 2 * lane + 1] = m[1];
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid < 64) {
+        const float tm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+        const float mo = msh[tid];
+        float mn = mo;
+        if (tm > mo + kRescaleSlack) mn = tm;
+        alpha[tid] = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
+        if (mn != mo && mo != -INFINITY) flag[it & 1] = 1;
+        msh[tid] = mn;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (flag[it & 1]) {
+        // raise the reference maximum of the accumulated O and l (the previous products are complete:
+        // they were issued before this tile's logits, whose completion this thread has seen)
+        for (int chk = 0; chk < 5; ++chk) {
+          uint32_t o[64];
+          tc::ld_32x64(tbase + lane_base + kColO + 64 * chk, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int h = 0; h < 64; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+          tc::st_32x64(tbase + lane_base + kColO + 64 * chk, o);
+        }
+        tc::wait_st();
+      }
+      // the logits again (still in tensor memory: the next tile's product waits for this tile's P)
+      uint32_t sr[64];
+      tc::ld_32x64(tbase + lane_base + kColS, sr);
+      tc::wait_ld();
+      // probabilities, fp16, row tid of P (MN-major: 64 heads contiguous, 128-byte swizzle)
+      uint8_t* prow = smem + kPOff + tid * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int h = 8 * c + 2 * k;
+          const float m0 = msh[h], m1 = msh[h + 1];
+          const float v0 = __uint_as_float(sr[h]) * p.scale_log2, v1 = __uint_as_float(sr[h + 1]) * p.scale_log2;
+          const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : exp2f(v0 - m0);
+          const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : exp2f(v1 - m1);
+          w[k] = f2_to_h2(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      tc::fence_proxy_async();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[P_FULL]);
+    }
+    // ---------------- epilogue ----------------
+    const bool have = all_softmax(ok && n_tiles > 0 && wait_bar(&bars[O_DONE], 0, abort_flag, p.hdr, 8));
+    tc::fence_after();
+    float* lsh = red;                        // the row sums, one per head (every lane holds all of them)
+    if (have && warp == 0) {
+      uint32_t lr[64];
+      tc::ld_32x64(tbase + kColL, lr);
+      tc::wait_ld();
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < 64; ++h) lsh[h] = __uint_as_float(lr[h]);
+      }
+    } else if (!have && tid < 64) {
+      lsh[tid] = 0.0f;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    const int64_t prow_base = (u.unit * p.splits + split) * H;
+    for (int chk = 0; chk < 4; ++chk) {
+      uint32_t o[64];
+      if (have) {
+        tc::ld_32x64(tbase + lane_base + kColO + 64 * chk, o);
+        tc::wait_ld();
+      } else {
+#pragma unroll
+        for (int h = 0; h < 64; ++h) o[h] = 0u;
+      }
+      const int d = 128 * chk + tid;
+#pragma unroll
+      for (int h = 0; h < 64; ++h) {
+        if (h >= H) break;
+        const float l = lsh[h];
+        const float x = __uint_as_float(o[h]);
+        if (p.splits == 1) p.out[(u.unit * H + h) * (int64_t)kLatent + d] = l > 0.0f ? x / l : 0.0f;
+        else p.part_o[(prow_base + h) * kLatent + d] = x;
+      }
+    }
+    if (tid < H) {
+      const float l = lsh[tid];
+      const float m = have ? msh[tid] : -INFINITY;
+      if (p.splits == 1) {
+        if (p.out_lse != nullptr) p.out_lse[u.unit * H + tid] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      } else {
+        *reinterpret_cast<float2*>(p.part_ml + (prow_base + tid) * 2) = make_float2(m, l);
+      }
+    }
+    tc::fence_before();
+  }
+
+  __syncthreads();
+  tc::fence_after();
+  if (warp == kMmaWarp) tc::dealloc(tbase, kTmemCols);
+}
+
+// out[u][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, splits in order; lse = (M + log2 L) ln 2.
+__global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
+  const int64_t row = blockIdx.x;                 // unit * H + h
+  const int64_t unit = row / p.heads;
+  const int h = (int)(row % p.heads);
+  const int d = threadIdx.x * 4;
+  float M = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit * p.splits + s) * p.heads + h) * 2);
+    if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const int64_t pr = (unit * p.splits + s) * p.heads + h;
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + pr * 2);
+      if (!(ml.y > 0.0f)) continue;
+      const float w = exp2f(ml.x - M);
+      const float4 v = *reinterpret_cast<const float4*>(p.part_o + pr * kLatent + d);
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      L += w * ml.y;
+    }
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  *reinterpret_cast<float4*>(p.out + row * kLatent + d) =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (threadIdx.x == 0 && p.out_lse != nullptr) p.out_lse[row] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda).
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
+  if (p.units == 0) return cudaSuccess;
+  // window rows as a [batch][swa_rows][512] bf16 tensor, copied in [1 x 128 x 64] boxes with the
+  // 128-byte swizzle of the kernel's panels; rows outside the tensor read as zero
+  CUtensorMap map;
+  std::memset(&map, 0, sizeof(map));
+  if (p.n_wt > 0) {
+    EncodeTiledFn enc = encode_tiled();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)kLatent, (cuuint64_t)p.swa_rows, (cuuint64_t)(p.units / p.n_query)};
+    const cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, (cuuint64_t)p.swa_stride_b * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(p.swa), dims, strides,
+                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  ProfScope prof("sparse_attn", s);
+  clear_stale_error();
+  cudaError_t e = ensure_smem_limit(attn_tc_kernel, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)p.splits, (unsigned)p.units);
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, map);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
+  if (p.units == 0 || p.splits == 1) return cudaSuccess;
+  ProfScope prof("attn_combine", s);
+  clear_stale_error();
+  combine_kernel<<<(unsigned)(p.units * p.heads), 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

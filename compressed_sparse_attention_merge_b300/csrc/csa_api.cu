@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "csa_internal.cuh"
@@ -72,19 +73,26 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 // ---------------------------------------------------------------------------------------------
 struct AttnLayout {
   int64_t units;
-  int tiles, splits;
+  int n_ct, n_wt, splits, cache_splits, win_split;
   size_t o_off, ml_off, total;
 };
 
+// One CTA per SM: the selected blocks of a query are cut into 128-row tiles (16 blocks) shared by the
+// cache splits, and the window rows, when there are SMs to spare, get a split of their own.
 AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   AttnLayout L{};
   L.units = batch * a->n_query;
-  L.tiles = (int)(ceil_div(a->top_k, kBlockEntries) + ceil_div(a->window, 64));
-  // one CTA per SM: split the row list so that the grid covers the SMs about once
-  int64_t splits = L.units > 0 ? num_sms / L.units : 1;
-  if (splits > L.tiles) splits = L.tiles;
-  if (splits < 1) splits = 1;
-  L.splits = (int)splits;
+  L.n_ct = (int)ceil_div(a->top_k, 16);
+  L.n_wt = a->swa_rows > 0 ? (int)ceil_div(a->window, 128) : 0;
+  const int64_t avail = L.units > 0 ? num_sms / L.units : 1;
+  if (L.n_wt > 0 && avail >= 2) {
+    L.cache_splits = (int)(avail - 1 < L.n_ct ? avail - 1 : L.n_ct);
+    L.win_split = 1;
+  } else {
+    L.cache_splits = (int)(avail < 1 ? 1 : (avail < L.n_ct ? avail : L.n_ct));
+    L.win_split = 0;
+  }
+  L.splits = L.cache_splits + L.win_split;
   L.o_off = CSA_WS_HEADER_BYTES;
   const size_t parts = L.splits > 1 ? (size_t)L.units * L.splits * a->heads : 0;
   L.ml_off = round_up(L.o_off + parts * kLatent * 4, 256);
@@ -146,6 +154,21 @@ void prof_end(cudaStream_t s) {
   g_prof.pending = false;
   if (prof_record(g_prof.cur.stop, s) != cudaSuccess) { ++g_prof.dropped; return; }
   g_prof.recs.push_back(g_prof.cur);
+}
+
+cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes) {
+  struct Entry { const void* fn; int dev; int bytes; };
+  static std::mutex mu;
+  static std::vector<Entry> table;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : table)
+    if (x.fn == kernel && x.dev == dev && x.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) table.push_back(Entry{kernel, dev, bytes});
+  return e;
 }
 
 thread_local char g_last_error[256] = "";
@@ -388,7 +411,7 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.q_pos = prefill ? a->q_pos : nullptr;
   p.swa = static_cast<const __nv_bfloat16*>(a->swa); p.swa_stride_b = a->swa_stride_b; p.swa_rows = a->swa_rows;
   p.swa_len = a->swa_len; p.swa_first_pos = a->swa_first_pos;
-  p.splits = L.splits; p.tiles = L.tiles;
+  p.splits = L.splits; p.cache_splits = L.cache_splits; p.win_split = L.win_split; p.n_ct = L.n_ct; p.n_wt = L.n_wt;
   p.part_o = reinterpret_cast<float*>(w + L.o_off);
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
   p.out = a->out; p.out_lse = a->out_lse;

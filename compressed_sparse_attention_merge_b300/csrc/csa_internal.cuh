@@ -78,6 +78,53 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 }
 
 // ------------------------------------------------------------------------------------------------
+// mbarrier and bulk-copy helpers (PTX ISA: mbarrier, cp.async.bulk). Every wait is bounded: after
+// kSpinLimit polls it gives up and returns false, and the caller records CSA_ERR_TIMEOUT.
+// ------------------------------------------------------------------------------------------------
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// Polls the phase with the given parity; true once it has completed, false after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from global to this CTA's
+// shared memory; completion is counted on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
 // Launch parameter blocks (host -> kernel launchers)
 // ------------------------------------------------------------------------------------------------
 struct PackParams {
@@ -157,7 +204,10 @@ struct AttnParams {
   int64_t swa_stride_b, swa_rows;
   const int32_t* swa_len;
   const int32_t* swa_first_pos;
-  int splits, tiles;           // tiles = ceil(top_k/8) + ceil(window/64)
+  // Work split (grid.x = splits): cache splits 0 .. cache_splits-1 share the n_ct cache tiles (16 selected
+  // blocks = 128 rows each); the n_wt window tiles (128 rows each) go to a split of their own when
+  // win_split is set, else to the last cache split.
+  int splits, cache_splits, win_split, n_ct, n_wt;
   float* part_o;               // [units][splits][heads][512]
   float* part_ml;              // [units][splits][heads][2]
   float* out;                  // used when splits == 1
@@ -180,6 +230,16 @@ cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
 // slot without checking it, so that the check after a launch reports that launch alone. A sticky error
 // (a faulted context) is not cleared by this and still fails the launch.
 inline void clear_stale_error() { (void)cudaGetLastError(); }
+
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per (device, kernel). The first
+// launch of a kernel on a device should not be inside stream capture (the attribute call is not a
+// stream operation); later launches find the limit in the table and skip it.
+cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes);
+
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, int bytes) {
+  return ensure_smem_limit_fn(reinterpret_cast<const void*>(kernel), bytes);
+}
 
 // Records the text of a CUDA runtime failure for csa_last_error() and returns CSA_ERR_CUDA.
 csa_status cuda_fail(cudaError_t e, const char* where);

@@ -277,8 +277,262 @@ __global__ void __launch_bounds__(256) coarse_score_kernel(CoarseScoreParams p) 
   if (lane == 0) *dst = __fadd_rn(s, 0.0f);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Streaming decode indexer (every unit's queries fit one MMA column group). The keys of all units are
+// cut into stages of 16 consecutive blocks; each CTA takes a contiguous range of stages. A producer
+// warp copies stages into a ring of shared-memory buffers with cp.async.bulk (one copy per stage: the
+// 16 blocks are contiguous in the cache), completing on the stage's "full" mbarrier; each of the 8
+// consumer warps takes two blocks of the stage into registers, releases the buffer on its "empty"
+// mbarrier and then scores them exactly as the kernel above does. Many stages in flight per SM keep
+// the HBM stream busy.
+// ------------------------------------------------------------------------------------------------
+constexpr int kStageBlocks = 16;
+constexpr int kConsumerWarps = kStageBlocks / 2;
+constexpr int kStreamThreads = (kConsumerWarps + 1) * 32;
+
+template <int DI>
+struct StreamCfg {
+  static constexpr int BB = block_bytes(DI);
+  static constexpr int stage_bytes = kStageBlocks * BB;
+  static constexpr int stages = DI == 64 ? 16 : (DI == 128 ? 8 : 4);
+  static constexpr int bar_off = stages * stage_bytes;
+  static constexpr int smem = bar_off + 2 * stages * 8;
+};
+
+// Walks a CTA's contiguous range of stages in order without per-stage divisions: the unit and its
+// data (sequence, query, valid entries) are refreshed only when the walk crosses into a new unit.
+struct StageCursor {
+  int64_t unit, st;         // unit index and stage within the unit
+  int64_t b, jq0, n_e, n_b;
+  int64_t slot0, id0;
+  int valid;                // leading blocks of the stage that exist in the cache
+
+  __device__ __forceinline__ void load_unit(const ScoreParams& p) {
+    const bool hier = p.kept != nullptr;
+    b = hier ? unit / p.n_query : unit;
+    jq0 = hier ? unit % p.n_query : 0;
+    int64_t n = p.n_entries[b];
+    n_e = n < 0 ? 0 : (n > p.max_entries ? p.max_entries : n);
+    n_b = (n_e + kBlockEntries - 1) / kBlockEntries;
+  }
+  __device__ __forceinline__ void load_stage(const ScoreParams& p) {
+    slot0 = st * kStageBlocks;
+    if (p.kept != nullptr) {
+      const int32_t g = p.kept[unit * p.keep_super + (st >> 2)];       // 4 stages per super-block
+      id0 = g < 0 ? -1 : (int64_t)g * kSuper + (slot0 & (kSuper - 1));
+    } else {
+      id0 = slot0;
+    }
+    int64_t v = id0 < 0 ? 0 : n_b - id0;
+    v = v < 0 ? 0 : (v > kStageBlocks ? kStageBlocks : v);
+    const int64_t slots_left = p.n_slots - slot0;
+    valid = (int)(v < slots_left ? v : slots_left);
+  }
+  __device__ __forceinline__ void begin(const ScoreParams& p, int64_t gs, int64_t spu) {
+    unit = gs / spu;
+    st = gs - unit * spu;
+    load_unit(p);
+    load_stage(p);
+  }
+  __device__ __forceinline__ bool next(const ScoreParams& p, int64_t spu) {   // true if the unit changed
+    bool changed = false;
+    if (++st == spu) { st = 0; ++unit; load_unit(p); changed = true; }
+    load_stage(p);
+    return changed;
+  }
+};
+
+template <int DI>
+__device__ __forceinline__ void load_row_smem(const uint8_t* blk, int r, int c, RowRaw<DI>& out) {
+  constexpr int BPL = DI / 8, GPL = DI / 64;
+  const uint32_t cp = smem_addr(blk + r * (DI / 2) + c * BPL);
+  if constexpr (BPL == 8) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(out.code[0]), "=r"(out.code[1]) : "r"(cp));
+  } else {
+#pragma unroll
+    for (int i = 0; i < BPL / 16; ++i)
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(out.code[4 * i]), "=r"(out.code[4 * i + 1]), "=r"(out.code[4 * i + 2]),
+                     "=r"(out.code[4 * i + 3])
+                   : "r"(cp + 16 * i));
+  }
+  const uint8_t* sp = blk + kBlockEntries * (DI / 2) + r * (DI / 16) + c * GPL;
+  if constexpr (GPL == 1) out.scale = *sp;
+  else if constexpr (GPL == 2) out.scale = *reinterpret_cast<const unsigned short*>(sp);
+  else out.scale = *reinterpret_cast<const unsigned int*>(sp);
+}
+
+template <int DI, int HI>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+index_stream_kernel(ScoreParams p, int64_t total_stages, int64_t stages_per_unit) {
+  using C = StreamCfg<DI>;
+  constexpr int KS = DI / 16;
+  constexpr int GPL = DI / 64;
+  constexpr int QPM = HI >= 8 ? 1 : 8 / HI;
+  constexpr int LPQ = HI >= 2 ? HI / 2 : 1;
+  constexpr int QPL = HI == 1 ? 2 : 1;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::bar_off);
+  uint64_t* empty = full + C::stages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t s0 = total_stages * blockIdx.x / gridDim.x;
+  const int64_t s1 = total_stages * (blockIdx.x + 1) / gridDim.x;
+  const bool hier = p.kept != nullptr;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---- producer: one lane issues every copy of this CTA's stages, in order
+    if (lane != 0) return;
+    int64_t issued = 0;
+    StageCursor si;
+    si.begin(p, s0, stages_per_unit);
+    for (int64_t gs = s0; gs < s1; ++gs, ++issued) {
+      const int64_t k = gs - s0;
+      const int slot = (int)(k % C::stages);
+      const uint32_t round = (uint32_t)(k / C::stages);
+      if (k > 0) si.next(p, stages_per_unit);
+      if (round > 0 && !mbar_wait(&empty[slot], (round - 1) & 1u)) {
+        report(p.hdr, CSA_ERR_TIMEOUT, KID_INDEX_SCORE, (uint32_t)blockIdx.x);
+        break;
+      }
+      const uint32_t bytes = (uint32_t)si.valid * C::BB;
+      if (bytes) {
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_g2s(smem + slot * C::stage_bytes, p.keys + si.b * p.keys_stride_b + si.id0 * C::BB, bytes,
+                 &full[slot]);
+      } else {
+        mbar_arrive(&full[slot]);
+      }
+    }
+    // the CTA must not exit while a copy into its shared memory is still in flight
+    for (int64_t k = issued - C::stages < 0 ? 0 : issued - C::stages; k < issued; ++k) {
+      if (!mbar_wait(&full[k % C::stages], (uint32_t)(k / C::stages) & 1u)) {
+        report(p.hdr, CSA_ERR_TIMEOUT, KID_INDEX_SCORE, (uint32_t)blockIdx.x);
+        break;
+      }
+    }
+    return;
+  }
+
+  // ---- consumers
+  const int r = lane >> 2, c = lane & 3;
+  float w0 = 1.0f, w1 = 1.0f;
+  if (p.head_w) { w0 = __ldg(p.head_w + (2 * c) % HI); w1 = __ldg(p.head_w + (2 * c + 1) % HI); }
+  uint32_t bq[KS][2];
+  StageCursor si;
+  si.begin(p, s0, stages_per_unit);
+  load_qfrag<DI, HI>(p, si.b, hier ? si.jq0 : (int64_t)(r / HI), lane, bq);
+  for (int64_t gs = s0; gs < s1; ++gs) {
+    const int64_t k = gs - s0;
+    const int slot = (int)(k % C::stages);
+    const uint32_t round = (uint32_t)(k / C::stages);
+    if (k > 0 && si.next(p, stages_per_unit))
+      load_qfrag<DI, HI>(p, si.b, hier ? si.jq0 : (int64_t)(r / HI), lane, bq);
+    const int64_t jq0 = si.jq0;
+    if (!mbar_wait(&full[slot], round & 1u)) {
+      if (lane == 0) report(p.hdr, CSA_ERR_TIMEOUT, KID_INDEX_SCORE, (uint32_t)blockIdx.x);
+      return;
+    }
+    const uint8_t* st = smem + slot * C::stage_bytes;
+    const int i0 = 2 * warp;
+    const bool ok0 = i0 < si.valid, ok1 = i0 + 1 < si.valid;
+    RowRaw<DI> ra, rb;
+    if (ok0) load_row_smem<DI>(st + i0 * C::BB, r, c, ra); else zero_row<DI>(ra);
+    if (ok1) load_row_smem<DI>(st + (i0 + 1) * C::BB, r, c, rb); else zero_row<DI>(rb);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (si.slot0 + i0 >= p.n_slots) continue;
+
+    uint32_t sa[GPL], sb[GPL];
+#pragma unroll
+    for (int gi = 0; gi < GPL; ++gi) {
+      sa[gi] = e4m3_to_f16x2_bcast((ra.scale >> (8 * gi)) & 0xFFu);
+      sb[gi] = e4m3_to_f16x2_bcast((rb.scale >> (8 * gi)) & 0xFFu);
+    }
+    uint32_t af[KS][4];
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) a_frag<DI>(ra, rb, sa, sb, kk, af[kk]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) mma16816(acc, af[kk], bq[kk][0], bq[kk][1]);
+
+    float tv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float d = p.relu ? fmaxf(acc[i], 0.0f) : acc[i];
+      tv[i] = __fmul_rn((i & 1) ? w1 : w0, d);
+    }
+    float sc[2][QPL];
+    if constexpr (HI == 1) {
+      sc[0][0] = tv[0]; sc[0][1] = tv[1]; sc[1][0] = tv[2]; sc[1][1] = tv[3];
+    } else {
+      const int base = (lane & ~3) | (c - c % LPQ);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float acc_s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < LPQ; ++i) {
+          const float x0 = __shfl_sync(0xffffffffu, tv[2 * half], base + i);
+          const float x1 = __shfl_sync(0xffffffffu, tv[2 * half + 1], base + i);
+          acc_s = (i == 0) ? x0 : __fadd_rn(acc_s, x0);
+          acc_s = __fadd_rn(acc_s, x1);
+        }
+        sc[half][0] = acc_s;
+      }
+    }
+    const int64_t eA = (si.id0 + i0) * kBlockEntries + r;
+    const int64_t eB = eA + kBlockEntries;
+#pragma unroll
+    for (int kq = 0; kq < QPL; ++kq) {
+      const int64_t jq = hier ? jq0 : (HI == 1 ? 2 * c + kq : c / LPQ);
+      int64_t pos = INT64_MAX;
+      if (p.q_pos != nullptr && jq < p.n_query) pos = p.q_pos[si.b * p.n_query + jq];
+      const bool vA = ok0 && eA < si.n_e && 2 * eA + 1 <= pos;
+      const bool vB = ok1 && eB < si.n_e && 2 * eB + 1 <= pos;
+      float mA = vA ? __fadd_rn(sc[0][kq], 0.0f) : -INFINITY;
+      float mB = vB ? __fadd_rn(sc[1][kq], 0.0f) : -INFINITY;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, off));
+        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, off));
+      }
+      const bool owner = (r == 0) && (HI == 1 || c % LPQ == 0) && jq < p.n_query;
+      if (owner) {
+        const int64_t row = hier ? si.unit : si.b * p.n_query + jq;
+        float* dst = p.scores + row * p.score_stride + si.slot0 + i0;
+        dst[0] = mA;
+        if (si.slot0 + i0 + 1 < p.n_slots) dst[1] = mB;
+      }
+    }
+  }
+}
+
 template <int DI, int HI>
 cudaError_t launch_score_t(const ScoreParams& p, int num_sms, cudaStream_t s) {
+  constexpr int QPM = HI >= 8 ? 1 : 8 / HI;
+  if (p.kept != nullptr || p.n_query <= QPM) {
+    // every unit's queries fit one MMA column group: stream the keys through shared memory
+    using C = StreamCfg<DI>;
+    const int64_t units = p.kept ? p.batch * p.n_query : p.batch;
+    const int64_t spu = (p.n_slots + kStageBlocks - 1) / kStageBlocks;
+    const int64_t total = units * spu;
+    int64_t grid = 2 * (int64_t)num_sms;
+    if (grid > total) grid = total;
+    if (grid < 1) return cudaSuccess;
+    cudaError_t e = ensure_smem_limit(index_stream_kernel<DI, HI>, C::smem);
+    if (e != cudaSuccess) return e;
+    clear_stale_error();
+    index_stream_kernel<DI, HI><<<(unsigned)grid, kStreamThreads, C::smem, s>>>(p, total, spu);
+    return cudaGetLastError();
+  }
   const int64_t units_y = p.kept ? p.batch * p.n_query : p.batch;
   const int64_t tiles = (p.n_slots + 1) / 2;
   constexpr int kThreads = 256, kWarps = kThreads / 32;

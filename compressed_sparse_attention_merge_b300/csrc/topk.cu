@@ -141,13 +141,142 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
   for (uint32_t pos = taken_before + tid; pos < k; pos += kTopkThreads) out[pos] = -1;
 }
 
+// Register-resident variant for n <= 1024 * KPT: thread t holds the keys of ids [t KPT, t KPT + KPT), so
+// thread order is id order. Histogram atomics are aggregated per warp over equal digits (long runs of
+// equal scores are common), the bin search runs in one warp, and one block scan of packed
+// (equal-count, greater-count) pairs places every selected id.
+template <int KPT>
+__global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkParams p) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t warp_sums[32];
+  __shared__ uint32_t s_prefix, s_krem, s_ncand;
+  const int64_t unit = blockIdx.x;
+  const float* sc = p.scores + unit * p.score_stride;
+  int32_t* out = p.out + unit * p.out_stride;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  uint32_t key[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const int64_t id = (int64_t)tid * KPT + i;
+    key[i] = id < p.n ? order_key(__ldg(sc + id)) : 0u;     // 0 < key of -inf: never a candidate
+  }
+  const uint32_t k = (uint32_t)p.k;
+  uint32_t prefix = 0u, mask = 0u, krem = k, ncand = 0u;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const bool in = key[i] > kNegInfKey && (key[i] & mask) == prefix;
+      const uint32_t digit = in ? (key[i] >> shift) & 0xFFu : 256u;
+      const uint32_t same = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(same) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(same));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns bins 255 - 8 l .. 248 - 8 l (descending)
+      uint32_t b[8], own = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { b[i] = hist[255 - 8 * lane - i]; own += b[i]; }
+      uint32_t incl = own;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      if (shift == 24 && lane == 0) s_ncand = total;
+      const uint32_t hit = __ballot_sync(0xffffffffu, incl >= krem);
+      if (hit != 0u && lane == __ffs(hit) - 1) {
+        uint32_t cum = incl - own;
+        int i = 0;
+        for (; i < 7; ++i) {
+          if (cum + b[i] >= krem) break;
+          cum += b[i];
+        }
+        s_krem = krem - cum;
+        s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+      }
+      if (hit == 0u && lane == 0) { s_krem = 0u; s_prefix = prefix; }   // fewer candidates than k
+    }
+    __syncthreads();
+    if (shift == 24) {
+      ncand = s_ncand;
+      if (ncand <= k) break;          // every candidate is taken
+    }
+    krem = s_krem;
+    prefix = s_prefix;
+    mask |= 0xFFu << shift;
+    __syncthreads();
+  }
+  const bool take_all = ncand <= k;
+  const uint32_t T = take_all ? kNegInfKey : prefix;
+  const uint32_t need_eq = take_all ? 0u : krem;
+
+  uint32_t gt = 0u, eq = 0u;
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    gt += key[i] > T ? 1u : 0u;
+    eq += (!take_all && key[i] == T) ? 1u : 0u;
+  }
+  // exclusive block scan of (eq << 16 | gt); both totals stay below 2^16
+  const uint32_t v = (eq << 16) | gt;
+  uint32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const uint32_t excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0u);
+  const uint32_t tot = warp_sums[31];
+  uint32_t eq_before = excl >> 16;
+  uint32_t pos = (excl & 0xFFFFu) + (eq_before < need_eq ? eq_before : need_eq);
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    bool take = key[i] > T;
+    if (!take_all && key[i] == T) {
+      take = eq_before < need_eq;
+      ++eq_before;
+    }
+    if (take) {
+      const int64_t idx = (int64_t)tid * KPT + i;
+      int32_t id = (int32_t)idx;
+      if (p.map_super != nullptr) {
+        const int32_t g = p.map_super[unit * p.map_stride + idx / kSuper];
+        id = g * kSuper + (int32_t)(idx % kSuper);
+      }
+      if (pos < k) out[pos] = id;
+      ++pos;
+    }
+  }
+  const uint32_t eq_tot = tot >> 16;
+  const uint32_t taken = (tot & 0xFFFFu) + (eq_tot < need_eq ? eq_tot : need_eq);
+  for (uint32_t q = taken + tid; q < k; q += kTopkThreads) out[q] = -1;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
   if (p.units == 0) return cudaSuccess;
   ProfScope prof("topk", s);
   clear_stale_error();
-  topk_kernel<<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
+  if (p.n <= 4 * kTopkThreads) topk_reg_kernel<4><<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
+  else if (p.n <= 8 * kTopkThreads) topk_reg_kernel<8><<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
+  else if (p.n <= 16 * kTopkThreads) topk_reg_kernel<16><<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
+  else topk_kernel<<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
