@@ -78,11 +78,12 @@ class DecodeWorkload:
     """Packed caches, queries and windows of a decode workload on one device, with `replicas` copies
     of the caches so that consecutive steps read different memory."""
 
-    def __init__(self, case, device, replicas):
+    def __init__(self, case, device, replicas, keep_inputs=False):
         from compressed_sparse_attention_merge_b300 import binding as csa
         from compressed_sparse_attention_merge_b300 import synth
         self.csa, self.case, self.device = csa, case, device
         d = synth.make_decode(case, device)
+        self.inputs = dict(d) if keep_inputs else None
         B, E, T = case.batch, case.max_entries, case.max_tokens
         self.B, self.E = B, E
         self.hier = case.hier_keep > 0
@@ -121,9 +122,9 @@ class DecodeWorkload:
         self.ws_pack = ws
         self.queries_per_step = B * case.n_query
 
-    def step(self, r, q=None, q_idx=None, new_tokens=None, new_keys=None, out=None):
+    def step(self, r, q=None, q_idx=None, new_tokens=None, new_keys=None, out=None, layer_outs=None):
         """One decode step on replica r. Optional arguments replace the resident inputs (end-to-end
-        mode passes freshly copied ones)."""
+        mode passes freshly copied ones); layer_outs, if given, receives every layer's output."""
         csa, c = self.csa, self.case
         q = self.q if q is None else q
         q_idx = self.q_idx if q_idx is None else q_idx
@@ -143,7 +144,8 @@ class DecodeWorkload:
                                max_entries=self.E, top_k=c.top_k, ws=self.ws_index, coarse_sum=coarse,
                                keep_blocks=c.hier_keep)
                 n_idx += 1
-            csa.sparse_attn_decode(q[layer], cache, self.n_entries, self.idx[src], out, max_entries=self.E,
+            o = out if layer_outs is None else layer_outs[layer]
+            csa.sparse_attn_decode(q[layer], cache, self.n_entries, self.idx[src], o, max_entries=self.E,
                                    window=c.window, scale=SCALE, ws=self.ws_attn, swa=self.swa[layer],
                                    swa_len=self.swa_len)
         return out
@@ -182,11 +184,12 @@ class PrefillWorkload:
     """A prefill chunk at the end of a long context: the prior cache is built once; each step packs the
     chunk, selects per position and attends."""
 
-    def __init__(self, case, device, replicas):
+    def __init__(self, case, device, replicas, keep_inputs=False):
         from compressed_sparse_attention_merge_b300 import binding as csa
         from compressed_sparse_attention_merge_b300 import synth
         self.csa, self.case, self.device = csa, case, device
         d = synth.make_prefill(case, device)
+        self.inputs = dict(d) if keep_inputs else None
         E, P = case.max_entries, case.first_pos
         self.E = E
         ws = csa.workspace(256, device)
@@ -261,11 +264,11 @@ class PrefillWorkload:
         return {"q": self.q, "q_idx": self.q_idx, "new_tokens": self.chunk, "new_keys": self.chunk_keys}
 
 
-def make_workload(name, device, replicas):
+def make_workload(name, device, replicas, keep_inputs=False):
     case = _cases()[name]
     if name.startswith("prefill"):
-        return PrefillWorkload(case, device, replicas)
-    return DecodeWorkload(case, device, replicas)
+        return PrefillWorkload(case, device, replicas, keep_inputs)
+    return DecodeWorkload(case, device, replicas, keep_inputs)
 
 
 def touched_bytes(w):
