@@ -28,7 +28,6 @@
 #include <cuda.h>
 
 #include <cstring>
-#include <mutex>
 
 #include "csa_internal.cuh"
 #include "tc.cuh"
@@ -621,26 +620,6 @@ __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
 }
 
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda).
-EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-    else
-      (void)cudaGetLastError();
-  });
-  return fn;
-}
-
 }  // namespace
 
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
@@ -650,7 +629,7 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   CUtensorMap map;
   std::memset(&map, 0, sizeof(map));
   if (p.n_wt > 0) {
-    EncodeTiledFn enc = encode_tiled();
+    EncodeTiledFn enc = encode_tiled_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {(cuuint64_t)kLatent, (cuuint64_t)p.swa_rows, (cuuint64_t)(p.units / p.n_query)};
     const cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, (cuuint64_t)p.swa_stride_b * 2};

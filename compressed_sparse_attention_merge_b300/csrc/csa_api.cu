@@ -171,6 +171,21 @@ cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes) {
   return e;
 }
 
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      (void)cudaGetLastError();
+  });
+  return fn;
+}
+
 thread_local char g_last_error[256] = "";
 
 csa_status cuda_fail(cudaError_t e, const char* where) {

@@ -3,6 +3,7 @@
 // scale per 16 elements, block-major layout) from the format definitions themselves.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -70,6 +71,27 @@ __device__ __forceinline__ uint32_t float_to_e4m3_satfinite(float x) {
   uint16_t out;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(out) : "f"(x));
   return out & 0xFFu;
+}
+
+// E2M1 code of y: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 to |y|, ties to the even code (the thresholds
+// alternate between strict and non-strict at the midpoints 0.25, 0.75, ..., 5), saturating at 6; the
+// sign bit copies the sign bit of y.
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
+               (a > 5.0f);
+  return c | ((__float_as_uint(y) >> 31) << 3);
+}
+
+// Smallest power of two >= sf (sf > 0), clamped to [2^-9, 256]; returns the E4M3 byte and the value.
+__device__ __forceinline__ uint32_t pow2_scale(float sf, float* value) {
+  const uint32_t bits = __float_as_uint(sf);
+  const int e = (int)((bits >> 23) & 0xFFu);
+  const uint32_t mant = bits & 0x7FFFFFu;
+  int k = (e == 0) ? -126 : (mant == 0u ? e - 127 : e - 126);
+  k = k < -9 ? -9 : (k > 8 ? 8 : k);
+  *value = __uint_as_float((uint32_t)(k + 127) << 23);
+  return k >= -6 ? (uint32_t)(k + 7) << 3 : (0x08u >> (-6 - k));
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
@@ -240,6 +262,13 @@ template <typename Kernel>
 cudaError_t ensure_smem_limit(Kernel kernel, int bytes) {
   return ensure_smem_limit_fn(reinterpret_cast<const void*>(kernel), bytes);
 }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda);
+// null if the driver does not provide it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
 
 // Records the text of a CUDA runtime failure for csa_last_error() and returns CSA_ERR_CUDA.
 csa_status cuda_fail(cudaError_t e, const char* where);

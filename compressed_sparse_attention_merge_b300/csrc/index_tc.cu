@@ -1,0 +1,520 @@
+// Indexer: block-scaled FP4 products of the index keys with the indexer queries on the fifth-generation
+// tensor cores (tcgen05.mma kind::mxf4nvf4), the weighted ReLU head sum, the causal mask and the maximum
+// over each block of 8 entries; plus the super-block scores of the hierarchical stage.
+//
+// Follows "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" (card), Key ideas: layers
+// "rescore with [their] own indexer query" and select "blocks of 8"; "a hierarchical sparse indexer (up
+// to 2,048 blocks of 8 positions) trims decoder indexing". The score function, the FP4 formats and the
+// super-block shape are this library's readings, stated in include/csa.h.
+//
+// Design. The index keys are stored as E2M1 codes with one E4M3 scale per 16 elements, which is exactly
+// the operand format of the block-scaled FP4 MMA, so the keys are never dequantised: a tensor-map copy
+// streams each stage of 16 blocks (128 entries) into shared memory in the swizzled K-major layout the MMA
+// reads, and the 128 entries are the M side of one product. The queries of one unit (a group of query
+// positions of one sequence, all indexer heads) are rounded to the same FP4 format with power-of-two
+// scales (exact for integer values in [-4, 4]) and form the N side. Each product lands in tensor memory;
+// four epilogue warps (thread = entry) write the keys' scale factors into tensor memory before the product
+// and afterwards apply ReLU, the head weights, the ordered head sum and the causal mask, and take the block
+// maximum across the 8 lanes that hold one block. The accumulator is double-buffered so that the epilogue
+// of one stage overlaps the product of the next.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "csa_internal.cuh"
+#include "tc.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kStageBlocks = 16;
+constexpr int kStageRows = kStageBlocks * kBlockEntries;     // 128 = M of the product
+constexpr int kStages = 6;
+constexpr int kThreads = 192;                                 // warp 0 copies, 1 MMA, 2-5 scales + epilogue
+
+template <int DI, int N>
+struct Cfg {
+  static constexpr int kRowCodes = DI / 2;
+  static constexpr int kRowScales = DI / kGroup;
+  static constexpr int kMmas = DI / 64;                       // K = 64 elements per block-scaled MMA
+  static constexpr int kCodesStage = kStageRows * kRowCodes;
+  static constexpr int kScalesStage = kStageRows * kRowScales;
+  static constexpr uint32_t kSwizzle = DI == 64 ? 6u : (DI == 128 ? 4u : 2u);   // 32, 64, 128-byte swizzle
+  static constexpr int kSwzShift = DI == 64 ? 2 : (DI == 128 ? 1 : 0);
+  static constexpr int kSwzMask = DI == 64 ? 1 : (DI == 128 ? 3 : 7);
+  static constexpr uint32_t kSbo = 8 * kRowCodes;
+  // shared memory (bytes)
+  static constexpr int kCodesOff = 0;
+  static constexpr int kScalesOff = kCodesOff + kStages * kCodesStage;
+  static constexpr int kQOff = kScalesOff + kStages * kScalesStage;                // N rows of query codes
+  static constexpr int kQScOff = kQOff + N * kRowCodes;                            // N x DI/16 query scales
+  static constexpr int kPosOff = (kQScOff + N * kRowScales + 7) & ~7;             // NQ query positions
+  static constexpr int kBarOff = (kPosOff + 4 * N + 7) & ~7;
+  static constexpr int kSmem = kBarOff + (3 * kStages + 2 * 4 + 2) * 8 + 16;
+  // pipeline depth in tensor memory: accumulator buffers and key-scale buffers (scales are written two
+  // stages ahead of the product that reads them)
+  static constexpr int kND = N <= 16 ? 4 : 2;
+  static constexpr int kNSF = 4;
+  static constexpr int kLook = 2;
+  // tensor memory columns
+  static constexpr uint32_t kColD = 0;                              // kND x N
+  static constexpr uint32_t kColSFA = kND * N;                      // kNSF x (4 per MMA)
+  static constexpr uint32_t kColSFB = kColSFA + kNSF * 4 * kMmas;   // 4 per MMA
+  static constexpr uint32_t kColsUsed = kColSFB + 4 * kMmas;
+  static constexpr uint32_t kTmemCols = kColsUsed <= 32 ? 32 : (kColsUsed <= 64 ? 64 : (kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512)));
+};
+
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B, UE4M3 scale factors, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void st_32x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void ld_32x16(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+               :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
+                  "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+                  "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* hdr) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  report(hdr, CSA_ERR_TIMEOUT, KID_INDEX_SCORE, blockIdx.x);
+  return false;
+}
+
+__device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
+    if (done) return;
+  }
+}
+
+// The FP4 rounding of 16 query values that both sides of the indexer use: power-of-two scale (the
+// POW2 rule of the cache), E2M1 codes. Returns the scale byte; codes are packed two per byte.
+__device__ __forceinline__ uint32_t quantize16_pow2(const float* v, uint32_t* lo, uint32_t* hi) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  const float sf = __fdiv_rn(amax, 6.0f);
+  uint32_t sbyte = 0;
+  float s = 0.0f;
+  if (sf > 0.0f) sbyte = pow2_scale(sf, &s);
+  *lo = 0;
+  *hi = 0;
+  if (s > 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t byte = e2m1_code(__fdiv_rn(v[2 * j], s)) | (e2m1_code(__fdiv_rn(v[2 * j + 1], s)) << 4);
+      if (j < 4) *lo |= byte << (8 * j); else *hi |= byte << (8 * (j - 4));
+    }
+  }
+  return sbyte;
+}
+
+struct IdxUnit {
+  int64_t b, j0, row0, n_e, n_b;
+  int nq;              // valid queries of the unit
+};
+
+template <int DI, int HI, int N>
+__global__ void __launch_bounds__(kThreads, 1)
+index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int groups_per_seq,
+                const __grid_constant__ CUtensorMap codes_map, const __grid_constant__ CUtensorMap scales_map) {
+  using C = Cfg<DI, N>;
+  constexpr int NQ = N / HI;                    // query slots of the unit (columns n = q * HI + h)
+  constexpr uint32_t kIdesc = idesc_mxf4(kStageRows, N);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint64_t* empty = full + kStages;
+  uint64_t* sfr = empty + kStages;
+  uint64_t* dfull = sfr + kStages;              // [kND]
+  uint64_t* dempty = dfull + 4;                 // [kND]
+  uint64_t* fin = dempty + 4;                   // [1]
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(fin + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_ptr + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool hier = p.kept != nullptr;
+  const int64_t unit = blockIdx.y;
+  IdxUnit u;
+  if (hier) {
+    u.b = unit / p.n_query; u.j0 = unit % p.n_query; u.nq = 1; u.row0 = unit;
+  } else {
+    u.b = unit / groups_per_seq; u.j0 = (unit % groups_per_seq) * NQ;
+    u.nq = (int)(p.n_query - u.j0 < NQ ? p.n_query - u.j0 : NQ);
+    u.row0 = u.b * p.n_query + u.j0;
+  }
+  int64_t n_e = p.n_entries[u.b];
+  if (n_e < 0 || n_e > p.max_entries) {
+    if (tid == 0 && blockIdx.x == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_INDEX_SCORE, (uint32_t)u.b);
+    n_e = n_e < 0 ? 0 : p.max_entries;
+  }
+  u.n_e = n_e;
+  u.n_b = (n_e + kBlockEntries - 1) / kBlockEntries;
+  const int64_t k0 = stages_per_unit * blockIdx.x / splits;
+  const int64_t k1 = stages_per_unit * (blockIdx.x + 1) / splits;
+  const int n = (int)(k1 - k0);
+
+  // ---------------- setup: barriers, tensor memory, the unit's FP4 queries ----------------
+  if (warp == 1) tc::alloc(tmem_ptr, C::kTmemCols);
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); mbar_init(&sfr[i], 4); }
+    for (int i = 0; i < C::kND; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4); }
+    mbar_init(fin, 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  uint8_t* qcodes = smem + C::kQOff;
+  uint8_t* qsc = smem + C::kQScOff;
+  int32_t* pos_sh = reinterpret_cast<int32_t*>(smem + C::kPosOff);
+  for (int q = tid; q < NQ; q += kThreads)
+    pos_sh[q] = (p.q_pos != nullptr && q < u.nq) ? __ldg(p.q_pos + u.b * p.n_query + u.j0 + q) : INT32_MAX;
+  for (int t = tid; t < N * C::kRowScales; t += kThreads) {
+    const int row = t / C::kRowScales, g = t % C::kRowScales;       // row = q * HI + h
+    const int q = row / HI, h = row % HI;
+    float v[16];
+    const bool have = q < u.nq && h < HI;
+    const float* src = p.q_idx + ((u.b * p.n_query + u.j0 + q) * HI + h) * (int64_t)DI + g * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = have ? __ldg(src + j) : 0.0f;
+    uint32_t lo, hi;
+    const uint32_t sb = quantize16_pow2(v, &lo, &hi);
+    const int chunk = (g * 8) >> 4, within = (g * 8) & 15;
+    uint8_t* dst = qcodes + row * C::kRowCodes + ((chunk ^ ((row >> C::kSwzShift) & C::kSwzMask)) << 4) + within;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+    qsc[row * C::kRowScales + g] = (uint8_t)sb;
+  }
+  tc::fence_proxy_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tmem_ptr;
+
+  if (warp >= 2) {
+    // query scale factors: column n at lane 32 j + n % 32, column kColSFB + 4 s + n / 32, for every
+    // subpartition j (each epilogue warp writes its own copy)
+    const int sp = warp & 3;
+    const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
+#pragma unroll
+    for (int s = 0; s < C::kMmas; ++s) {
+#pragma unroll
+      for (int c = 0; c < (N + 31) / 32; ++c) {
+        const int nn = lane + 32 * c;
+        uint32_t w = 0;
+        if (nn < N) w = *reinterpret_cast<const uint32_t*>(qsc + nn * C::kRowScales + 4 * s);
+        st_32x1(tbase + lane_base + C::kColSFB + 4 * s + c, w);
+      }
+    }
+    tc::wait_st();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+
+  const uint32_t s_base = smem_addr(smem);
+  if (warp == 0) {
+    // ---------------- tensor-map copies of the key stages ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int k = 0; k < n; ++k) {
+        const int slot = k % kStages;
+        if (k >= kStages && !wait_or_abort(&empty[slot], ((k / kStages) - 1) & 1, abort_flag, p.hdr)) break;
+        const int64_t st = k0 + k;
+        int64_t id0 = st * kStageBlocks;
+        if (hier) {
+          const int32_t g = p.kept[unit * p.keep_super + (st >> 2)];
+          id0 = g < 0 ? -1 : (int64_t)g * kSuper + (st & 3) * kStageBlocks;
+        }
+        if (id0 >= 0 && id0 < u.n_b) {
+          mbar_arrive_expect_tx(&full[slot], C::kCodesStage + C::kScalesStage);
+          tma_load_4d(smem + C::kCodesOff + slot * C::kCodesStage, &codes_map, 0, 0, (int)id0, (int)u.b, &full[slot]);
+          tma_load_3d(smem + C::kScalesOff + slot * C::kScalesStage, &scales_map, 0, (int)id0, (int)u.b, &full[slot]);
+        } else {
+          mbar_arrive(&full[slot]);
+        }
+        ++issued;
+      }
+      for (int k = issued - kStages < 0 ? 0 : issued - kStages; k < issued; ++k)
+        drain(&full[k % kStages], (k / kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- products ----------------
+    if (lane == 0) {
+      for (int k = 0; k < n; ++k) {
+        const int slot = k % kStages, db = k % C::kND, sb = k % C::kNSF;
+        if (!wait_or_abort(&sfr[slot], (k / kStages) & 1, abort_flag, p.hdr)) break;
+        if (k >= C::kND && !wait_or_abort(&dempty[db], ((k / C::kND) - 1) & 1, abort_flag, p.hdr)) break;
+        tc::fence_after();
+        const uint32_t a0 = s_base + C::kCodesOff + slot * C::kCodesStage;
+        const uint32_t b0 = s_base + C::kQOff;
+#pragma unroll
+        for (int s = 0; s < C::kMmas; ++s) {
+          const uint64_t a = tc::smem_desc(a0 + 32 * s, 16, C::kSbo, C::kSwizzle);
+          const uint64_t b = tc::smem_desc(b0 + 32 * s, 16, C::kSbo, C::kSwizzle);
+          mma_mxf4(tbase + C::kColD + db * N, a, b, kIdesc, tbase + C::kColSFA + sb * 4 * C::kMmas + 4 * s,
+                   tbase + C::kColSFB + 4 * s, s > 0 ? 1u : 0u);
+        }
+        tc::commit(&empty[slot]);
+        tc::commit(&dfull[db]);
+      }
+      tc::commit(fin);
+      drain(fin, 0);
+    }
+  } else {
+    // ---------------- key scale factors and epilogue (thread = entry row of the stage) ----------------
+    const int sp = warp & 3;
+    const int m = sp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
+    float w[HI];
+#pragma unroll
+    for (int h = 0; h < HI; ++h) w[h] = p.head_w ? __ldg(p.head_w + h) : 1.0f;
+    // key scale factors of stage k into scale buffer k % kNSF (lane m, column base + 4 s + m / 32)
+    auto write_scales = [&](int k) -> bool {
+      const int slot = k % kStages;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&full[slot], (k / kStages) & 1, abort_flag, p.hdr))) return false;
+      const uint8_t* sc = smem + C::kScalesOff + slot * C::kScalesStage + (m >> 3) * (8 * C::kRowScales) +
+                          (m & 7) * C::kRowScales;
+#pragma unroll
+      for (int s = 0; s < C::kMmas; ++s)
+        st_32x1(tbase + lane_base + C::kColSFA + (k % C::kNSF) * 4 * C::kMmas + 4 * s + sp,
+                *reinterpret_cast<const uint32_t*>(sc + 4 * s));
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfr[slot]);
+      return true;
+    };
+    bool ok = true;
+    for (int k = 0; k < C::kLook && k < n && ok; ++k) ok = write_scales(k);
+    for (int k = 0; k < n && ok; ++k) {
+      if (k + C::kLook < n && !write_scales(k + C::kLook)) break;
+      const int db = k % C::kND;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&dfull[db], (k / C::kND) & 1, abort_flag, p.hdr))) break;
+      tc::fence_after();
+      const int64_t st = k0 + k;
+      const int64_t slot0 = st * kStageBlocks;
+      int64_t id0 = slot0;
+      if (hier) {
+        const int32_t g = p.kept[unit * p.keep_super + (st >> 2)];
+        id0 = g < 0 ? -1 : (int64_t)g * kSuper + (st & 3) * kStageBlocks;
+      }
+      const int64_t blk = id0 + (m >> 3);
+      const int64_t e = blk * kBlockEntries + (m & 7);
+      const bool row_ok = id0 >= 0 && blk < u.n_b && e < u.n_e;
+      const int64_t slot = slot0 + (m >> 3);
+#pragma unroll
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        if (c0 >= u.nq * HI) break;
+        uint32_t r[16];
+        ld_32x16(tbase + lane_base + C::kColD + db * N + c0, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int qq = 0; qq < 16 / HI; ++qq) {
+          const int q = c0 / HI + qq;
+          if (q >= NQ || q >= u.nq) break;
+          float sum = 0.0f;
+#pragma unroll
+          for (int h = 0; h < HI; ++h) {
+            const float dot = __uint_as_float(r[qq * HI + h]);
+            const float t = __fmul_rn(w[h], p.relu ? fmaxf(dot, 0.0f) : dot);
+            sum = h == 0 ? t : __fadd_rn(sum, t);
+          }
+          const bool okq = row_ok && 2 * e + 1 <= (int64_t)pos_sh[q];
+          float mx = okq ? __fadd_rn(sum, 0.0f) : -INFINITY;
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          if ((lane & 7) == 0 && slot < p.n_slots) {
+            const int64_t row = hier ? u.row0 : u.row0 + q;
+            p.scores[row * p.score_stride + slot] = mx;
+          }
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dempty[db]);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (warp == 1) tc::dealloc(tbase, C::kTmemCols);
+}
+
+// Super-block scores: one warp per (unit, super-block), lanes over the feature index; the query is the
+// same FP4 rounding (power-of-two scale per 16 elements) as in the block products.
+__global__ void __launch_bounds__(256) coarse_score_kernel(CoarseScoreParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t units = p.batch * p.n_query;
+  if (gw >= units * p.n_super) return;
+  const int64_t unit = gw / p.n_super, g = gw % p.n_super;
+  const int64_t b = unit / p.n_query;
+  const int64_t n_e = p.n_entries[b];
+  float* dst = p.scores + unit * p.n_super + g;
+  if (g * (int64_t)kSuper * kBlockEntries >= n_e) {
+    if (lane == 0) *dst = -INFINITY;
+    return;
+  }
+  const float* crow = p.coarse + b * p.coarse_stride_b + g * p.dim;
+  float s = 0.0f;
+  for (int h = 0; h < p.heads; ++h) {
+    const float* qrow = p.q_idx + (unit * p.heads + h) * (int64_t)p.dim;
+    float d = 0.0f;
+    for (int i0 = 0; i0 < p.dim; i0 += 32) {
+      // lanes i0 .. i0+31 hold two 16-element groups; round each to FP4 like the block products do
+      const float x = __ldg(qrow + i0 + lane);
+      float amax = fabsf(x);
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float sf = __fdiv_rn(amax, 6.0f);
+      float sc = 0.0f;
+      if (sf > 0.0f) pow2_scale(sf, &sc);
+      float xq = 0.0f;
+      if (sc > 0.0f) {
+        const uint32_t code = e2m1_code(__fdiv_rn(x, sc));
+        const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+        xq = __fmul_rn((code & 8u) ? -mag[code & 7u] : mag[code & 7u], sc);
+      }
+      d = fmaf(xq, __ldg(crow + i0 + lane), d);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (p.relu) d = fmaxf(d, 0.0f);
+    const float wgt = p.head_w ? __ldg(p.head_w + h) : 1.0f;
+    const float t = __fmul_rn(wgt, d);
+    s = (h == 0) ? t : __fadd_rn(s, t);
+  }
+  if (lane == 0) *dst = __fadd_rn(s, 0.0f);
+}
+
+template <int DI, int HI, int N>
+cudaError_t launch_tc(const ScoreParams& p, int num_sms, cudaStream_t s) {
+  using C = Cfg<DI, N>;
+  constexpr int NQ = N / HI;
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const int64_t n_b_cap = (p.max_entries + kBlockEntries - 1) / kBlockEntries;
+  const int64_t bb = block_bytes(DI);
+  const int64_t seq_stride = p.batch > 1 ? p.keys_stride_b : n_b_cap * bb;
+  CUtensorMap codes_map, scales_map;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)(DI / 2), 8, (cuuint64_t)n_b_cap, (cuuint64_t)p.batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)(DI / 2), (cuuint64_t)bb, (cuuint64_t)seq_stride};
+    const cuuint32_t box[4] = {(cuuint32_t)(DI / 2), 8, (cuuint32_t)kStageBlocks, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapSwizzle swz = DI == 64 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                            : (DI == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+    if (enc(&codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.keys), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)(DI / 2), (cuuint64_t)n_b_cap, (cuuint64_t)p.batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)bb, (cuuint64_t)seq_stride};
+    const cuuint32_t box[3] = {(cuuint32_t)(DI / 2), (cuuint32_t)kStageBlocks, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&scales_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.keys) + kBlockEntries * (DI / 2), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const bool hier = p.kept != nullptr;
+  const int groups_per_seq = hier ? 1 : (int)((p.n_query + NQ - 1) / NQ);
+  const int64_t units = hier ? p.batch * p.n_query : p.batch * groups_per_seq;
+  const int64_t spu = (p.n_slots + kStageBlocks - 1) / kStageBlocks;
+  // a few CTAs per SM in total (as many as tensor memory allows), each with a contiguous range of one
+  // unit's stages
+  const int per_sm = (int)(512 / C::kTmemCols) < 4 ? (int)(512 / C::kTmemCols) : 4;
+  int64_t splits = (int64_t)num_sms * per_sm / units;
+  if (splits > spu) splits = spu;
+  if (splits < 1) splits = 1;
+  if (units > 65535) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_smem_limit(index_tc_kernel<DI, HI, N>, C::kSmem);
+  if (e != cudaSuccess) return e;
+  clear_stale_error();
+  dim3 grid((unsigned)splits, (unsigned)units);
+  index_tc_kernel<DI, HI, N><<<grid, kThreads, C::kSmem, s>>>(p, spu, (int)splits, groups_per_seq, codes_map,
+                                                              scales_map);
+  return cudaGetLastError();
+}
+
+template <int DI, int HI>
+cudaError_t launch_h(const ScoreParams& p, int num_sms, cudaStream_t s) {
+  // one unit per query group that fits 16 columns (decode), else 64 columns (64 / HI query positions)
+  if (p.kept != nullptr || p.n_query * HI <= 16) return launch_tc<DI, HI, 16>(p, num_sms, s);
+  return launch_tc<DI, HI, 64>(p, num_sms, s);
+}
+
+template <int DI>
+cudaError_t launch_d(const ScoreParams& p, int num_sms, cudaStream_t s) {
+  switch (p.heads) {
+    case 1: return launch_h<DI, 1>(p, num_sms, s);
+    case 2: return launch_h<DI, 2>(p, num_sms, s);
+    case 4: return launch_h<DI, 4>(p, num_sms, s);
+    case 8: return launch_h<DI, 8>(p, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s) {
+  if (p.n_slots == 0) return cudaSuccess;
+  ProfScope prof(p.kept ? "index_score_hier" : "index_score", s);
+  switch (p.dim) {
+    case 64: return launch_d<64>(p, num_sms, s);
+    case 128: return launch_d<128>(p, num_sms, s);
+    case 256: return launch_d<256>(p, num_sms, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s) {
+  const int64_t warps = p.batch * p.n_query * p.n_super;
+  if (warps == 0) return cudaSuccess;
+  ProfScope prof("coarse_score", s);
+  const int64_t blocks = (warps + 7) / 8;
+  clear_stale_error();
+  coarse_score_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -35,27 +35,6 @@ __device__ __forceinline__ void load16(const void* base, int dtype, int64_t elem
   }
 }
 
-// E2M1 code of y: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 to |y|, ties to the even code (the thresholds
-// alternate between strict and non-strict at the midpoints 0.25, 0.75, ..., 5), saturating at 6; the
-// sign bit copies the sign bit of y.
-__device__ __forceinline__ uint32_t e2m1_code(float y) {
-  const float a = fabsf(y);
-  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
-               (a > 5.0f);
-  return c | ((__float_as_uint(y) >> 31) << 3);
-}
-
-// Smallest power of two >= sf (sf > 0), clamped to [2^-9, 256]; returns the E4M3 byte and the value.
-__device__ __forceinline__ uint32_t pow2_scale(float sf, float* value) {
-  const uint32_t bits = __float_as_uint(sf);
-  const int e = (int)((bits >> 23) & 0xFFu);
-  const uint32_t mant = bits & 0x7FFFFFu;
-  int k = (e == 0) ? -126 : (mant == 0u ? e - 127 : e - 126);
-  k = k < -9 ? -9 : (k > 8 ? 8 : k);
-  *value = __uint_as_float((uint32_t)(k + 127) << 23);
-  return k >= -6 ? (uint32_t)(k + 7) << 3 : (0x08u >> (-6 - k));
-}
-
 __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
   const int groups = p.dim / kGroup;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -118,12 +97,17 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
 }
 
 // coarse_sum[b][g][d] = fp32 sum, ascending entry order, of the dequantised element d of entries
-// [512 g, min(512 (g + 1), first + n_new)), for every super-block g touched by this call.
-__global__ void __launch_bounds__(128) coarse_sum_kernel(PackParams p, int touched) {
-  const int d = blockIdx.x * blockDim.x + threadIdx.x;
-  const int gl = blockIdx.y;
-  const int64_t b = blockIdx.z;
-  if (d >= p.dim) return;
+// [512 g, min(512 (g + 1), first + n_new)), for every super-block g touched by this call. One CTA per
+// (super-block, sequence), one thread per element d: the super-block's packed bytes are staged through
+// shared memory in chunks with coalesced 16-byte loads, and each thread then sums its element over the
+// chunk's entries in ascending order.
+constexpr int kCoarseStage = 36864;
+
+__global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touched) {
+  __shared__ __align__(16) uint8_t stage[kCoarseStage];
+  const int d = threadIdx.x;                     // blockDim.x == dim
+  const int gl = blockIdx.x;
+  const int64_t b = blockIdx.y;
   const int64_t first = p.first_entry ? (int64_t)p.first_entry[b] : 0;
   if (first < 0 || first + p.n_new > p.max_entries || p.n_new == 0) return;
   const int64_t end = first + p.n_new;
@@ -132,19 +116,31 @@ __global__ void __launch_bounds__(128) coarse_sum_kernel(PackParams p, int touch
   if (gl >= touched || g * per_super >= end) return;
   const int64_t e_hi = (g + 1) * per_super < end ? (g + 1) * per_super : end;
 
-  const uint8_t* seq = p.cache + b * p.cache_stride_b;
   const int bb = block_bytes(p.dim);
   const int half = p.dim / 2, groups = p.dim / kGroup;
+  const int chunk_blocks = kCoarseStage / bb < kSuper ? kCoarseStage / bb : kSuper;
+  const uint8_t* seq = p.cache + b * p.cache_stride_b;
   const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
   float acc = 0.0f;
-  for (int64_t e = g * per_super; e < e_hi; ++e) {
-    const uint8_t* blk = seq + (e / kBlockEntries) * bb;
-    const int slot = (int)(e % kBlockEntries);
-    const uint32_t byte = blk[slot * half + d / 2];
-    const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 0xFu);
-    const float sc = e4m3_to_float(blk[kBlockEntries * half + slot * groups + d / kGroup]);
-    const float v = __fmul_rn((code & 8u) ? -mag[code & 7u] : mag[code & 7u], sc);
-    acc = __fadd_rn(acc, v);
+  for (int64_t blk0 = g * kSuper; blk0 * kBlockEntries < e_hi; blk0 += chunk_blocks) {
+    const int64_t n_e = e_hi - blk0 * kBlockEntries;
+    const int nb = (int)((n_e + kBlockEntries - 1) / kBlockEntries < chunk_blocks
+                             ? (n_e + kBlockEntries - 1) / kBlockEntries : chunk_blocks);
+    __syncthreads();
+    const uint4* src = reinterpret_cast<const uint4*>(seq + blk0 * bb);
+    for (int i = d; i < nb * bb / 16; i += blockDim.x) reinterpret_cast<uint4*>(stage)[i] = __ldg(src + i);
+    __syncthreads();
+    const int ne = (int)(n_e < (int64_t)nb * kBlockEntries ? n_e : (int64_t)nb * kBlockEntries);
+#pragma unroll 8
+    for (int i = 0; i < ne; ++i) {
+      const uint8_t* blk = stage + (i >> 3) * bb;
+      const int slot = i & 7;
+      const uint32_t byte = blk[slot * half + d / 2];
+      const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 0xFu);
+      const float sc = e4m3_to_float(blk[kBlockEntries * half + slot * groups + d / kGroup]);
+      const float v = __fmul_rn((code & 8u) ? -mag[code & 7u] : mag[code & 7u], sc);
+      acc = __fadd_rn(acc, v);
+    }
   }
   p.coarse_sum[b * p.coarse_stride_b + g * p.dim + d] = acc;
 }
@@ -166,10 +162,10 @@ cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s) {
   if (p.coarse_sum == nullptr || p.n_new == 0 || p.batch == 0) return cudaSuccess;
   const int64_t per_super = (int64_t)kSuper * kBlockEntries;
   const int touched = (int)((p.n_new + per_super - 1) / per_super) + 1;
-  dim3 grid((unsigned)((p.dim + 127) / 128), (unsigned)touched, (unsigned)p.batch);
+  dim3 grid((unsigned)touched, (unsigned)p.batch);
   ProfScope prof("coarse_sum", s);
   clear_stale_error();
-  coarse_sum_kernel<<<grid, 128, 0, s>>>(p, touched);
+  coarse_sum_kernel<<<grid, p.dim, 0, s>>>(p, touched);
   return cudaGetLastError();
 }
 

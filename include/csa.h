@@ -165,9 +165,11 @@ csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* args, void* ws, size
  *
  * Per query u = (b, j):
  *   entry score   s_e = sum over h = 0..H-1, in that order, of fl32(w_h * r_{h,e}),
- *                 r_{h,e} = max(0, q_h . k_e) (plain q_h . k_e without CSA_IDX_RELU),
- *                 k_e the dequantized index key; the dot product is exact when q and k are integers with
- *                 |partial sums| <= 2048 (the kernels multiply in fp16 and accumulate in fp32).
+ *                 r_{h,e} = max(0, q^_h . k_e) (plain q^_h . k_e without CSA_IDX_RELU), where k_e is the
+ *                 dequantized index key and q^_h is the query rounded to the same FP4 format with the
+ *                 CSA_SCALE_POW2 rule (E2M1 codes, one power-of-two scale per 16 elements; the identity for
+ *                 integer values in [-4, 4]). Both enter a block-scaled FP4 tensor-core product with fp32
+ *                 accumulation, exact when the dequantized values are integers and |partial sums| < 2^24.
  *   eligible      e < n_entries[b], and 2e + 1 <= q_pos[b][j] when q_pos is given (prefill causality).
  *   block score   S_blk = max of s_e over eligible entries of the block; blocks with none are not
  *                 candidates.

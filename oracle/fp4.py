@@ -145,6 +145,17 @@ def quantize(m, rule, rows_per_chunk=4096):
     return codes.reshape(n, dim), sb
 
 
+def round_trip(x, rule):
+    """Values of x (float32 [..., dim], dim % 16 == 0) after quantising them with `rule` and
+    dequantising: the FP4 value each element is stored as."""
+    x = np.asarray(x, dtype=np.float32)
+    shape = x.shape
+    rows = x.reshape(-1, shape[-1])
+    codes, scales = quantize(rows, rule)
+    s = np.repeat(e4m3_value(scales), GROUP, axis=1)
+    return (e2m1_value(codes) * s).reshape(shape)
+
+
 def entry_bytes(dim):
     return dim // 2 + dim // GROUP
 

@@ -7,10 +7,14 @@ query" (Reindex) or reuse "Top-K indices" (Reuse); selection is over "blocks of 
 hierarchical sparse indexer (up to 2,048 blocks of 8 positions) trims decoder indexing". The pages give
 no score function, tie rule or hierarchy shape; the readings taken here:
 
-  * entry score s_e = sum over heads h (in order 0, 1, ...) of fl32(w_h * r_h), r_h = max(0, q_h . k_e)
-    with ReLU, plain q_h . k_e without; k_e the dequantised index key shared by all indexer heads. The
-    dot products are taken in fp64 and rounded to fp32 (exact for the integer-valued inputs used
-    throughout); the weighted head sum is taken in fp32 in that fixed order, and -0 is made +0.
+  * both operands of the indexer product are FP4: k_e is the dequantised index key shared by all
+    indexer heads, and the query q_h is rounded to the same FP4 format with the POW2 scale rule (one
+    power-of-two scale per 16 elements), q^_h = dequant(quant_pow2(q_h)). For integer-valued queries
+    in [-4, 4] the rounding is the identity.
+  * entry score s_e = sum over heads h (in order 0, 1, ...) of fl32(w_h * r_h), r_h = max(0, q^_h . k_e)
+    with ReLU, plain q^_h . k_e without. The dot products are taken in fp64 and rounded to fp32 (exact
+    for the integer-valued inputs used throughout); the weighted head sum is taken in fp32 in that fixed
+    order, and -0 is made +0.
   * a block's score is the maximum over its eligible entries; a block with no eligible entry is not a
     candidate (score -inf here).
   * Top-K: the min(K, #candidates) candidates with the largest scores, ties to the lower block id,
@@ -23,14 +27,16 @@ no score function, tie rule or hierarchy shape; the readings taken here:
 
 import numpy as np
 
+from . import fp4
+
 BLOCK = 8
 SUPER = 64
 ENTRIES_PER_SUPER = BLOCK * SUPER
 
 
 def entry_scores(q, keys, head_w=None, relu=True):
-    """q: [Q, H, D] (integer-valued), keys: [n_e, D] dequantised. Returns float32 [Q, n_e]."""
-    q = np.asarray(q, dtype=np.float64)
+    """q: [Q, H, D] (rounded to FP4 here), keys: [n_e, D] dequantised. Returns float32 [Q, n_e]."""
+    q = fp4.round_trip(np.asarray(q, dtype=np.float32), "pow2").astype(np.float64)
     keys = np.asarray(keys, dtype=np.float64)
     nq, nh, d = q.shape
     w = np.ones(nh, np.float32) if head_w is None else np.asarray(head_w, np.float32)

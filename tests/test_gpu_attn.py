@@ -111,7 +111,7 @@ def test_topk_covering_everything_equals_dense(csa):
     idx = torch.tensor(list(range(nb - 1, -1, -1)) + [-1] * 3, dtype=torch.int32, device=DEV).view(1, 1, -1)
     out, lse = gpu_decode_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV), idx, swa,
                                torch.tensor([W], dtype=torch.int32, device=DEV), E, W)
-    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    entries = o_fp4.dequantize(o_fp4.pack(to_np(x)[0], 2, "amax"), 512, E)
     ref, ref_lse = o_attn.dense_attention(to_np(q)[0, 0].astype(np.float64), entries, E, to_np(swa)[0], SCALE)
     assert_attn_close(out[0, 0].cpu().numpy(), ref)
     assert_lse_close(lse[0, 0].cpu().numpy(), ref_lse)
@@ -129,7 +129,7 @@ def test_zero_query_is_mean_of_rows(csa):
     idx = torch.arange(8, dtype=torch.int32, device=DEV).view(1, 1, 8)
     out, lse = gpu_decode_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV), idx, swa,
                                torch.tensor([10], dtype=torch.int32, device=DEV), E, W)
-    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    entries = o_fp4.dequantize(o_fp4.pack(to_np(x)[0], 2, "amax"), 512, E)
     rows = np.concatenate([entries, to_np(swa)[0, :10]])
     np.testing.assert_allclose(out[0, 0].cpu().numpy(), np.broadcast_to(rows.mean(0), (16, 512)), atol=2e-3)
     np.testing.assert_allclose(lse[0, 0].cpu().numpy(), math.log(rows.shape[0]), atol=1e-4)
@@ -165,7 +165,7 @@ def test_out_of_capacity_block_id_is_reported(csa):
     csa.sparse_attn_decode(q, cache, n_entries, idx, out, max_entries=E, window=W, scale=SCALE, ws=ws, swa=swa,
                            swa_len=swa_len)
     assert csa.device_status(ws) == csa.ERR_DEVICE_CHECK
-    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    entries = o_fp4.dequantize(o_fp4.pack(to_np(x)[0], 2, "amax"), 512, E)
     ref, _ = o_attn.decode_attention(to_np(q)[0, 0].astype(np.float64), entries, E, [3, 0], to_np(swa)[0], SCALE)
     assert_attn_close(out[0, 0].cpu().numpy(), ref)
 
@@ -189,7 +189,7 @@ def test_prefill_matches_oracle(csa):
     out, lse = gpu_prefill_attn(csa, q, cache, torch.tensor([E], dtype=torch.int32, device=DEV),
                                 torch.from_numpy(idx_np).to(DEV), torch.from_numpy(pos)[None].to(DEV), swa,
                                 torch.tensor([first], dtype=torch.int32, device=DEV), E, W)
-    entries = o_fp4.dequantize(cache[0].cpu().numpy(), 512, E)
+    entries = o_fp4.dequantize(o_fp4.pack(to_np(x)[0], 2, "amax"), 512, E)
     qf, sf = to_np(q)[0], to_np(swa)[0]
     out, lse = out.cpu().numpy(), lse.cpu().numpy()
     for j in range(Q):

@@ -64,7 +64,7 @@ def test_head_weights_and_no_relu(csa):
     for relu in (True, False):
         idx, scores = gpu_index(csa, q_idx, kc, n_entries, E, 40, head_w=w, relu=relu, want_scores=True)
         for b in range(B):
-            deq = o_fp4.dequantize(kc[b].cpu().numpy(), dim, E)
+            deq = o_fp4.dequantize(o_fp4.pack(keys[b].cpu().numpy(), 1, "pow2"), dim, E)
             ref_idx, ref_S = o_idx.flat_topk(q_idx[b].cpu().numpy(), deq, E, 40, head_w=w.cpu().numpy(),
                                              relu=relu)
             np.testing.assert_array_equal(idx[b].cpu().numpy(), ref_idx)
@@ -92,7 +92,7 @@ def test_prefill_causal_positions(csa):
     kc = gpu_pack_sequences(csa, keys, [E], E, dim, 1, csa.SCALE_POW2, ws)
     idx, scores = gpu_index(csa, q_idx, kc, torch.tensor([E], dtype=torch.int32, device=DEV), E, 20,
                             q_pos=q_pos, want_scores=True)
-    deq = o_fp4.dequantize(kc[0].cpu().numpy(), dim, E)
+    deq = o_fp4.dequantize(o_fp4.pack(keys[0].cpu().numpy(), 1, "pow2"), dim, E)
     ref_idx, ref_S = o_idx.flat_topk(q_idx[0].cpu().numpy(), deq, E, 20, q_pos=pos.numpy())
     np.testing.assert_array_equal(idx[0].cpu().numpy(), ref_idx)
     np.testing.assert_array_equal(scores[0].cpu().numpy()[:, :ref_S.shape[1]], ref_S)
@@ -115,9 +115,27 @@ def test_hierarchical_bit_exact(csa, keep_blocks, top_k):
     n_entries = torch.tensor(lengths, dtype=torch.int32, device=DEV)
     idx, _ = gpu_index(csa, q_idx, kc, n_entries, E, top_k, coarse=coarse, keep_blocks=keep_blocks)
     for b, n in enumerate(lengths):
-        deq = o_fp4.dequantize(kc[b].cpu().numpy(), dim, E)
+        deq = o_fp4.dequantize(o_fp4.pack(keys[b, :n].cpu().numpy(), 1, "pow2", n_blocks=-(-E // 8)), dim, E)
         ref_idx, _ = o_idx.hierarchical_topk(q_idx[b].cpu().numpy(), deq, n, top_k, keep_blocks)
         np.testing.assert_array_equal(idx[b].cpu().numpy(), ref_idx, err_msg=f"seq {b}")
         if keep_blocks >= 64 * (-(-n // 512)):
             flat, _ = o_idx.flat_topk(q_idx[b].cpu().numpy(), deq, n, top_k)
             np.testing.assert_array_equal(idx[b].cpu().numpy(), flat)
+
+
+def test_off_grid_queries_are_rounded_like_the_oracle(csa):
+    # queries outside the E2M1 grid (5, 7, fractions): both sides round them to FP4 with the POW2 rule
+    g = torch.Generator(device=DEV).manual_seed(51)
+    B, E, dim, heads = 2, 900, 128, 4
+    keys = _keys(g, B, E, dim)
+    vals = torch.tensor([5.0, -5.0, 7.0, 0.3, -0.75, 2.5, 1.0, 0.0], device=DEV)
+    q_idx = vals[torch.randint(0, 8, (B, 1, heads, dim), generator=g, device=DEV)]
+    ws = csa.workspace(256, DEV)
+    kc = gpu_pack_sequences(csa, keys, [E, E - 13], E, dim, 1, csa.SCALE_POW2, ws)
+    n_entries = torch.tensor([E, E - 13], dtype=torch.int32, device=DEV)
+    idx, scores = gpu_index(csa, q_idx, kc, n_entries, E, 30, want_scores=True)
+    for b, n in enumerate([E, E - 13]):
+        deq = o_fp4.dequantize(o_fp4.pack(keys[b, :n].cpu().numpy(), 1, "pow2"), dim, n)
+        ref_idx, ref_S = o_idx.flat_topk(q_idx[b].cpu().numpy(), deq, n, 30)
+        np.testing.assert_array_equal(idx[b].cpu().numpy(), ref_idx)
+        np.testing.assert_array_equal(scores[b].cpu().numpy()[:, :ref_S.shape[1]], ref_S)

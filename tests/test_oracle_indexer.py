@@ -113,3 +113,34 @@ def test_coarse_keys_sum_in_order():
     np.testing.assert_array_equal(c[:, 0], [512, 512, 76])
     for a, b in itertools.product(range(2), range(2)):
         assert c[a, b] == 512
+
+
+def test_query_rounding_is_identity_on_small_integers():
+    # every integer in [-4, 4] survives the POW2 FP4 rounding, whatever the group's maximum magnitude
+    rng = np.random.default_rng(11)
+    for a in range(0, 5):
+        for _ in range(200):
+            g = rng.integers(-a, a + 1, 16).astype(np.float32)
+            if a:
+                g[rng.integers(16)] = a * (1 if rng.random() < 0.5 else -1)
+            np.testing.assert_array_equal(fp4.round_trip(g[None], "pow2")[0], g)
+
+
+def test_query_rounding_hand_worked():
+    # amax 5 -> 5/6 -> scale 1; 5 lies halfway between 4 (code 6) and 6 (code 7): ties go to the even code
+    # amax 7 -> 7/6 -> scale 2; 7/2 = 3.5 lies halfway between 3 (code 5) and 4 (code 6) -> 4 -> 8
+    # amax 0.3 -> 0.05 -> scale 2^-4; 0.3 / 2^-4 = 4.8 -> nearest grid value 4 -> 0.25
+    for v, want in [(5.0, 4.0), (-5.0, -4.0), (7.0, 8.0), (0.3, 0.25)]:
+        g = np.zeros(16, np.float32)
+        g[3] = v
+        out = fp4.round_trip(g[None], "pow2")[0]
+        assert out[3] == want and np.all(np.delete(out, 3) == 0)
+
+
+def test_scores_use_the_rounded_query():
+    # a query of 5s scores exactly like a query of 4s (its FP4 rounding), against integer brute force
+    rng = np.random.default_rng(12)
+    k = rng.integers(-4, 5, (64, 64))
+    q = np.full((1, 1, 64), 5.0, np.float32)
+    got = indexer.entry_scores(q, k)
+    np.testing.assert_array_equal(got.astype(np.int64), _int_scores(np.full((1, 1, 64), 4), k, [1], True))
