@@ -43,19 +43,23 @@ constexpr int kRing = 4;
 constexpr int kLatBlk = block_bytes(kLatent);              // 2304
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.0f;                      // log2 headroom before the reference max moves
+constexpr float kMaxProb = 256.0f;                         // 2^kRescaleSlack
 
 // shared-memory map (bytes); the operand regions start on 1024-byte boundaries
 constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB
 constexpr int kQOff = 0;
-constexpr int kRawStage = kTileBlocks * kLatBlk;           // 36,864
+// Staged blocks are padded by 32 bytes so that the same code column of rows in different blocks falls
+// in different shared-memory banks.
+constexpr int kRawBlk = kLatBlk + 32;                      // 2,336
+constexpr int kRawStage = kTileBlocks * kRawBlk;           // 37,376
 constexpr int kRawOff = kQOff + kPanels * kQPanel;         // 65,536
 constexpr int kPanelBytes = kRows * 128;                   // 16 KB
-constexpr int kRingOff = kRawOff + 2 * kRawStage;          // 139,264
+constexpr int kRingOff = (kRawOff + 2 * kRawStage + 1023) & ~1023;   // 141,312
 constexpr int kWinOff = kRawOff;                           // window tile: 8 panels over the raw and ring areas
-constexpr int kPOff = kRingOff + kRing * kPanelBytes;      // 204,800
-constexpr int kOnesOff = kPOff + kRows * 128;              // 221,184
-constexpr int kBarOff = kOnesOff + 1024;                   // 222,208
-constexpr int kNumBars = 20;
+constexpr int kPOff = kRingOff + kRing * kPanelBytes;      // 206,848
+constexpr int kOnesOff = kPOff + kRows * 128;              // 223,232
+constexpr int kBarOff = kOnesOff + 1024;                   // 224,256
+constexpr int kNumBars = 24;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
 constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort
 constexpr int kMOff = kFlagOff + 16;                       // float m[64]
@@ -64,29 +68,37 @@ constexpr int kRedOff = kAlphaOff + 64 * 4;                // float red[4][64]
 constexpr int kSmemBytes = kRedOff + 4 * 64 * 4;
 static_assert(kWinOff + kPanels * kPanelBytes <= kPOff, "window panels must fit below P");
 
-enum Bar { RAW_FULL = 0, RAW_EMPTY = 2, RING_FULL = 4, RING_EMPTY = 8, S_FULL = 12, P_FULL = 13, O_DONE = 14,
-           FIN = 15, WIN_FULL = 16, WIN_CVT = 17, WIN_EMPTY = 18 };
+// The logits' A operand of a cache tile comes from a ring of four panels in tensor memory (TRING); the
+// values' A operand from a ring of two pair slots (two panels, one 128-column chunk) in shared memory.
+enum Bar { RAW_FULL = 0, RAW_EMPTY = 2, RING_FULL = 4, RING_EMPTY = 6, TRING_FULL = 8, TRING_EMPTY = 12,
+           S_FULL = 16, P_FULL = 17, PV_DONE = 18, FIN = 19, WIN_FULL = 20, WIN_CVT = 21, WIN_EMPTY = 22 };
+constexpr int kPairBytes = 2 * kPanelBytes;
+constexpr int kTRing = 4;
 
-constexpr int kDqWarp0 = 4, kDqWarps = 8;
+constexpr int kDqWarp0 = 4, kDqWarps = 8;      // 4-7 logits panels (tensor memory), 8-11 value panels
 constexpr int kGatherWarp = 12, kMmaWarp = 13;
 constexpr int kThreads = 14 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 64, kColL = 320;
+constexpr uint32_t kColS = 0, kColA = 64, kColO = 192, kColL = 448;
 
 constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
 constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
 constexpr uint32_t kIdescL = tc::idesc_f16_f32(128, kHeadsPad, 0, 1);   // ones K-major, P^T MN-major
+
+// Row of a cache tile held by tensor-memory lane l (0..127) in the logits: lanes of one quarter warp take
+// the same slot of 8 different blocks, so that their raw loads fall in different banks.
+__device__ __forceinline__ int lane_row(int l) {
+  const int sp = l >> 5, i = l & 31;
+  return 8 * (8 * (sp & 1) + (i & 7)) + 4 * (sp >> 1) + (i >> 3);
+}
 
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          uint32_t* hdr, uint32_t detail) {
   const uint32_t a = smem_addr(bar);
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
-    if (done) return true;
-    if ((i & 255u) == 255u && *abort_flag) return false;
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 7u) == 7u && *abort_flag) return false;
   }
   *abort_flag = 1;
   report(hdr, CSA_ERR_TIMEOUT, KID_ATTN, detail);
@@ -97,10 +109,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
-    if (done) return;
+    if (mbar_try_wait(a, parity)) return;
   }
 }
 
@@ -118,6 +127,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
                " [%0], [%1, {%2, %3, %4}], [%5];"
                :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
                   "r"(smem_addr(bar)) : "memory");
+}
+
+// OR of v over the 128 softmax threads (named barrier 1).
+__device__ __forceinline__ bool any_softmax(bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, 1, 128, q;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(r) : "r"((uint32_t)v) : "memory");
+  return r != 0;
 }
 
 struct UnitCtx {
@@ -214,11 +231,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   // ---------------- setup ----------------
   if (warp == kMmaWarp) tc::alloc(tmem_ptr, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) { mbar_init(&bars[RAW_FULL + i], 1); mbar_init(&bars[RAW_EMPTY + i], kDqWarps); }
-    for (int i = 0; i < kRing; ++i) { mbar_init(&bars[RING_FULL + i], kDqWarps); mbar_init(&bars[RING_EMPTY + i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[RAW_FULL + i], 1);
+      mbar_init(&bars[RAW_EMPTY + i], kDqWarps);
+      mbar_init(&bars[RING_FULL + i], kDqWarps / 2);
+      mbar_init(&bars[RING_EMPTY + i], 1);
+    }
+    for (int i = 0; i < kTRing; ++i) {
+      mbar_init(&bars[TRING_FULL + i], kDqWarps / 2);
+      mbar_init(&bars[TRING_EMPTY + i], 1);
+    }
     mbar_init(&bars[S_FULL], 1);
     mbar_init(&bars[P_FULL], 4);
-    mbar_init(&bars[O_DONE], 1);
+    mbar_init(&bars[PV_DONE], 1);
     mbar_init(&bars[FIN], 1);
     mbar_init(&bars[WIN_FULL], 1);
     mbar_init(&bars[WIN_CVT], kDqWarps);
@@ -273,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           mbar_arrive_expect_tx(&bars[RAW_FULL + stage], bytes);
 #pragma unroll
           for (int j = 0; j < kTileBlocks; ++j)
-            if (ids[j] >= 0) bulk_g2s(dst + j * kLatBlk, seq + ids[j] * kLatBlk, kLatBlk, &bars[RAW_FULL + stage]);
+            if (ids[j] >= 0) bulk_g2s(dst + j * kRawBlk, seq + ids[j] * kLatBlk, kLatBlk, &bars[RAW_FULL + stage]);
         } else {
           mbar_arrive(&bars[RAW_FULL + stage]);
         }
@@ -299,56 +324,113 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     }
   } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
     // ---------------- dequantisation ----------------
-    const int dt = tid - kDqWarp0 * 32;        // 0..255
-    const int cp = dt & 3;                     // 16-element scale group within a panel
-    uint32_t ring_k = 0;
+    // Two groups of four warps work on every cache tile side by side: group A (warps 4-7, one per
+    // tensor-memory subpartition, thread = lane = row lane_row(lane)) writes the 8 logits panels into the
+    // tensor-memory ring; group B (warps 8-11) writes the same panels, as four pairs, into the shared ring
+    // for the values. Both release the tile's raw stage when done.
+    const bool group_a = warp < kDqWarp0 + 4;
     bool stop = false;
-    for (int it = 0; it < n_cache && !stop; ++it) {
-      const int stage = it & 1;
-      if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
-      const uint8_t* raw = smem + kRawOff + stage * kRawStage;
-      // this thread's rows r = dt / 4 + 64 j and the offsets of their codes and scales in the raw stage
-      bool vr[2];
-      uint32_t code_off[2], sc_off[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int r = (dt >> 2) + 64 * j;
+    if (group_a) {
+      const int sp = warp & 3;
+      const int l = sp * 32 + lane;
+      const int r = lane_row(l);
+      const int blk = r >> 3, sl = r & 7;
+      const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
+      uint32_t t_k = 0;
+      for (int it = 0; it < n_cache && !stop; ++it) {
+        const int stage = it & 1;
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
+        const uint8_t* raw = smem + kRawOff + stage * kRawStage;
         int64_t id;
-        vr[j] = cache_row(p, u, c0 + it, r, &id);
-        const uint32_t blk = (uint32_t)(r >> 3) * kLatBlk, sl = (uint32_t)(r & 7);
-        code_off[j] = vr[j] ? blk + sl * 256 + cp * 8 : 0u;
-        sc_off[j] = vr[j] ? blk + 2048 + sl * 32 + cp : 0u;
-      }
-      for (int pass = 0; pass < 2 && !stop; ++pass) {
+        const bool vr = cache_row(p, u, c0 + it, r, &id);
+        const uint8_t* codes = raw + (vr ? blk * kRawBlk + sl * 256 : 0);
+        const uint8_t* scales = raw + (vr ? blk * kRawBlk + 2048 + sl * 32 : 0);
         for (int pp = 0; pp < kPanels; ++pp) {
-          const uint32_t slot = ring_k % kRing, n = ring_k / kRing;
+          const uint32_t slot = t_k % kTRing, n = t_k / kTRing;
+          if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
+            stop = true;
+            break;
+          }
+          const uint4 c0w = *reinterpret_cast<const uint4*>(codes + pp * 32);
+          const uint4 c1w = *reinterpret_cast<const uint4*>(codes + pp * 32 + 16);
+          const uint32_t sw = *reinterpret_cast<const uint32_t*>(scales + pp * 4);
+          uint32_t h[32];
+          e2m1x8_to_f16x8(c0w.x, h);      e2m1x8_to_f16x8(c0w.y, h + 4);
+          e2m1x8_to_f16x8(c0w.z, h + 8);  e2m1x8_to_f16x8(c0w.w, h + 12);
+          e2m1x8_to_f16x8(c1w.x, h + 16); e2m1x8_to_f16x8(c1w.y, h + 20);
+          e2m1x8_to_f16x8(c1w.z, h + 24); e2m1x8_to_f16x8(c1w.w, h + 28);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t sc = e4m3_to_f16x2_bcast((sw >> (8 * g)) & 0xFFu);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) h[8 * g + k] = vr ? hmul2_u32(h[8 * g + k], sc) : 0u;
+          }
+          tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
+          tc::wait_st();
+          tc::fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[TRING_FULL + slot]);
+          ++t_k;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
+      }
+    } else {
+      // group B: thread dt handles group cp of rows (block 4 w4 + bq, slot sq + 2 i), i = 0..3
+      const int dt = tid - (kDqWarp0 + 4) * 32;   // 0..127
+      const int cp = dt & 3;
+      const int blk = 4 * (dt >> 5) + ((dt >> 2) & 3);
+      const int sq = (dt >> 4) & 1;
+      uint32_t pair_k = 0;
+      for (int it = 0; it < n_cache && !stop; ++it) {
+        const int stage = it & 1;
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
+        const uint8_t* raw = smem + kRawOff + stage * kRawStage;
+        bool vr[4];
+        uint32_t code_off[4], sc_off[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int sl = sq + 2 * i, r = 8 * blk + sl;
+          int64_t id;
+          vr[i] = cache_row(p, u, c0 + it, r, &id);
+          code_off[i] = vr[i] ? (uint32_t)(blk * kRawBlk + sl * 256 + cp * 8) : 0u;
+          sc_off[i] = vr[i] ? (uint32_t)(blk * kRawBlk + 2048 + sl * 32 + cp) : 0u;
+        }
+        for (int pj = 0; pj < 4; ++pj) {
+          const uint32_t slot = pair_k & 1, n = pair_k >> 1;
           if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[RING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
             stop = true;
             break;
           }
-          uint8_t* panel = smem + kRingOff + slot * kPanelBytes;
+          uint8_t* pair = smem + kRingOff + slot * kPairBytes;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int r = (dt >> 2) + 64 * j;
-            const uint2 cw = *reinterpret_cast<const uint2*>(raw + code_off[j] + pp * 32);
-            const uint32_t sc = e4m3_to_f16x2_bcast(raw[sc_off[j] + pp * 4]);
-            uint32_t h[8];
-            e2m1x8_to_f16x8(cw.x, h);
-            e2m1x8_to_f16x8(cw.y, h + 4);
+          for (int half = 0; half < 2; ++half) {
+            const int pp = 2 * pj + half;
+            uint8_t* panel = pair + half * kPanelBytes;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] = vr[j] ? hmul2_u32(h[k], sc) : 0u;
-            *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp) ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+            for (int i = 0; i < 4; ++i) {
+              const int r = 8 * blk + sq + 2 * i;
+              const uint2 cw = *reinterpret_cast<const uint2*>(raw + code_off[i] + pp * 32);
+              const uint32_t sc = e4m3_to_f16x2_bcast(raw[sc_off[i] + pp * 4]);
+              uint32_t h[8];
+              e2m1x8_to_f16x8(cw.x, h);
+              e2m1x8_to_f16x8(cw.y, h + 4);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) h[k] = vr[i] ? hmul2_u32(h[k], sc) : 0u;
+              *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp) ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+            }
           }
           tc::fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[RING_FULL + slot]);
-          ++ring_k;
+          ++pair_k;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
     }
+    const int dt = tid - kDqWarp0 * 32;          // 0..255 over both groups
     for (int tw = 0; tw < nw && !stop; ++tw) {
       if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], tw & 1, abort_flag, p.hdr, 10))) break;
       // in place: bf16 -> fp16, rows that are not attended -> 0; this thread's rows are (k & 3) * 32 + dt / 8
@@ -375,47 +457,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue ----------------
     if (lane == 0) {
-      uint32_t ring_k = 0;
+      uint32_t pair_k = 0;
       const uint32_t q_addr = s_base + kQOff, ring_addr = s_base + kRingOff, p_addr = s_base + kPOff;
       const uint32_t ones_addr = s_base + kOnesOff, win_addr = s_base + kWinOff;
-      bool ok = true;
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        const bool is_cache = it < n_cache;
-        if (!is_cache && !wait_bar(&bars[WIN_CVT], (it - n_cache) & 1, abort_flag, p.hdr, 11)) { ok = false; break; }
-        // S^T = C . Q^T over the 8 panels
-        for (int pp = 0; pp < kPanels && ok; ++pp) {
-          uint32_t c_addr;
+      uint32_t t_k = 0;
+      // S^T(it) = C . Q^T over the 8 panels: cache tiles read C from the tensor-memory ring, window tiles
+      // from the window panels in shared memory
+      auto logits = [&](int it, bool cache) -> bool {
+        for (int pp = 0; pp < kPanels; ++pp) {
           uint32_t slot = 0;
-          if (is_cache) {
-            slot = ring_k % kRing;
-            if (!wait_bar(&bars[RING_FULL + slot], (ring_k / kRing) & 1u, abort_flag, p.hdr, 4)) { ok = false; break; }
-            c_addr = ring_addr + slot * kPanelBytes;
-          } else {
-            c_addr = win_addr + pp * kPanelBytes;
+          if (cache) {
+            slot = t_k % kTRing;
+            if (!wait_bar(&bars[TRING_FULL + slot], (t_k / kTRing) & 1u, abort_flag, p.hdr, 4)) return false;
           }
           tc::fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = tc::smem_desc(c_addr + ks * 32, 16, 1024, tc::kSwizzle128B);
             const uint64_t bq = tc::smem_desc(q_addr + pp * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
-            tc::mma_f16(tbase + kColS, a, bq, kIdescS, (pp | ks) != 0);
+            if (cache) {
+              tc::mma_f16_ts(tbase + kColS, tbase + kColA + 32 * slot + 8 * ks, bq, kIdescS, (pp | ks) != 0);
+            } else {
+              const uint64_t a = tc::smem_desc(win_addr + pp * kPanelBytes + ks * 32, 16, 1024, tc::kSwizzle128B);
+              tc::mma_f16(tbase + kColS, a, bq, kIdescS, (pp | ks) != 0);
+            }
           }
-          if (is_cache) { tc::commit(&bars[RING_EMPTY + slot]); ++ring_k; }
+          if (cache) { tc::commit(&bars[TRING_EMPTY + slot]); ++t_k; }
         }
-        if (!ok) break;
         tc::commit(&bars[S_FULL]);
-        if (!wait_bar(&bars[P_FULL], it & 1, abort_flag, p.hdr, 5)) { ok = false; break; }
-        tc::fence_after();
-        // O^T += C^T . P^T, four chunks of 128 latent columns (two adjacent panels each)
-        for (int ch = 0; ch < 4 && ok; ++ch) {
-          uint32_t c_addr;
-          uint32_t slot = 0;
-          if (is_cache) {
-            slot = ring_k % kRing;
-            const uint32_t n = ring_k / kRing;
-            if (!wait_bar(&bars[RING_FULL + slot], n & 1u, abort_flag, p.hdr, 6) ||
-                !wait_bar(&bars[RING_FULL + slot + 1], n & 1u, abort_flag, p.hdr, 6)) { ok = false; break; }
-            c_addr = ring_addr + slot * kPanelBytes;
+        return true;
+      };
+      // O^T += C^T . P^T (four chunks of 128 latent columns) and l += ones . P^T for tile it, chunks
+      // [ch0, ch1) at a time
+      auto values = [&](int it, bool cache, int ch0, int ch1) -> bool {
+        if (ch0 == 0) {
+          if (!wait_bar(&bars[P_FULL], it & 1, abort_flag, p.hdr, 5)) return false;
+          tc::fence_after();
+        }
+        for (int ch = ch0; ch < ch1; ++ch) {
+          uint32_t c_addr, slot = 0;
+          if (cache) {
+            slot = pair_k & 1;
+            if (!wait_bar(&bars[RING_FULL + slot], (pair_k >> 1) & 1u, abort_flag, p.hdr, 6)) return false;
+            c_addr = ring_addr + slot * kPairBytes;
           } else {
             c_addr = win_addr + 2 * ch * kPanelBytes;
           }
@@ -426,25 +509,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
             const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
             tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || j > 0) ? 1u : 0u);
           }
-          if (is_cache) {
-            tc::commit(&bars[RING_EMPTY + slot]);
-            tc::commit(&bars[RING_EMPTY + slot + 1]);
-            ring_k += 2;
-          }
+          if (cache) { tc::commit(&bars[RING_EMPTY + slot]); ++pair_k; }
         }
-        if (!ok) break;
-        // l += ones . P^T
+        if (ch1 == 4) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint64_t a = tc::smem_desc(ones_addr + (j & 3) * 32, 16, 0, tc::kSwizzle128B);
-          const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
-          tc::mma_f16(tbase + kColL, a, bp, kIdescL, (it > 0 || j > 0) ? 1u : 0u);
+          for (int j = 0; j < 8; ++j) {
+            const uint64_t a = tc::smem_desc(ones_addr + (j & 3) * 32, 16, 0, tc::kSwizzle128B);
+            const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
+            tc::mma_f16(tbase + kColL, a, bp, kIdescL, (it > 0 || j > 0) ? 1u : 0u);
+          }
+          tc::commit(&bars[PV_DONE]);
+          // the window panels overlay the raw and ring buffers: free them after the last cache tile and
+          // after every window tile
+          if ((cache && it == n_cache - 1 && nw > 0) || !cache) tc::commit(&bars[WIN_EMPTY]);
         }
-        // the window panels overlay the raw and ring buffers: free them after the last cache tile and
-        // after every window tile
-        if ((is_cache && it == n_cache - 1 && nw > 0) || !is_cache) tc::commit(&bars[WIN_EMPTY]);
+        return true;
+      };
+      // cache tiles: the next tile's logits go between the halves of this tile's values, so that the
+      // tensor core works while the value panels of the second half are being written
+      bool ok = n_cache == 0 || logits(0, true);
+      for (int it = 0; it < n_cache && ok; ++it) {
+        if (!values(it, true, 0, 2)) { ok = false; break; }
+        if (it + 1 < n_cache && !logits(it + 1, true)) { ok = false; break; }
+        if (!values(it, true, 2, 4)) { ok = false; break; }
       }
-      if (ok && n_tiles > 0) tc::commit(&bars[O_DONE]);
+      for (int tw = 0; tw < nw && ok; ++tw) {
+        const int it = n_cache + tw;
+        if (!wait_bar(&bars[WIN_CVT], tw & 1, abort_flag, p.hdr, 11)) { ok = false; break; }
+        if (!logits(it, false) || !values(it, false, 0, 4)) { ok = false; break; }
+      }
       // every MMA issued must be complete before the tensor memory is released
       tc::commit(&bars[FIN]);
       drain_bar(&bars[FIN], 0);
@@ -454,90 +547,111 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     bool ok = true;
     for (int it = 0; it < n_tiles; ++it) {
-      if (tid == 0) flag[it & 1] = 0;
+      // tensor-memory lane tid holds row lane_row(tid) of a cache tile (row tid of a window tile)
+      const int row = it < n_cache ? lane_row(tid) : tid;
       bool valid;
       if (it < n_cache) {
         int64_t id;
-        valid = cache_row(p, u, c0 + it, tid, &id);
+        valid = cache_row(p, u, c0 + it, row, &id);
       } else {
         bool oob;
-        valid = window_row(p, u, it - n_cache, tid, &oob);
+        valid = window_row(p, u, it - n_cache, row, &oob);
       }
+      const uint32_t s_col = kColS;
       if (!all_softmax(wait_bar(&bars[S_FULL], it & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
       tc::fence_after();
+      // Fast path: probabilities against the current reference maxima; the full path runs only when a
+      // probability would exceed 2^8 (a maximum moved by more than the slack, or none was set yet).
+      uint32_t w[32];
+      bool over = false;
       {
-        // per-head maximum over the warp's 32 rows: reduce-scatter, lane ends with heads 2 lane, 2 lane + 1
         uint32_t sr[64];
-        tc::ld_32x64(tbase + lane_base + kColS, sr);
+        tc::ld_32x64(tbase + lane_base + s_col, sr);
         tc::wait_ld();
-        float m[64];
 #pragma unroll
-        for (int h = 0; h < 64; ++h) m[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+        for (int c = 0; c < 8; ++c) {
+          const float4 ma = *reinterpret_cast<const float4*>(msh + 8 * c);
+          const float4 mb = *reinterpret_cast<const float4*>(msh + 8 * c + 4);
+          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
 #pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          const int o = 16 >> k, half = 32 >> k;
-          const bool up = (lane & o) != 0;
-#pragma unroll
-          for (int i = 0; i < half; ++i) {
-            const float send = up ? m[i] : m[i + half];
-            const float keep = up ? m[i + half] : m[i];
-            m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+          for (int k = 0; k < 4; ++k) {
+            const int h = 8 * c + 2 * k;
+            const float p0 = valid ? exp2f(__uint_as_float(sr[h]) * p.scale_log2 - mm[2 * k]) : 0.0f;
+            const float p1 = valid ? exp2f(__uint_as_float(sr[h + 1]) * p.scale_log2 - mm[2 * k + 1]) : 0.0f;
+            over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
+            w[4 * c + k] = f2_to_h2(p0, p1);
           }
         }
-        red[warp * 64 + 2 * lane] = m[0];
-        red[warp * 64 + 2 * lane + 1] = m[1];
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (tid < 64) {
-        const float tm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
-        const float mo = msh[tid];
-        float mn = mo;
-        if (tm > mo + kRescaleSlack) mn = tm;
-        alpha[tid] = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
-        if (mn != mo && mo != -INFINITY) flag[it & 1] = 1;
-        msh[tid] = mn;
-      }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (flag[it & 1]) {
-        // raise the reference maximum of the accumulated O and l (the previous products are complete:
-        // they were issued before this tile's logits, whose completion this thread has seen)
-        for (int chk = 0; chk < 5; ++chk) {
-          uint32_t o[64];
-          tc::ld_32x64(tbase + lane_base + kColO + 64 * chk, o);
+      if (any_softmax(over)) {
+        if (tid == 0) flag[it & 1] = 0;
+        {
+          // per-head maximum over the warp's 32 rows (one warp reduction per head)
+          uint32_t sr[64];
+          tc::ld_32x64(tbase + lane_base + s_col, sr);
           tc::wait_ld();
 #pragma unroll
-          for (int h = 0; h < 64; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-          tc::st_32x64(tbase + lane_base + kColO + 64 * chk, o);
+          for (int h = 0; h < 64; ++h) {
+            const float v = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+            float mx;
+            asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(v));
+            red[warp * 64 + h] = mx;
+          }
         }
-        tc::wait_st();
-      }
-      // the logits again (still in tensor memory: the next tile's product waits for this tile's P)
-      uint32_t sr[64];
-      tc::ld_32x64(tbase + lane_base + kColS, sr);
-      tc::wait_ld();
-      // probabilities, fp16, row tid of P (MN-major: 64 heads contiguous, 128-byte swizzle)
-      uint8_t* prow = smem + kPOff + tid * 128;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (tid < 64) {
+          const float tm = fmaxf(fmaxf(red[tid], red[64 + tid]), fmaxf(red[128 + tid], red[192 + tid]));
+          const float mo = msh[tid];
+          float mn = mo;
+          if (tm > mo + kRescaleSlack) mn = tm;
+          alpha[tid] = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
+          if (mn != mo && mo != -INFINITY) flag[it & 1] = 1;
+          msh[tid] = mn;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        // the previous tile's value products must be complete before O is rescaled
+        if (it > 0) {
+          if (!all_softmax(wait_bar(&bars[PV_DONE], (it - 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
+          tc::fence_after();
+        }
+        if (flag[it & 1]) {
+          // raise the reference maximum of the accumulated O and l
+          for (int chk = 0; chk < 5; ++chk) {
+            uint32_t o[64];
+            tc::ld_32x64(tbase + lane_base + kColO + 64 * chk, o);
+            tc::wait_ld();
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
+            for (int h = 0; h < 64; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+            tc::st_32x64(tbase + lane_base + kColO + 64 * chk, o);
+          }
+          tc::wait_st();
+        }
+        uint32_t sr[64];
+        tc::ld_32x64(tbase + lane_base + s_col, sr);
+        tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int h = 8 * c + 2 * k;
-          const float m0 = msh[h], m1 = msh[h + 1];
-          const float v0 = __uint_as_float(sr[h]) * p.scale_log2, v1 = __uint_as_float(sr[h + 1]) * p.scale_log2;
-          const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : exp2f(v0 - m0);
-          const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : exp2f(v1 - m1);
+        for (int k = 0; k < 32; ++k) {
+          const float m0 = msh[2 * k], m1 = msh[2 * k + 1];
+          const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[2 * k]) * p.scale_log2 - m0);
+          const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[2 * k + 1]) * p.scale_log2 - m1);
           w[k] = f2_to_h2(p0, p1);
         }
-        *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else if (it > 0) {
+        // the previous tile's value products read P: they must be complete before it is overwritten
+        if (!all_softmax(wait_bar(&bars[PV_DONE], (it - 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
       }
+      // probabilities, fp16, row `row` of P (MN-major: 64 heads contiguous, 128-byte swizzle)
+      uint8_t* prow = smem + kPOff + row * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       tc::fence_proxy_async();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[P_FULL]);
     }
     // ---------------- epilogue ----------------
-    const bool have = all_softmax(ok && n_tiles > 0 && wait_bar(&bars[O_DONE], 0, abort_flag, p.hdr, 8));
+    const bool have = all_softmax(ok && n_tiles > 0 && wait_bar(&bars[PV_DONE], (n_tiles - 1) & 1, abort_flag, p.hdr, 8));
     tc::fence_after();
     float* lsh = red;                        // the row sums, one per head (every lane holds all of them)
     if (have && warp == 0) {

@@ -100,10 +100,20 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// mbarrier and bulk-copy helpers (PTX ISA: mbarrier, cp.async.bulk). Every wait is bounded: after
-// kSpinLimit polls it gives up and returns false, and the caller records CSA_ERR_TIMEOUT.
+// mbarrier and bulk-copy helpers (PTX ISA: mbarrier, cp.async.bulk). Every wait is bounded: a poll
+// suspends the thread in hardware until the phase completes or kWaitHintNs pass, and after kSpinLimit
+// polls (a few seconds at most) the wait gives up and returns false; the caller records CSA_ERR_TIMEOUT.
 // ------------------------------------------------------------------------------------------------
-constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr uint32_t kSpinLimit = 1u << 17;
+constexpr uint32_t kWaitHintNs = 20000;
+
+// One poll of the phase with the given parity: true once it has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(bar_addr), "r"(parity), "r"(kWaitHintNs) : "memory");
+  return done != 0;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -130,12 +140,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 // Polls the phase with the given parity; true once it has completed, false after kSpinLimit polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
-    if (done) return true;
-  }
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(a, parity)) return true;
   return false;
 }
 

@@ -104,11 +104,8 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* hdr) {
   const uint32_t a = smem_addr(bar);
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
-    if (done) return true;
-    if ((i & 255u) == 255u && *abort_flag) return false;
+    if (mbar_try_wait(a, parity)) return true;
+    if ((i & 7u) == 7u && *abort_flag) return false;
   }
   *abort_flag = 1;
   report(hdr, CSA_ERR_TIMEOUT, KID_INDEX_SCORE, blockIdx.x);
@@ -118,10 +115,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(a), "r"(parity) : "memory");
-    if (done) return;
+    if (mbar_try_wait(a, parity)) return;
   }
 }
 
