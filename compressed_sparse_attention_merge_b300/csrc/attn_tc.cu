@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   const uint8_t* seq = p.cache + u.b * p.cache_stride_b;
 
   // ---------------- setup ----------------
+  // The barriers first, so that the gather warp can start the first tiles' copies while the other warps
+  // load and convert the queries.
   if (warp == kMmaWarp) tc::alloc(tmem_ptr, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -251,28 +253,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     fence_mbar_init();
     flag[0] = 0; flag[1] = 0; *abort_flag = 0;
   }
-  {
-    // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero
-    const __nv_bfloat16* qg = p.q + u.unit * (int64_t)H * kLatent;
-    for (int i = tid; i < kHeadsPad * 64; i += kThreads) {
-      const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < H) {
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(qg + (int64_t)h * kLatent + ch * 8));
-        v = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
-      }
-      *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = v;
-    }
-    for (int i = tid; i < 64; i += kThreads)
-      *reinterpret_cast<uint4*>(smem + kOnesOff + i * 16) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-    for (int i = tid; i < 64; i += kThreads) msh[i] = -INFINITY;
-  }
-  tc::fence_proxy_async();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tmem_ptr;
   const uint32_t s_base = smem_addr(smem);
+  if (warp != kGatherWarp) {
+    // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero. Every load of a
+    // thread is issued before the first conversion.
+    constexpr int kQThreads = kThreads - 32;
+    constexpr int kQItems = kHeadsPad * 64;
+    constexpr int kQPer = (kQItems + kQThreads - 1) / kQThreads;
+    const int qt = tid < kGatherWarp * 32 ? tid : tid - 32;
+    const __nv_bfloat16* qg = p.q + u.unit * (int64_t)H * kLatent;
+    uint4 v[kQPer];
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = qt + k * kQThreads;
+      const int h = i >> 6, ch = i & 63;
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (i < kQItems && h < H) v[k] = __ldg(reinterpret_cast<const uint4*>(qg + (int64_t)h * kLatent + ch * 8));
+    }
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = qt + k * kQThreads;
+      if (i < kQItems) {
+        const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
+        const uint4 w = make_uint4(bf2_to_h2(v[k].x), bf2_to_h2(v[k].y), bf2_to_h2(v[k].z), bf2_to_h2(v[k].w));
+        *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = w;
+      }
+    }
+    if (qt < 64) {
+      *reinterpret_cast<uint4*>(smem + kOnesOff + qt * 16) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+      msh[qt] = -INFINITY;
+    }
+    tc::fence_proxy_async();
+    asm volatile("bar.sync 2, %0;" :: "n"(kQThreads) : "memory");
+  }
 
   if (warp == kGatherWarp) {
     // ---------------- gather: cache blocks (cp.async.bulk), window rows (tensor map) ----------------

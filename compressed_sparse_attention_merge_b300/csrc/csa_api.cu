@@ -85,13 +85,9 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   L.n_ct = (int)ceil_div(a->top_k, 16);
   L.n_wt = a->swa_rows > 0 ? (int)ceil_div(a->window, 128) : 0;
   const int64_t avail = L.units > 0 ? num_sms / L.units : 1;
-  if (L.n_wt > 0 && avail >= 2) {
-    L.cache_splits = (int)(avail - 1 < L.n_ct ? avail - 1 : L.n_ct);
-    L.win_split = 1;
-  } else {
-    L.cache_splits = (int)(avail < 1 ? 1 : (avail < L.n_ct ? avail : L.n_ct));
-    L.win_split = 0;
-  }
+  L.cache_splits = (int)(avail < 1 ? 1 : (avail < L.n_ct ? avail : L.n_ct));
+  // the window tiles get a split of their own only if it still fits the one wave of CTAs
+  L.win_split = (L.n_wt > 0 && L.units * (L.cache_splits + 1) <= num_sms) ? 1 : 0;
   L.splits = L.cache_splits + L.win_split;
   L.o_off = CSA_WS_HEADER_BYTES;
   const size_t parts = L.splits > 1 ? (size_t)L.units * L.splits * a->heads : 0;
