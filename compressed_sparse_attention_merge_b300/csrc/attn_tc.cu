@@ -9,22 +9,26 @@
 // Design. A CTA owns one query (all heads) and some 128-row tiles of its row list: a range of cache
 // tiles (16 selected blocks each) and/or the window tiles. Because one latent row c is both key and
 // value, both products are taken with the rows as the 128-wide M side and the heads as N:
-//   S^T [rows x heads]  = C [rows x 512] . Q^T                   (C K-major, Q K-major)
-//   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (C and P MN-major)
-// C lives in shared memory as fp16 panels of 64 latent columns in the 128-byte-swizzled layout; the same
-// bytes are the K-major operand of the first product and the MN-major operand of the second.
-//   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk; the tile is
-//   dequantised twice, panel by panel, through a ring of four panel buffers (once per product).
-//   Window tiles: a tensor-map copy (TMA, 128-byte swizzle) lands the 128 bf16 rows directly in panel
-//   layout; they are converted to fp16 in place and serve both products.
-// The row sums l come from a fifth product whose A operand is a 1 KB atom of ones repeated over every
-// row (stride 0). S, O and l accumulate in tensor memory (64 + 256 + 64 columns of fp32).
+//   S^T [rows x heads]  = C [rows x 512] . Q^T                   (logits)
+//   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (values)
+// and the row sums l come from a third product whose A operand is a 1 KB atom of ones repeated over
+// every row (stride 0). S, O and l accumulate in tensor memory.
+//   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk into one of two
+//   raw stages. Two groups of four warps dequantise every tile: group A writes the logits operand
+//   straight into tensor memory (thread = row, one 64-column panel at a time, a two-panel ring); group B
+//   writes the values operand into a three-slot shared-memory ring of [128 latent x 64 row] units in the
+//   128-byte-swizzled MN-major layout.
+//   Window tiles: a tensor-map copy (TMA, 128-byte swizzle) lands the 128 bf16 rows in panel layout over
+//   the raw and ring areas; they are converted to fp16 in place and serve both products.
+// Pipelining: S is double-buffered in tensor memory and P in shared memory, and the logits and the
+// values have separate issuing threads, so that the logits of tile t+1 run while the softmax of tile t
+// works and the values of tile t run while the softmax of tile t+1 works.
 //
-// Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-11 dequantisation, 12 gather, 13 MMA issue
-// and tensor-memory allocation. The softmax keeps, per head, a reference maximum that is raised only
-// when a tile's maximum exceeds it by more than 8 (in log2 units), so the probabilities stay below 2^8
-// and the accumulators are rescaled rarely. Splits write unnormalised partials (o, m, l); the combine
-// kernel merges them in split order.
+// Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-7 group A, 8-11 group B, 12 gather,
+// 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue. The softmax keeps, per head, a
+// reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in log2
+// units), so the probabilities stay below 2^8 and the accumulators are rescaled rarely. Splits write
+// unnormalised partials (o, m, l); the combine kernel merges them in split order.
 #include <cuda.h>
 
 #include <cstring>
@@ -39,7 +43,6 @@ constexpr int kRows = 128;                                 // rows per tile: M o
 constexpr int kTileBlocks = kRows / kBlockEntries;         // 16 cache blocks per tile
 constexpr int kHeadsPad = 64;                              // N of both products (heads, zero-padded)
 constexpr int kPanels = kLatent / 64;                      // 8 panels of 64 latent columns
-constexpr int kRing = 4;
 constexpr int kLatBlk = block_bytes(kLatent);              // 2304
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.0f;                      // log2 headroom before the reference max moves
@@ -47,49 +50,60 @@ constexpr float kMaxProb = 256.0f;                         // 2^kRescaleSlack
 
 // shared-memory map (bytes); the operand regions start on 1024-byte boundaries
 constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB
-constexpr int kQOff = 0;
-// Staged blocks are padded by 32 bytes so that the same code column of rows in different blocks falls
-// in different shared-memory banks.
-constexpr int kRawBlk = kLatBlk + 32;                      // 2,336
-constexpr int kRawStage = kTileBlocks * kRawBlk;           // 37,376
-constexpr int kRawOff = kQOff + kPanels * kQPanel;         // 65,536
-constexpr int kPanelBytes = kRows * 128;                   // 16 KB
-constexpr int kRingOff = (kRawOff + 2 * kRawStage + 1023) & ~1023;   // 141,312
+constexpr int kQOff = 0;                                   // queries: 8 K-major panels, 64 KB
+constexpr int kPBytes = kRows * 128;                       // one P^T buffer: 16 KB
+constexpr int kPOff = kQOff + kPanels * kQPanel;           // 65,536: two P^T buffers
+constexpr int kOnesOff = kPOff + 2 * kPBytes;              // 98,304
+// Staged blocks are padded by 16 bytes so that the same byte of a row falls in a different bank in each
+// of 8 consecutive blocks.
+constexpr int kRawBlk = kLatBlk + 16;                      // 2,320
+constexpr int kRawStage = kTileBlocks * kRawBlk;           // 37,120
+constexpr int kRawOff = kOnesOff + 1024;                   // 99,328
+constexpr int kUnitBytes = 2 * 64 * 128;                   // values unit: 128 latent columns x 64 rows
+constexpr int kRing = 3;
+constexpr int kRingOff = (kRawOff + 2 * kRawStage + 1023) & ~1023;   // 174,080
+constexpr int kPanelBytes = kRows * 128;                   // 16 KB: one 64-column panel of a whole tile
 constexpr int kWinOff = kRawOff;                           // window tile: 8 panels over the raw and ring areas
-constexpr int kPOff = kRingOff + kRing * kPanelBytes;      // 206,848
-constexpr int kOnesOff = kPOff + kRows * 128;              // 223,232
-constexpr int kBarOff = kOnesOff + 1024;                   // 224,256
-constexpr int kNumBars = 24;
+constexpr int kBarOff = kWinOff + kPanels * kPanelBytes;   // 230,400
+constexpr int kNumBars = 28;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
 constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort
 constexpr int kMOff = kFlagOff + 16;                       // float m[64]
 constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[64]
 constexpr int kRedOff = kAlphaOff + 64 * 4;                // float red[4][64]
 constexpr int kSmemBytes = kRedOff + 4 * 64 * 4;
-static_assert(kWinOff + kPanels * kPanelBytes <= kPOff, "window panels must fit below P");
+static_assert(kRingOff + kRing * kUnitBytes <= kBarOff, "the ring must lie inside the window overlay");
+static_assert(kSmemBytes <= 232448, "shared memory");
 
-// The logits' A operand of a cache tile comes from a ring of four panels in tensor memory (TRING); the
-// values' A operand from a ring of two pair slots (two panels, one 128-column chunk) in shared memory.
-enum Bar { RAW_FULL = 0, RAW_EMPTY = 2, RING_FULL = 4, RING_EMPTY = 6, TRING_FULL = 8, TRING_EMPTY = 12,
-           S_FULL = 16, P_FULL = 17, PV_DONE = 18, FIN = 19, WIN_FULL = 20, WIN_CVT = 21, WIN_EMPTY = 22 };
-constexpr int kPairBytes = 2 * kPanelBytes;
-constexpr int kTRing = 4;
+enum Bar {
+  RAW_FULL = 0, RAW_EMPTY = 2,          // raw stages: gather -> both dequantisation groups
+  TRING_FULL = 4, TRING_EMPTY = 6,      // logits operand panels in tensor memory: group A <-> logits issuer
+  RING_FULL = 8, RING_EMPTY = 11,       // values operand units in shared memory: group B <-> values issuer
+  S_FULL = 14, S_EMPTY = 16,            // logits buffers: logits issuer <-> softmax
+  P_FULL = 18, PV_DONE = 20,            // probability buffers: softmax <-> values issuer
+  WIN_FULL = 22, WIN_CVT = 23, WIN_EMPTY = 24,
+  FIN_L = 25, FIN_V = 26
+};
+constexpr int kTRing = 2;
 
-constexpr int kDqWarp0 = 4, kDqWarps = 8;      // 4-7 logits panels (tensor memory), 8-11 value panels
-constexpr int kGatherWarp = 12, kMmaWarp = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kGrpA0 = 4, kGrpB0 = 8;          // first warps of the two dequantisation groups
+constexpr int kDqWarps = 8;
+constexpr int kGatherWarp = 12, kLogitsWarp = 13, kValuesWarp = 14;
+constexpr int kThreads = 15 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColA = 64, kColO = 192, kColL = 448;
+constexpr uint32_t kColS = 0, kColA = 128, kColO = 192, kColL = 448;   // S: two buffers of 64 columns
 
 constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
 constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
 constexpr uint32_t kIdescL = tc::idesc_f16_f32(128, kHeadsPad, 0, 1);   // ones K-major, P^T MN-major
 
-// Row of a cache tile held by tensor-memory lane l (0..127) in the logits: lanes of one quarter warp take
-// the same slot of 8 different blocks, so that their raw loads fall in different banks.
+// Row of a cache tile held by tensor-memory lane l (0..127) in the logits. The 8 lanes of a quarter warp
+// take 8 different blocks and 8 different slots, so that their raw loads and their P^T stores fall in
+// different banks.
 __device__ __forceinline__ int lane_row(int l) {
-  const int sp = l >> 5, i = l & 31;
-  return 8 * (8 * (sp & 1) + (i & 7)) + 4 * (sp >> 1) + (i >> 3);
+  const int h = l >> 3, i = l & 7;
+  const int blk = i + 8 * (h & 1), slot = (i + (h >> 1)) & 7;
+  return 8 * blk + slot;
 }
 
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
@@ -231,25 +245,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   // ---------------- setup ----------------
   // The barriers first, so that the gather warp can start the first tiles' copies while the other warps
   // load and convert the queries.
-  if (warp == kMmaWarp) tc::alloc(tmem_ptr, kTmemCols);
+  if (warp == kLogitsWarp) tc::alloc(tmem_ptr, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[RAW_FULL + i], 1);
       mbar_init(&bars[RAW_EMPTY + i], kDqWarps);
-      mbar_init(&bars[RING_FULL + i], kDqWarps / 2);
+      mbar_init(&bars[TRING_FULL + i], 4);
+      mbar_init(&bars[TRING_EMPTY + i], 1);
+      mbar_init(&bars[S_FULL + i], 1);
+      mbar_init(&bars[S_EMPTY + i], 4);
+      mbar_init(&bars[P_FULL + i], 4);
+      mbar_init(&bars[PV_DONE + i], 1);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bars[RING_FULL + i], 4);
       mbar_init(&bars[RING_EMPTY + i], 1);
     }
-    for (int i = 0; i < kTRing; ++i) {
-      mbar_init(&bars[TRING_FULL + i], kDqWarps / 2);
-      mbar_init(&bars[TRING_EMPTY + i], 1);
-    }
-    mbar_init(&bars[S_FULL], 1);
-    mbar_init(&bars[P_FULL], 4);
-    mbar_init(&bars[PV_DONE], 1);
-    mbar_init(&bars[FIN], 1);
     mbar_init(&bars[WIN_FULL], 1);
     mbar_init(&bars[WIN_CVT], kDqWarps);
     mbar_init(&bars[WIN_EMPTY], 1);
+    mbar_init(&bars[FIN_L], 1);
+    mbar_init(&bars[FIN_V], 1);
     fence_mbar_init();
     flag[0] = 0; flag[1] = 0; *abort_flag = 0;
   }
@@ -339,15 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it) drain_bar(&bars[RAW_FULL + (it & 1)], (it >> 1) & 1);
       if (win_issued > 0) drain_bar(&bars[WIN_FULL], (win_issued - 1) & 1);
     }
-  } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
+  } else if (warp >= kGrpA0 && warp < kGrpA0 + kDqWarps) {
     // ---------------- dequantisation ----------------
-    // Two groups of four warps work on every cache tile side by side: group A (warps 4-7, one per
-    // tensor-memory subpartition, thread = lane = row lane_row(lane)) writes the 8 logits panels into the
-    // tensor-memory ring; group B (warps 8-11) writes the same panels, as four pairs, into the shared ring
-    // for the values. Both release the tile's raw stage when done.
-    const bool group_a = warp < kDqWarp0 + 4;
     bool stop = false;
-    if (group_a) {
+    if (warp < kGrpB0) {
+      // group A: one warp per tensor-memory subpartition, thread = lane = row lane_row(lane); writes the 8
+      // logits panels of a tile into the two-slot tensor-memory ring
       const int sp = warp & 3;
       const int l = sp * 32 + lane;
       const int r = lane_row(l);
@@ -357,20 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       for (int it = 0; it < n_cache && !stop; ++it) {
         const int stage = it & 1;
         if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
-        const uint8_t* raw = smem + kRawOff + stage * kRawStage;
+        const uint8_t* raw = smem + kRawOff + stage * kRawStage + blk * kRawBlk;
         int64_t id;
         const bool vr = cache_row(p, u, c0 + it, r, &id);
-        const uint8_t* codes = raw + (vr ? blk * kRawBlk + sl * 256 : 0);
-        const uint8_t* scales = raw + (vr ? blk * kRawBlk + 2048 + sl * 32 : 0);
+        const uint8_t* codes = raw + sl * 256;
+        const uint8_t* scales = raw + 2048 + sl * 32;
         for (int pp = 0; pp < kPanels; ++pp) {
-          const uint32_t slot = t_k % kTRing, n = t_k / kTRing;
-          if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
-            stop = true;
-            break;
-          }
           const uint4 c0w = *reinterpret_cast<const uint4*>(codes + pp * 32);
           const uint4 c1w = *reinterpret_cast<const uint4*>(codes + pp * 32 + 16);
-          const uint32_t sw = *reinterpret_cast<const uint32_t*>(scales + pp * 4);
+          const uint32_t sw = vr ? *reinterpret_cast<const uint32_t*>(scales + pp * 4) : 0u;
           uint32_t h[32];
           e2m1x8_to_f16x8(c0w.x, h);      e2m1x8_to_f16x8(c0w.y, h + 4);
           e2m1x8_to_f16x8(c0w.z, h + 8);  e2m1x8_to_f16x8(c0w.w, h + 12);
@@ -378,10 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           e2m1x8_to_f16x8(c1w.z, h + 24); e2m1x8_to_f16x8(c1w.w, h + 28);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
+            // a zero scale (rows that are not attended) gives exact zeros: E2M1 has no infinities or NaNs
             const uint32_t sc = e4m3_to_f16x2_bcast((sw >> (8 * g)) & 0xFFu);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[8 * g + k] = vr ? hmul2_u32(h[8 * g + k], sc) : 0u;
+            for (int k = 0; k < 8; ++k) h[8 * g + k] = hmul2_u32(h[8 * g + k], sc);
           }
+          const uint32_t slot = t_k % kTRing, n = t_k / kTRing;
+          if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
+            stop = true;
+            break;
+          }
+          tc::fence_after();
           tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
           tc::wait_st();
           tc::fence_before();
@@ -393,61 +408,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
       }
     } else {
-      // group B: thread dt handles group cp of rows (block 4 w4 + bq, slot sq + 2 i), i = 0..3
-      const int dt = tid - (kDqWarp0 + 4) * 32;   // 0..127
-      const int cp = dt & 3;
-      const int blk = 4 * (dt >> 5) + ((dt >> 2) & 3);
-      const int sq = (dt >> 4) & 1;
-      uint32_t pair_k = 0;
+      // group B: writes the values operand as 8 units of [128 latent columns x 64 rows] per tile (unit
+      // 2 ch + rh: latent chunk ch, rows 64 rh ..). Per unit a thread converts 8 chunks of 8 elements:
+      // column chunk c of block 8 rh + 2 bsel + (k & 1), slot 2 wl + ((k >> 1) & 1), panel half k >> 2.
+      const int wl = warp - kGrpB0;
+      const int c = lane & 7, bsel = lane >> 3;
+      uint32_t u_k = 0;
       for (int it = 0; it < n_cache && !stop; ++it) {
         const int stage = it & 1;
         if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
         const uint8_t* raw = smem + kRawOff + stage * kRawStage;
-        bool vr[4];
-        uint32_t code_off[4], sc_off[4];
+        uint32_t vmask = 0;       // bit 4 rh + (k & 3): row attended
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int sl = sq + 2 * i, r = 8 * blk + sl;
-          int64_t id;
-          vr[i] = cache_row(p, u, c0 + it, r, &id);
-          code_off[i] = vr[i] ? (uint32_t)(blk * kRawBlk + sl * 256 + cp * 8) : 0u;
-          sc_off[i] = vr[i] ? (uint32_t)(blk * kRawBlk + 2048 + sl * 32 + cp) : 0u;
+        for (int rh = 0; rh < 2; ++rh) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = 8 * (8 * rh + 2 * bsel + (k & 1)) + 2 * wl + (k >> 1);
+            int64_t id;
+            if (cache_row(p, u, c0 + it, r, &id)) vmask |= 1u << (4 * rh + k);
+          }
         }
-        for (int pj = 0; pj < 4; ++pj) {
-          const uint32_t slot = pair_k & 1, n = pair_k >> 1;
+        for (int unit = 0; unit < 8; ++unit) {
+          const int ch = unit >> 1, rh = unit & 1;
+          const uint32_t slot = u_k % kRing, n = u_k / kRing;
           if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[RING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
             stop = true;
             break;
           }
-          uint8_t* pair = smem + kRingOff + slot * kPairBytes;
+          uint8_t* dst = smem + kRingOff + slot * kUnitBytes;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int pp = 2 * pj + half;
-            uint8_t* panel = pair + half * kPanelBytes;
+          for (int k = 0; k < 8; ++k) {
+            const int bl = 2 * bsel + (k & 1), sl = 2 * wl + ((k >> 1) & 1), ph = k >> 2;
+            const int pnl = 2 * ch + ph;
+            const uint8_t* src = raw + (8 * rh + bl) * kRawBlk;
+            const uint32_t cw = *reinterpret_cast<const uint32_t*>(src + sl * 256 + pnl * 32 + c * 4);
+            const uint32_t sb = src[2048 + sl * 32 + pnl * 4 + (c >> 1)];
+            const uint32_t sc = (vmask >> (4 * rh + (k & 3))) & 1u ? e4m3_to_f16x2_bcast(sb) : 0u;
+            uint32_t h[4];
+            e2m1x8_to_f16x8(cw, h);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = 8 * blk + sq + 2 * i;
-              const uint2 cw = *reinterpret_cast<const uint2*>(raw + code_off[i] + pp * 32);
-              const uint32_t sc = e4m3_to_f16x2_bcast(raw[sc_off[i] + pp * 4]);
-              uint32_t h[8];
-              e2m1x8_to_f16x8(cw.x, h);
-              e2m1x8_to_f16x8(cw.y, h + 4);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) h[k] = vr[i] ? hmul2_u32(h[k], sc) : 0u;
-              *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp) ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(panel + r * 128 + (((2 * cp + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-            }
+            for (int e = 0; e < 4; ++e) h[e] = hmul2_u32(h[e], sc);
+            const int rl = 8 * bl + sl;
+            *reinterpret_cast<uint4*>(dst + ph * (kUnitBytes / 2) + rl * 128 + ((c ^ sl) << 4)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
           }
           tc::fence_proxy_async();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[RING_FULL + slot]);
-          ++pair_k;
+          ++u_k;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
       }
     }
-    const int dt = tid - kDqWarp0 * 32;          // 0..255 over both groups
+    const int dt = tid - kGrpA0 * 32;          // 0..255 over both groups
     for (int tw = 0; tw < nw && !stop; ++tw) {
       if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], tw & 1, abort_flag, p.hdr, 10))) break;
       // in place: bf16 -> fp16, rows that are not attended -> 0; this thread's rows are (k & 3) * 32 + dt / 8
@@ -461,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll 4
       for (int k = 0; k < 32; ++k) {
         const int q = k * 256 + dt;
-        const int pp = q >> 10, row = (q & 1023) >> 3, c = q & 7;
-        uint4* a = reinterpret_cast<uint4*>(smem + kWinOff + pp * kPanelBytes + row * 128 + ((c ^ (row & 7)) << 4));
+        const int pp = q >> 10, row = (q & 1023) >> 3, cc = q & 7;
+        uint4* a = reinterpret_cast<uint4*>(smem + kWinOff + pp * kPanelBytes + row * 128 + ((cc ^ (row & 7)) << 4));
         const uint4 x = *a;
         const bool v = vr[k & 3];
         *a = v ? make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w)) : make_uint4(0, 0, 0, 0);
@@ -471,99 +485,103 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[WIN_CVT]);
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------- MMA issue ----------------
+  } else if (warp == kLogitsWarp) {
+    // ---------------- logits MMA issue: S^T(t) = C . Q^T into S buffer t & 1 ----------------
     if (lane == 0) {
-      uint32_t pair_k = 0;
-      const uint32_t q_addr = s_base + kQOff, ring_addr = s_base + kRingOff, p_addr = s_base + kPOff;
-      const uint32_t ones_addr = s_base + kOnesOff, win_addr = s_base + kWinOff;
+      const uint32_t q_addr = s_base + kQOff, win_addr = s_base + kWinOff;
       uint32_t t_k = 0;
-      // S^T(it) = C . Q^T over the 8 panels: cache tiles read C from the tensor-memory ring, window tiles
-      // from the window panels in shared memory
-      auto logits = [&](int it, bool cache) -> bool {
+      bool ok = true;
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const int sb = it & 1;
+        const bool cache = it < n_cache;
+        if (it >= 2 && !wait_bar(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4)) { ok = false; break; }
+        if (!cache && !wait_bar(&bars[WIN_CVT], (it - n_cache) & 1, abort_flag, p.hdr, 11)) { ok = false; break; }
+        const uint32_t d = tbase + kColS + 64 * sb;
         for (int pp = 0; pp < kPanels; ++pp) {
           uint32_t slot = 0;
           if (cache) {
             slot = t_k % kTRing;
-            if (!wait_bar(&bars[TRING_FULL + slot], (t_k / kTRing) & 1u, abort_flag, p.hdr, 4)) return false;
+            if (!wait_bar(&bars[TRING_FULL + slot], (t_k / kTRing) & 1u, abort_flag, p.hdr, 4)) { ok = false; break; }
           }
           tc::fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t bq = tc::smem_desc(q_addr + pp * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
             if (cache) {
-              tc::mma_f16_ts(tbase + kColS, tbase + kColA + 32 * slot + 8 * ks, bq, kIdescS, (pp | ks) != 0);
+              tc::mma_f16_ts(d, tbase + kColA + 32 * slot + 8 * ks, bq, kIdescS, (pp | ks) != 0);
             } else {
               const uint64_t a = tc::smem_desc(win_addr + pp * kPanelBytes + ks * 32, 16, 1024, tc::kSwizzle128B);
-              tc::mma_f16(tbase + kColS, a, bq, kIdescS, (pp | ks) != 0);
+              tc::mma_f16(d, a, bq, kIdescS, (pp | ks) != 0);
             }
           }
           if (cache) { tc::commit(&bars[TRING_EMPTY + slot]); ++t_k; }
         }
-        tc::commit(&bars[S_FULL]);
-        return true;
-      };
-      // O^T += C^T . P^T (four chunks of 128 latent columns) and l += ones . P^T for tile it, chunks
-      // [ch0, ch1) at a time
-      auto values = [&](int it, bool cache, int ch0, int ch1) -> bool {
-        if (ch0 == 0) {
-          if (!wait_bar(&bars[P_FULL], it & 1, abort_flag, p.hdr, 5)) return false;
-          tc::fence_after();
-        }
-        for (int ch = ch0; ch < ch1; ++ch) {
-          uint32_t c_addr, slot = 0;
-          if (cache) {
-            slot = pair_k & 1;
-            if (!wait_bar(&bars[RING_FULL + slot], (pair_k >> 1) & 1u, abort_flag, p.hdr, 6)) return false;
-            c_addr = ring_addr + slot * kPairBytes;
-          } else {
-            c_addr = win_addr + 2 * ch * kPanelBytes;
-          }
-          tc::fence_after();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint64_t a = tc::smem_desc(c_addr + j * 2048, kPanelBytes, 1024, tc::kSwizzle128B);
-            const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
-            tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || j > 0) ? 1u : 0u);
-          }
-          if (cache) { tc::commit(&bars[RING_EMPTY + slot]); ++pair_k; }
-        }
-        if (ch1 == 4) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint64_t a = tc::smem_desc(ones_addr + (j & 3) * 32, 16, 0, tc::kSwizzle128B);
-            const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
-            tc::mma_f16(tbase + kColL, a, bp, kIdescL, (it > 0 || j > 0) ? 1u : 0u);
-          }
-          tc::commit(&bars[PV_DONE]);
-          // the window panels overlay the raw and ring buffers: free them after the last cache tile and
-          // after every window tile
-          if ((cache && it == n_cache - 1 && nw > 0) || !cache) tc::commit(&bars[WIN_EMPTY]);
-        }
-        return true;
-      };
-      // cache tiles: the next tile's logits go between the halves of this tile's values, so that the
-      // tensor core works while the value panels of the second half are being written
-      bool ok = n_cache == 0 || logits(0, true);
-      for (int it = 0; it < n_cache && ok; ++it) {
-        if (!values(it, true, 0, 2)) { ok = false; break; }
-        if (it + 1 < n_cache && !logits(it + 1, true)) { ok = false; break; }
-        if (!values(it, true, 2, 4)) { ok = false; break; }
-      }
-      for (int tw = 0; tw < nw && ok; ++tw) {
-        const int it = n_cache + tw;
-        if (!wait_bar(&bars[WIN_CVT], tw & 1, abort_flag, p.hdr, 11)) { ok = false; break; }
-        if (!logits(it, false) || !values(it, false, 0, 4)) { ok = false; break; }
+        if (ok) tc::commit(&bars[S_FULL + sb]);
       }
       // every MMA issued must be complete before the tensor memory is released
-      tc::commit(&bars[FIN]);
-      drain_bar(&bars[FIN], 0);
+      tc::commit(&bars[FIN_L]);
+      drain_bar(&bars[FIN_L], 0);
+    }
+  } else if (warp == kValuesWarp) {
+    // ---------------- values MMA issue: O^T += C^T . P^T and l += ones . P^T ----------------
+    if (lane == 0) {
+      const uint32_t ring_addr = s_base + kRingOff, ones_addr = s_base + kOnesOff, win_addr = s_base + kWinOff;
+      uint32_t u_k = 0;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int pb = it & 1;
+        const bool cache = it < n_cache;
+        const uint32_t p_addr = s_base + kPOff + pb * kPBytes;
+        if (!wait_bar(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 5)) break;
+        tc::fence_after();
+        bool ok = true;
+        if (cache) {
+          for (int unit = 0; unit < 8; ++unit) {
+            const int ch = unit >> 1, rh = unit & 1;
+            const uint32_t slot = u_k % kRing;
+            if (!wait_bar(&bars[RING_FULL + slot], (u_k / kRing) & 1u, abort_flag, p.hdr, 6)) { ok = false; break; }
+            tc::fence_after();
+            const uint32_t c_addr = ring_addr + slot * kUnitBytes;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t a = tc::smem_desc(c_addr + j * 2048, kUnitBytes / 2, 1024, tc::kSwizzle128B);
+              const uint64_t bp = tc::smem_desc(p_addr + rh * (kPBytes / 2) + j * 2048, 8192, 1024, tc::kSwizzle128B);
+              tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || rh > 0 || j > 0) ? 1u : 0u);
+            }
+            tc::commit(&bars[RING_EMPTY + slot]);
+            ++u_k;
+          }
+        } else {
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t c_addr = win_addr + 2 * ch * kPanelBytes;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint64_t a = tc::smem_desc(c_addr + j * 2048, kPanelBytes, 1024, tc::kSwizzle128B);
+              const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
+              tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || j > 0) ? 1u : 0u);
+            }
+          }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t a = tc::smem_desc(ones_addr + (j & 3) * 32, 16, 0, tc::kSwizzle128B);
+          const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
+          tc::mma_f16(tbase + kColL, a, bp, kIdescL, (it > 0 || j > 0) ? 1u : 0u);
+        }
+        tc::commit(&bars[PV_DONE + pb]);
+        // the window panels overlay the raw and ring buffers: free them after the last cache tile and
+        // after every window tile
+        if ((cache && it == n_cache - 1 && nw > 0) || !cache) tc::commit(&bars[WIN_EMPTY]);
+      }
+      tc::commit(&bars[FIN_V]);
+      drain_bar(&bars[FIN_V], 0);
     }
   } else {
     // ---------------- softmax (warps 0-3, thread = tile row) ----------------
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     bool ok = true;
     for (int it = 0; it < n_tiles; ++it) {
+      const int sb = it & 1;
       // tensor-memory lane tid holds row lane_row(tid) of a cache tile (row tid of a window tile)
       const int row = it < n_cache ? lane_row(tid) : tid;
       bool valid;
@@ -574,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         bool oob;
         valid = window_row(p, u, it - n_cache, row, &oob);
       }
-      const uint32_t s_col = kColS;
-      if (!all_softmax(wait_bar(&bars[S_FULL], it & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
+      const uint32_t s_col = kColS + 64 * sb;
+      if (!all_softmax(wait_bar(&bars[S_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
       tc::fence_after();
       // Fast path: probabilities against the current reference maxima; the full path runs only when a
       // probability would exceed 2^8 (a maximum moved by more than the slack, or none was set yet).
@@ -601,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
       }
       if (any_softmax(over)) {
-        if (tid == 0) flag[it & 1] = 0;
+        if (tid == 0) flag[sb] = 0;
         {
           // per-head maximum over the warp's 32 rows (one warp reduction per head)
           uint32_t sr[64];
@@ -622,16 +640,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           float mn = mo;
           if (tm > mo + kRescaleSlack) mn = tm;
           alpha[tid] = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
-          if (mn != mo && mo != -INFINITY) flag[it & 1] = 1;
+          if (mn != mo && mo != -INFINITY) flag[sb] = 1;
           msh[tid] = mn;
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        // the previous tile's value products must be complete before O is rescaled
-        if (it > 0) {
-          if (!all_softmax(wait_bar(&bars[PV_DONE], (it - 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
-          tc::fence_after();
-        }
-        if (flag[it & 1]) {
+        if (flag[sb]) {
+          // the previous tile's value products must be complete before O and l are rescaled (the ones
+          // before it completed earlier: the values are issued in tile order)
+          if (it > 0) {
+            if (!all_softmax(wait_bar(&bars[PV_DONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 12))) {
+              ok = false;
+              break;
+            }
+            tc::fence_after();
+          }
           // raise the reference maximum of the accumulated O and l
           for (int chk = 0; chk < 5; ++chk) {
             uint32_t o[64];
@@ -653,22 +675,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[2 * k + 1]) * p.scale_log2 - m1);
           w[k] = f2_to_h2(p0, p1);
         }
-      } else if (it > 0) {
-        // the previous tile's value products read P: they must be complete before it is overwritten
-        if (!all_softmax(wait_bar(&bars[PV_DONE], (it - 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
+      }
+      // S buffer sb has been read for the last time: the logits of tile it + 2 may overwrite it
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
+      // P buffer sb was read by the values of tile it - 2
+      if (it >= 2) {
+        if (!all_softmax(wait_bar(&bars[PV_DONE + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
       }
       // probabilities, fp16, row `row` of P (MN-major: 64 heads contiguous, 128-byte swizzle)
-      uint8_t* prow = smem + kPOff + row * 128;
+      uint8_t* prow = smem + kPOff + sb * kPBytes + row * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       tc::fence_proxy_async();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[P_FULL]);
+      if (lane == 0) mbar_arrive(&bars[P_FULL + sb]);
     }
     // ---------------- epilogue ----------------
-    const bool have = all_softmax(ok && n_tiles > 0 && wait_bar(&bars[PV_DONE], (n_tiles - 1) & 1, abort_flag, p.hdr, 8));
+    const int last = n_tiles - 1;
+    const bool have = all_softmax(ok && n_tiles > 0 &&
+                                  wait_bar(&bars[PV_DONE + (last & 1)], (last >> 1) & 1, abort_flag, p.hdr, 8));
     tc::fence_after();
     float* lsh = red;                        // the row sums, one per head (every lane holds all of them)
     if (have && warp == 0) {
@@ -717,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 
   __syncthreads();
   tc::fence_after();
-  if (warp == kMmaWarp) tc::dealloc(tbase, kTmemCols);
+  if (warp == kLogitsWarp) tc::dealloc(tbase, kTmemCols);
 }
 
 // out[u][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, splits in order; lse = (M + log2 L) ln 2.
