@@ -11,11 +11,11 @@
 // value, both products are taken with the rows as the 128-wide M side and the heads as N:
 //   S^T [rows x heads]  = C [rows x 512] . Q^T                   (logits)
 //   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (values)
-// and the row sums l come from a third product whose A operand is a 1 KB atom of ones repeated over
-// every row (stride 0). S, O and l accumulate in tensor memory.
+// S and O accumulate in tensor memory; the row sums l are added up by one warp from the fp16
+// probabilities in shared memory (the same values the tensor core multiplies).
 //   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk into one of two
 //   raw stages. Two groups of four warps dequantise every tile: group A writes the logits operand
-//   straight into tensor memory (thread = row, one 64-column panel at a time, a two-panel ring); group B
+//   straight into tensor memory (thread = row, 64-column panels, a four-panel ring); group B
 //   writes the values operand into a three-slot shared-memory ring of [128 latent x 64 row] units in the
 //   128-byte-swizzled MN-major layout.
 //   Window tiles: a tensor-map copy (TMA, 128-byte swizzle) lands the 128 bf16 rows in panel layout over
@@ -25,7 +25,7 @@
 // works and the values of tile t run while the softmax of tile t+1 works.
 //
 // Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-7 group A, 8-11 group B, 12 gather,
-// 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue. The softmax keeps, per head, a
+// 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps, per head, a
 // reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in log2
 // units), so the probabilities stay below 2^8 and the accumulators are rescaled rarely. Splits write
 // unnormalised partials (o, m, l); the combine kernel merges them in split order.
@@ -53,49 +53,54 @@ constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB
 constexpr int kQOff = 0;                                   // queries: 8 K-major panels, 64 KB
 constexpr int kPBytes = kRows * 128;                       // one P^T buffer: 16 KB
 constexpr int kPOff = kQOff + kPanels * kQPanel;           // 65,536: two P^T buffers
-constexpr int kOnesOff = kPOff + 2 * kPBytes;              // 98,304
 // Staged blocks are padded by 16 bytes so that the same byte of a row falls in a different bank in each
 // of 8 consecutive blocks.
 constexpr int kRawBlk = kLatBlk + 16;                      // 2,320
 constexpr int kRawStage = kTileBlocks * kRawBlk;           // 37,120
-constexpr int kRawOff = kOnesOff + 1024;                   // 99,328
+constexpr int kRawOff = kPOff + 2 * kPBytes;               // 98,304
 constexpr int kUnitBytes = 2 * 64 * 128;                   // values unit: 128 latent columns x 64 rows
 constexpr int kRing = 3;
-constexpr int kRingOff = (kRawOff + 2 * kRawStage + 1023) & ~1023;   // 174,080
+constexpr int kRingOff = (kRawOff + 2 * kRawStage + 1023) & ~1023;   // 173,056
 constexpr int kPanelBytes = kRows * 128;                   // 16 KB: one 64-column panel of a whole tile
 constexpr int kWinOff = kRawOff;                           // window tile: 8 panels over the raw and ring areas
-constexpr int kBarOff = kWinOff + kPanels * kPanelBytes;   // 230,400
-constexpr int kNumBars = 28;
+constexpr int kBarOff = kWinOff + kPanels * kPanelBytes;   // 229,376
+constexpr int kNumBars = 32;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
 constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort
 constexpr int kMOff = kFlagOff + 16;                       // float m[64]
-constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[64]
-constexpr int kRedOff = kAlphaOff + 64 * 4;                // float red[4][64]
-constexpr int kSmemBytes = kRedOff + 4 * 64 * 4;
+constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[2][64]: per P buffer
+constexpr int kRedOff = kAlphaOff + 2 * 64 * 4;            // float red[4][64]
+constexpr int kLsumOff = kRedOff + 4 * 64 * 4;             // float lsum[64]: final row sums
+constexpr int kSmemBytes = kLsumOff + 64 * 4;
 static_assert(kRingOff + kRing * kUnitBytes <= kBarOff, "the ring must lie inside the window overlay");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
+constexpr int kTRing = 4;
 enum Bar {
   RAW_FULL = 0, RAW_EMPTY = 2,          // raw stages: gather -> both dequantisation groups
-  TRING_FULL = 4, TRING_EMPTY = 6,      // logits operand panels in tensor memory: group A <-> logits issuer
-  RING_FULL = 8, RING_EMPTY = 11,       // values operand units in shared memory: group B <-> values issuer
-  S_FULL = 14, S_EMPTY = 16,            // logits buffers: logits issuer <-> softmax
-  P_FULL = 18, PV_DONE = 20,            // probability buffers: softmax <-> values issuer
-  WIN_FULL = 22, WIN_CVT = 23, WIN_EMPTY = 24,
-  FIN_L = 25, FIN_V = 26
+  TRING_FULL = 4,                       // logits operand panels in tensor memory: group A <-> logits issuer
+  TRING_EMPTY = TRING_FULL + kTRing,
+  RING_FULL = TRING_EMPTY + kTRing,     // values operand units in shared memory: group B <-> values issuer
+  RING_EMPTY = RING_FULL + kRing,
+  S_FULL = RING_EMPTY + kRing,          // logits buffers: logits issuer <-> softmax
+  S_EMPTY = S_FULL + 2,
+  P_FULL = S_EMPTY + 2,                 // probability buffers: softmax <-> values issuer and row-sum warp
+  PV_DONE = P_FULL + 2,
+  WIN_FULL = PV_DONE + 2, WIN_CVT, WIN_EMPTY,
+  FIN_L, FIN_V, NUM_BARS
 };
-constexpr int kTRing = 2;
+
+static_assert(NUM_BARS <= kNumBars, "barrier area");
 
 constexpr int kGrpA0 = 4, kGrpB0 = 8;          // first warps of the two dequantisation groups
 constexpr int kDqWarps = 8;
-constexpr int kGatherWarp = 12, kLogitsWarp = 13, kValuesWarp = 14;
-constexpr int kThreads = 15 * 32;
+constexpr int kGatherWarp = 12, kLogitsWarp = 13, kValuesWarp = 14, kSumWarp = 15;
+constexpr int kThreads = 16 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColA = 128, kColO = 192, kColL = 448;   // S: two buffers of 64 columns
+constexpr uint32_t kColS = 0, kColA = 128, kColO = 256;   // S: two buffers of 64 columns; A: four panels
 
 constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
 constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
-constexpr uint32_t kIdescL = tc::idesc_f16_f32(128, kHeadsPad, 0, 1);   // ones K-major, P^T MN-major
 
 // Row of a cache tile held by tensor-memory lane l (0..127) in the logits. The 8 lanes of a quarter warp
 // take 8 different blocks and 8 different slots, so that their raw loads and their P^T stores fall in
@@ -156,16 +161,22 @@ struct UnitCtx {
   bool prefill;
 };
 
-// Cache row r of cache tile t: block id (or -1) and whether the row's entry is attended.
-__device__ __forceinline__ bool cache_row(const AttnParams& p, const UnitCtx& u, int t, int r, int64_t* id_out) {
+// Block id of row r of cache tile t as stored in the index list (-1 past the list).
+__device__ __forceinline__ int cache_id(const AttnParams& p, const UnitCtx& u, int t, int r) {
   const int slot = t * kTileBlocks + (r >> 3);
-  int64_t id = -1;
-  if (slot < p.top_k) id = __ldg(p.idx + u.unit * p.top_k + slot);
-  const bool ok = id >= 0 && id < u.n_b;
-  *id_out = ok ? id : -1;
-  if (!ok) return false;
+  return slot < p.top_k ? __ldg(p.idx + u.unit * p.top_k + slot) : -1;
+}
+
+// Whether row r (slot r & 7) of a block with stored id `id` is attended.
+__device__ __forceinline__ bool cache_ok(const UnitCtx& u, int64_t id, int r) {
+  if (id < 0 || id >= u.n_b) return false;
   const int64_t e = id * kBlockEntries + (r & 7);
   return e < u.n_e && 2 * e + 1 <= u.pos;
+}
+
+// Bulk prefetch of a global range into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
 
 // First window-buffer row of window tile tw (may be negative or past the buffer: those rows are filled
@@ -184,6 +195,14 @@ __device__ __forceinline__ bool window_row(const AttnParams& p, const UnitCtx& u
   const int64_t s = window_row0(p, u, tw) + r;
   if (declared && (s < 0 || s >= p.swa_rows)) { *oob = true; return false; }
   return declared;
+}
+
+// 2^x by the hardware approximation (relative error near 2^-22; subnormal results flush to zero). The
+// probabilities it produces are rounded to fp16 for the tensor core, so the approximation is invisible.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
@@ -247,15 +266,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   // load and convert the queries.
   if (warp == kLogitsWarp) tc::alloc(tmem_ptr, kTmemCols);
   if (tid == 0) {
+    for (int i = 0; i < kTRing; ++i) {
+      mbar_init(&bars[TRING_FULL + i], 4);
+      mbar_init(&bars[TRING_EMPTY + i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[RAW_FULL + i], 1);
       mbar_init(&bars[RAW_EMPTY + i], kDqWarps);
-      mbar_init(&bars[TRING_FULL + i], 4);
-      mbar_init(&bars[TRING_EMPTY + i], 1);
       mbar_init(&bars[S_FULL + i], 1);
       mbar_init(&bars[S_EMPTY + i], 4);
       mbar_init(&bars[P_FULL + i], 4);
-      mbar_init(&bars[PV_DONE + i], 1);
+      mbar_init(&bars[PV_DONE + i], 2);        // the values' commit and the row-sum warp
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&bars[RING_FULL + i], 4);
@@ -299,10 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = w;
       }
     }
-    if (qt < 64) {
-      *reinterpret_cast<uint4*>(smem + kOnesOff + qt * 16) = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-      msh[qt] = -INFINITY;
-    }
+    if (qt < 64) msh[qt] = -INFINITY;
     tc::fence_proxy_async();
     asm volatile("bar.sync 2, %0;" :: "n"(kQThreads) : "memory");
   }
@@ -336,6 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           mbar_arrive(&bars[RAW_FULL + stage]);
         }
         ++issued;
+        if (it == 1 || (it == 0 && n_cache == 1)) {
+          // the later tiles of this CTA go to L2 now, so that refilling a raw stage costs an L2 read
+          for (int t2 = c0 + 2; t2 < c1; ++t2) {
+            for (int j = 0; j < kTileBlocks; ++j) {
+              const int slot = t2 * kTileBlocks + j;
+              const int64_t id = slot < p.top_k ? (int64_t)__ldg(p.idx + u.unit * p.top_k + slot) : -1;
+              if (id >= 0 && id < u.n_b) prefetch_l2(seq + id * kLatBlk, kLatBlk);
+            }
+          }
+        }
       }
       if (issued == n_cache) {
         for (int tw = 0; tw < nw; ++tw) {
@@ -367,43 +395,63 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       const int blk = r >> 3, sl = r & 7;
       const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
       uint32_t t_k = 0;
+      int id_next = n_cache > 0 ? cache_id(p, u, c0, r) : -1;
       for (int it = 0; it < n_cache && !stop; ++it) {
         const int stage = it & 1;
+        const bool vr = cache_ok(u, id_next, r);
+        if (it + 1 < n_cache) id_next = cache_id(p, u, c0 + it + 1, r);
         if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
         const uint8_t* raw = smem + kRawOff + stage * kRawStage + blk * kRawBlk;
-        int64_t id;
-        const bool vr = cache_row(p, u, c0 + it, r, &id);
         const uint8_t* codes = raw + sl * 256;
         const uint8_t* scales = raw + 2048 + sl * 32;
-        for (int pp = 0; pp < kPanels; ++pp) {
-          const uint4 c0w = *reinterpret_cast<const uint4*>(codes + pp * 32);
-          const uint4 c1w = *reinterpret_cast<const uint4*>(codes + pp * 32 + 16);
-          const uint32_t sw = vr ? *reinterpret_cast<const uint32_t*>(scales + pp * 4) : 0u;
-          uint32_t h[32];
-          e2m1x8_to_f16x8(c0w.x, h);      e2m1x8_to_f16x8(c0w.y, h + 4);
-          e2m1x8_to_f16x8(c0w.z, h + 8);  e2m1x8_to_f16x8(c0w.w, h + 12);
-          e2m1x8_to_f16x8(c1w.x, h + 16); e2m1x8_to_f16x8(c1w.y, h + 20);
-          e2m1x8_to_f16x8(c1w.z, h + 24); e2m1x8_to_f16x8(c1w.w, h + 28);
+        // Panels go out in pairs: both are converted and stored, then one wait covers both stores. The
+        // next panel's raw words are loaded while the current one is converted.
+        uint4 wa = *reinterpret_cast<const uint4*>(codes);
+        uint4 wb = *reinterpret_cast<const uint4*>(codes + 16);
+        uint32_t ws = vr ? *reinterpret_cast<const uint32_t*>(scales) : 0u;
+#pragma unroll 1
+        for (int pp = 0; pp < kPanels && !stop; pp += 2) {
+          uint32_t slots[2];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            // a zero scale (rows that are not attended) gives exact zeros: E2M1 has no infinities or NaNs
-            const uint32_t sc = e4m3_to_f16x2_bcast((sw >> (8 * g)) & 0xFFu);
+          for (int q = 0; q < 2; ++q) {
+            uint32_t h[32];
+            e2m1x8_to_f16x8(wa.x, h);      e2m1x8_to_f16x8(wa.y, h + 4);
+            e2m1x8_to_f16x8(wa.z, h + 8);  e2m1x8_to_f16x8(wa.w, h + 12);
+            e2m1x8_to_f16x8(wb.x, h + 16); e2m1x8_to_f16x8(wb.y, h + 20);
+            e2m1x8_to_f16x8(wb.z, h + 24); e2m1x8_to_f16x8(wb.w, h + 28);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[8 * g + k] = hmul2_u32(h[8 * g + k], sc);
+            for (int g = 0; g < 4; ++g) {
+              // a zero scale (rows that are not attended) gives exact zeros: E2M1 has no infinities or NaNs
+              const uint32_t sc = e4m3_to_f16x2_bcast((ws >> (8 * g)) & 0xFFu);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) h[8 * g + k] = hmul2_u32(h[8 * g + k], sc);
+            }
+            const int nx = pp + q + 1;
+            if (nx < kPanels) {
+              wa = *reinterpret_cast<const uint4*>(codes + nx * 32);
+              wb = *reinterpret_cast<const uint4*>(codes + nx * 32 + 16);
+              ws = vr ? *reinterpret_cast<const uint32_t*>(scales + nx * 4) : 0u;
+            }
+            const uint32_t slot = t_k % kTRing, n = t_k / kTRing;
+            if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
+              stop = true;
+              break;
+            }
+            tc::fence_after();
+            tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
+            slots[q] = slot;
+            ++t_k;
           }
-          const uint32_t slot = t_k % kTRing, n = t_k / kTRing;
-          if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
-            stop = true;
-            break;
-          }
-          tc::fence_after();
-          tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
+          if (stop) break;
           tc::wait_st();
           tc::fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[TRING_FULL + slot]);
-          ++t_k;
+          if (lane == 0) {
+            mbar_arrive(&bars[TRING_FULL + slots[0]]);
+            mbar_arrive(&bars[TRING_FULL + slots[1]]);
+          }
         }
+        tc::wait_st();      // no tensor-memory store may be in flight if the loop gave up
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
       }
@@ -414,22 +462,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       const int wl = warp - kGrpB0;
       const int c = lane & 7, bsel = lane >> 3;
       uint32_t u_k = 0;
+      // the 4 blocks of this thread's rows in a tile: 8 rh + 2 bsel + j (rh, j in {0, 1})
+      int ids_next[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) ids_next[q] = n_cache > 0 ? cache_id(p, u, c0, 8 * (8 * (q >> 1) + 2 * bsel + (q & 1))) : -1;
       for (int it = 0; it < n_cache && !stop; ++it) {
         const int stage = it & 1;
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
-        const uint8_t* raw = smem + kRawOff + stage * kRawStage;
         uint32_t vmask = 0;       // bit 4 rh + (k & 3): row attended
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int r = 8 * (8 * rh + 2 * bsel + (k & 1)) + 2 * wl + (k >> 1);
-            int64_t id;
-            if (cache_row(p, u, c0 + it, r, &id)) vmask |= 1u << (4 * rh + k);
+            if (cache_ok(u, ids_next[2 * rh + (k & 1)], r)) vmask |= 1u << (4 * rh + k);
           }
         }
+        if (it + 1 < n_cache) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ids_next[q] = cache_id(p, u, c0 + it + 1, 8 * (8 * (q >> 1) + 2 * bsel + (q & 1)));
+        }
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
+        const uint8_t* raw = smem + kRawOff + stage * kRawStage;
         for (int unit = 0; unit < 8; ++unit) {
           const int ch = unit >> 1, rh = unit & 1;
+          // the unit's raw words first: one load latency per unit instead of one per item
+          uint32_t cw[8], sb[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int bl = 2 * bsel + (k & 1), sl = 2 * wl + ((k >> 1) & 1), pnl = 2 * ch + (k >> 2);
+            const uint8_t* src = raw + (8 * rh + bl) * kRawBlk;
+            cw[k] = *reinterpret_cast<const uint32_t*>(src + sl * 256 + pnl * 32 + c * 4);
+            sb[k] = src[2048 + sl * 32 + pnl * 4 + (c >> 1)];
+          }
           const uint32_t slot = u_k % kRing, n = u_k / kRing;
           if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[RING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
             stop = true;
@@ -439,18 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const int bl = 2 * bsel + (k & 1), sl = 2 * wl + ((k >> 1) & 1), ph = k >> 2;
-            const int pnl = 2 * ch + ph;
-            const uint8_t* src = raw + (8 * rh + bl) * kRawBlk;
-            const uint32_t cw = *reinterpret_cast<const uint32_t*>(src + sl * 256 + pnl * 32 + c * 4);
-            const uint32_t sb = src[2048 + sl * 32 + pnl * 4 + (c >> 1)];
-            const uint32_t sc = (vmask >> (4 * rh + (k & 3))) & 1u ? e4m3_to_f16x2_bcast(sb) : 0u;
-            uint32_t h[4];
-            e2m1x8_to_f16x8(cw, h);
+            const uint32_t sc = (vmask >> (4 * rh + (k & 3))) & 1u ? e4m3_to_f16x2_bcast(sb[k]) : 0u;
+            uint32_t hh[4];
+            e2m1x8_to_f16x8(cw[k], hh);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = hmul2_u32(h[e], sc);
+            for (int e = 0; e < 4; ++e) hh[e] = hmul2_u32(hh[e], sc);
             const int rl = 8 * bl + sl;
             *reinterpret_cast<uint4*>(dst + ph * (kUnitBytes / 2) + rl * 128 + ((c ^ sl) << 4)) =
-                make_uint4(h[0], h[1], h[2], h[3]);
+                make_uint4(hh[0], hh[1], hh[2], hh[3]);
           }
           tc::fence_proxy_async();
           __syncwarp();
@@ -525,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   } else if (warp == kValuesWarp) {
     // ---------------- values MMA issue: O^T += C^T . P^T and l += ones . P^T ----------------
     if (lane == 0) {
-      const uint32_t ring_addr = s_base + kRingOff, ones_addr = s_base + kOnesOff, win_addr = s_base + kWinOff;
+      const uint32_t ring_addr = s_base + kRingOff, win_addr = s_base + kWinOff;
       uint32_t u_k = 0;
       for (int it = 0; it < n_tiles; ++it) {
         const int pb = it & 1;
@@ -562,12 +622,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           }
         }
         if (!ok) break;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint64_t a = tc::smem_desc(ones_addr + (j & 3) * 32, 16, 0, tc::kSwizzle128B);
-          const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
-          tc::mma_f16(tbase + kColL, a, bp, kIdescL, (it > 0 || j > 0) ? 1u : 0u);
-        }
         tc::commit(&bars[PV_DONE + pb]);
         // the window panels overlay the raw and ring buffers: free them after the last cache tile and
         // after every window tile
@@ -576,25 +630,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       tc::commit(&bars[FIN_V]);
       drain_bar(&bars[FIN_V], 0);
     }
+  } else if (warp == kSumWarp) {
+    // ---------------- row sums: l += sum over the tile's rows of P (lane = heads 2 lane, 2 lane + 1) ----
+    float l0 = 0.0f, l1 = 0.0f;
+    const int h0 = 2 * lane;
+    bool ok = true;
+    for (int it = 0; it < n_tiles && ok; ++it) {
+      const int pb = it & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 13))) { ok = false; break; }
+      if (flag[pb]) {
+        // the softmax raised the reference maxima for this tile: rescale like O
+        l0 *= alpha[64 * pb + h0];
+        l1 *= alpha[64 * pb + h0 + 1];
+      }
+      const uint8_t* pbuf = smem + kPOff + pb * kPBytes + (lane & 3) * 4;
+      float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
+#pragma unroll 8
+      for (int r = 0; r < kRows; r += 2) {
+        const uint32_t x = *reinterpret_cast<const uint32_t*>(pbuf + r * 128 + (((lane >> 2) ^ (r & 7)) << 4));
+        const uint32_t y = *reinterpret_cast<const uint32_t*>(pbuf + (r + 1) * 128 + (((lane >> 2) ^ ((r + 1) & 7)) << 4));
+        const float2 fx = __half22float2(*reinterpret_cast<const __half2*>(&x));
+        const float2 fy = __half22float2(*reinterpret_cast<const __half2*>(&y));
+        a0 += fx.x; a1 += fx.y; b0 += fy.x; b1 += fy.y;
+      }
+      l0 += a0 + b0;
+      l1 += a1 + b1;
+      if (it == n_tiles - 1) {
+        float* lsum = reinterpret_cast<float*>(smem + kLsumOff);
+        lsum[h0] = l0;
+        lsum[h0 + 1] = l1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[PV_DONE + pb]);
+    }
   } else {
     // ---------------- softmax (warps 0-3, thread = tile row) ----------------
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     bool ok = true;
+    int id_next = n_cache > 0 ? cache_id(p, u, c0, lane_row(tid)) : -1;
     for (int it = 0; it < n_tiles; ++it) {
       const int sb = it & 1;
       // tensor-memory lane tid holds row lane_row(tid) of a cache tile (row tid of a window tile)
       const int row = it < n_cache ? lane_row(tid) : tid;
       bool valid;
       if (it < n_cache) {
-        int64_t id;
-        valid = cache_row(p, u, c0 + it, row, &id);
+        valid = cache_ok(u, id_next, row);
+        if (it + 1 < n_cache) id_next = cache_id(p, u, c0 + it + 1, row);
       } else {
         bool oob;
         valid = window_row(p, u, it - n_cache, row, &oob);
       }
       const uint32_t s_col = kColS + 64 * sb;
       if (!all_softmax(wait_bar(&bars[S_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
+      // P buffer sb, alpha[sb] and flag[sb] were last read by the values and row sums of tile it - 2
+      if (it >= 2) {
+        if (!all_softmax(wait_bar(&bars[PV_DONE + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
+      }
       tc::fence_after();
+      float* al = alpha + 64 * sb;
       // Fast path: probabilities against the current reference maxima; the full path runs only when a
       // probability would exceed 2^8 (a maximum moved by more than the slack, or none was set yet).
       uint32_t w[32];
@@ -611,26 +704,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int h = 8 * c + 2 * k;
-            const float p0 = valid ? exp2f(__uint_as_float(sr[h]) * p.scale_log2 - mm[2 * k]) : 0.0f;
-            const float p1 = valid ? exp2f(__uint_as_float(sr[h + 1]) * p.scale_log2 - mm[2 * k + 1]) : 0.0f;
+            const float p0 = valid ? ex2(__uint_as_float(sr[h]) * p.scale_log2 - mm[2 * k]) : 0.0f;
+            const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * p.scale_log2 - mm[2 * k + 1]) : 0.0f;
             over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
             w[4 * c + k] = f2_to_h2(p0, p1);
           }
         }
       }
-      if (any_softmax(over)) {
-        if (tid == 0) flag[sb] = 0;
-        {
+      const bool full = any_softmax(over);
+      if (tid == 0) flag[sb] = 0;
+      if (full) {
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
           // per-head maximum over the warp's 32 rows (one warp reduction per head)
-          uint32_t sr[64];
-          tc::ld_32x64(tbase + lane_base + s_col, sr);
+          uint32_t sr[32];
+          tc::ld_32x32(tbase + lane_base + s_col + 32 * half, sr);
           tc::wait_ld();
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
+          for (int h = 0; h < 32; ++h) {
             const float v = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
             float mx;
             asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(v));
-            red[warp * 64 + h] = mx;
+            red[warp * 64 + 32 * half + h] = mx;
           }
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -639,14 +734,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           const float mo = msh[tid];
           float mn = mo;
           if (tm > mo + kRescaleSlack) mn = tm;
-          alpha[tid] = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
+          al[tid] = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
           if (mn != mo && mo != -INFINITY) flag[sb] = 1;
           msh[tid] = mn;
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (flag[sb]) {
-          // the previous tile's value products must be complete before O and l are rescaled (the ones
-          // before it completed earlier: the values are issued in tile order)
+          // the previous tile's value products must be complete before O is rescaled (the ones before it
+          // completed earlier: the values are issued in tile order); the row-sum warp rescales l itself
           if (it > 0) {
             if (!all_softmax(wait_bar(&bars[PV_DONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 12))) {
               ok = false;
@@ -654,36 +749,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
             }
             tc::fence_after();
           }
-          // raise the reference maximum of the accumulated O and l
-          for (int chk = 0; chk < 5; ++chk) {
-            uint32_t o[64];
-            tc::ld_32x64(tbase + lane_base + kColO + 64 * chk, o);
+          // raise the reference maximum of the accumulated O (32 columns = 32 heads at a time)
+#pragma unroll 1
+          for (int k = 0; k < 8; ++k) {
+            uint32_t o[32];
+            tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
             tc::wait_ld();
+            const float* ak = al + 32 * (k & 1);
 #pragma unroll
-            for (int h = 0; h < 64; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-            tc::st_32x64(tbase + lane_base + kColO + 64 * chk, o);
+            for (int h = 0; h < 32; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * ak[h]);
+            tc::st_32x32(tbase + lane_base + kColO + 32 * k, o);
           }
           tc::wait_st();
         }
-        uint32_t sr[64];
-        tc::ld_32x64(tbase + lane_base + s_col, sr);
-        tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float m0 = msh[2 * k], m1 = msh[2 * k + 1];
-          const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[2 * k]) * p.scale_log2 - m0);
-          const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : exp2f(__uint_as_float(sr[2 * k + 1]) * p.scale_log2 - m1);
-          w[k] = f2_to_h2(p0, p1);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sr[32];
+          tc::ld_32x32(tbase + lane_base + s_col + 32 * half, sr);
+          tc::wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float m0 = msh[32 * half + 2 * k], m1 = msh[32 * half + 2 * k + 1];
+            const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[2 * k]) * p.scale_log2 - m0);
+            const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[2 * k + 1]) * p.scale_log2 - m1);
+            w[16 * half + k] = f2_to_h2(p0, p1);
+          }
         }
       }
       // S buffer sb has been read for the last time: the logits of tile it + 2 may overwrite it
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
-      // P buffer sb was read by the values of tile it - 2
-      if (it >= 2) {
-        if (!all_softmax(wait_bar(&bars[PV_DONE + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
-      }
       // probabilities, fp16, row `row` of P (MN-major: 64 heads contiguous, 128-byte swizzle)
       uint8_t* prow = smem + kPOff + sb * kPBytes + row * 128;
 #pragma unroll
@@ -699,35 +795,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const bool have = all_softmax(ok && n_tiles > 0 &&
                                   wait_bar(&bars[PV_DONE + (last & 1)], (last >> 1) & 1, abort_flag, p.hdr, 8));
     tc::fence_after();
-    float* lsh = red;                        // the row sums, one per head (every lane holds all of them)
-    if (have && warp == 0) {
-      uint32_t lr[64];
-      tc::ld_32x64(tbase + kColL, lr);
-      tc::wait_ld();
-      if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < 64; ++h) lsh[h] = __uint_as_float(lr[h]);
-      }
-    } else if (!have && tid < 64) {
-      lsh[tid] = 0.0f;
-    }
+    // the row sums, one per head, written by the row-sum warp before its last arrival on PV_DONE
+    float* lsh = reinterpret_cast<float*>(smem + kLsumOff);
+    if (!have && tid < 64) lsh[tid] = 0.0f;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const int64_t prow_base = (u.unit * p.splits + split) * H;
-    for (int chk = 0; chk < 4; ++chk) {
-      uint32_t o[64];
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      uint32_t o[32];
       if (have) {
-        tc::ld_32x64(tbase + lane_base + kColO + 64 * chk, o);
+        tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
         tc::wait_ld();
       } else {
 #pragma unroll
-        for (int h = 0; h < 64; ++h) o[h] = 0u;
+        for (int h = 0; h < 32; ++h) o[h] = 0u;
       }
-      const int d = 128 * chk + tid;
+      const int d = 128 * (k >> 1) + tid;
 #pragma unroll
-      for (int h = 0; h < 64; ++h) {
+      for (int j = 0; j < 32; ++j) {
+        const int h = 32 * (k & 1) + j;
         if (h >= H) break;
         const float l = lsh[h];
-        const float x = __uint_as_float(o[h]);
+        const float x = __uint_as_float(o[j]);
         if (p.splits == 1) p.out[(u.unit * H + h) * (int64_t)kLatent + d] = l > 0.0f ? x / l : 0.0f;
         else p.part_o[(prow_base + h) * kLatent + d] = x;
       }
