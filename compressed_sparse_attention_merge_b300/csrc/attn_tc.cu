@@ -28,10 +28,16 @@
 // 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps, per head, a
 // reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in log2
 // units), so the probabilities stay below 2^8 and the accumulators are rescaled rarely. Splits write
-// unnormalised partials (o, m, l); the combine kernel merges them in split order.
+// unnormalised partials (o, m, l); the combine kernel merges them in split order. When the splits of a
+// unit form one thread-block cluster, each CTA stages its (o, m, l) in its own shared memory instead and
+// CTA r merges latent columns [512 r / S, 512 (r + 1) / S) of every split, in split order, through
+// distributed shared memory.
 #include <cuda.h>
 
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "csa_internal.cuh"
 #include "tc.cuh"
@@ -195,6 +201,31 @@ __device__ __forceinline__ bool window_row(const AttnParams& p, const UnitCtx& u
   const int64_t s = window_row0(p, u, tw) + r;
   if (declared && (s < 0 || s >= p.swa_rows)) { *oob = true; return false; }
   return declared;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// Every thread of every CTA of the cluster arrives; shared-memory writes before it are visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 2^x by the hardware approximation (relative error near 2^-22; subnormal results flush to zero). The
@@ -800,8 +831,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     if (!have && tid < 64) lsh[tid] = 0.0f;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const int64_t prow_base = (u.unit * p.splits + split) * H;
+    if (p.cluster) {
+      // stage o as [head][512] fp32 over the operand area (every product has completed); m and l are
+      // already in shared memory
+      float* stage = reinterpret_cast<float*>(smem + kRawOff);
 #pragma unroll 1
-    for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < 8; ++k) {
+        uint32_t o[32];
+        if (have) {
+          tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
+          tc::wait_ld();
+        }
+        const int d = 128 * (k >> 1) + tid;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) stage[(32 * (k & 1) + j) * kLatent + d] = have ? __uint_as_float(o[j]) : 0.0f;
+      }
+      if (!have && tid < 64) msh[tid] = -INFINITY;
+    }
+#pragma unroll 1
+    for (int k = 0; k < 8 && !p.cluster; ++k) {
       uint32_t o[32];
       if (have) {
         tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
@@ -821,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         else p.part_o[(prow_base + h) * kLatent + d] = x;
       }
     }
-    if (tid < H) {
+    if (tid < H && !p.cluster) {
       const float l = lsh[tid];
       const float m = have ? msh[tid] : -INFINITY;
       if (p.splits == 1) {
@@ -833,6 +881,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     tc::fence_before();
   }
 
+  if (p.cluster) {
+    // ---------------- merge of the cluster's splits ----------------
+    // Thread = (head tid / 8, every eighth float4 column of this CTA's slice); the weights of the splits
+    // for its head are computed once: w_s = 2^(m_s - M) / sum_s 2^(m_s - M) l_s over splits with l_s > 0.
+    __syncwarp();
+    cluster_sync();
+    const int S = p.splits;
+    const int h = tid >> 3, t8 = tid & 7;
+    const int c_lo = split * (kLatent / 4) / S, c_hi = (split + 1) * (kLatent / 4) / S;
+    const float* stage = reinterpret_cast<const float*>(smem + kRawOff);
+    const float* lsum = reinterpret_cast<const float*>(smem + kLsumOff);
+    if (h < H) {
+      float ms[8], ls[8];
+      float M = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        ms[s] = -INFINITY;
+        ls[s] = 0.0f;
+        if (s < S) {
+          ms[s] = ld_cluster_f32(cluster_addr(msh + h, s));
+          ls[s] = ld_cluster_f32(cluster_addr(lsum + h, s));
+          if (ls[s] > 0.0f) M = fmaxf(M, ms[s]);
+        }
+      }
+      float L = 0.0f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        ms[s] = (s < S && ls[s] > 0.0f) ? exp2f(ms[s] - M) : 0.0f;     // the split's weight
+        L += ms[s] * ls[s];
+      }
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      for (int c = c_lo + t8; c < c_hi; c += 8) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          if (s < S && ms[s] > 0.0f) {
+            const float4 v = ld_cluster_v4(cluster_addr(stage + h * kLatent + 4 * c, s));
+            acc.x += ms[s] * v.x; acc.y += ms[s] * v.y; acc.z += ms[s] * v.z; acc.w += ms[s] * v.w;
+          }
+        }
+        *reinterpret_cast<float4*>(p.out + (u.unit * H + h) * (int64_t)kLatent + 4 * c) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+      if (split == 0 && t8 == 0 && p.out_lse != nullptr)
+        p.out_lse[u.unit * H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+    // no CTA may leave while another still reads its shared memory
+    cluster_sync();
+  }
   __syncthreads();
   tc::fence_after();
   if (warp == kLogitsWarp) tc::dealloc(tbase, kTmemCols);
@@ -894,12 +991,59 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   cudaError_t e = ensure_smem_limit(attn_tc_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.splits, (unsigned)p.units);
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, map);
-  return cudaGetLastError();
+  if (!p.cluster) {
+    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, map);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, map);
+}
+
+int attn_max_clusters(int size) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> known;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(dev, size);
+  auto it = known.find(key);
+  if (it != known.end()) return it->second;
+  int n = 0;
+  if (ensure_smem_limit(attn_tc_kernel, kSmemBytes) == cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)size, 1, 1);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  known[key] = n;
+  return n;
 }
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
-  if (p.units == 0 || p.splits == 1) return cudaSuccess;
+  if (p.units == 0 || p.splits == 1 || p.cluster) return cudaSuccess;
   ProfScope prof("attn_combine", s);
   clear_stale_error();
   combine_kernel<<<(unsigned)(p.units * p.heads), 128, 0, s>>>(p);

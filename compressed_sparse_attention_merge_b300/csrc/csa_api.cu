@@ -73,7 +73,7 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 // ---------------------------------------------------------------------------------------------
 struct AttnLayout {
   int64_t units;
-  int n_ct, n_wt, splits, cache_splits, win_split;
+  int n_ct, n_wt, splits, cache_splits, win_split, cluster;
   size_t o_off, ml_off, total;
 };
 
@@ -89,8 +89,11 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   // the window tiles get a split of their own only if it still fits the one wave of CTAs
   L.win_split = (L.n_wt > 0 && L.units * (L.cache_splits + 1) <= num_sms) ? 1 : 0;
   L.splits = L.cache_splits + L.win_split;
+  // the splits of a unit merge in shared memory when they fit a portable cluster and every unit's
+  // cluster can be resident at once; otherwise through partials in the workspace and a combine kernel
+  L.cluster = (L.splits >= 2 && L.splits <= 8 && L.units <= attn_max_clusters(L.splits)) ? 1 : 0;
   L.o_off = CSA_WS_HEADER_BYTES;
-  const size_t parts = L.splits > 1 ? (size_t)L.units * L.splits * a->heads : 0;
+  const size_t parts = (L.splits > 1 && !L.cluster) ? (size_t)L.units * L.splits * a->heads : 0;
   L.ml_off = round_up(L.o_off + parts * kLatent * 4, 256);
   L.total = round_up(L.ml_off + parts * 2 * 4, 256);
   return L;
@@ -423,6 +426,7 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.swa = static_cast<const __nv_bfloat16*>(a->swa); p.swa_stride_b = a->swa_stride_b; p.swa_rows = a->swa_rows;
   p.swa_len = a->swa_len; p.swa_first_pos = a->swa_first_pos;
   p.splits = L.splits; p.cache_splits = L.cache_splits; p.win_split = L.win_split; p.n_ct = L.n_ct; p.n_wt = L.n_wt;
+  p.cluster = L.cluster;
   p.part_o = reinterpret_cast<float*>(w + L.o_off);
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
   p.out = a->out; p.out_lse = a->out_lse;

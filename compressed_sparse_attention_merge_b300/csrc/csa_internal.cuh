@@ -236,6 +236,9 @@ struct AttnParams {
   // blocks = 128 rows each); the n_wt window tiles (128 rows each) go to a split of their own when
   // win_split is set, else to the last cache split.
   int splits, cache_splits, win_split, n_ct, n_wt;
+  // cluster = 1: the splits of a unit form one thread-block cluster and are merged through distributed
+  // shared memory by the attention kernel itself (no partials, no combine launch).
+  int cluster;
   float* part_o;               // [units][splits][heads][512]
   float* part_ml;              // [units][splits][heads][2]
   float* out;                  // used when splits == 1
@@ -252,6 +255,8 @@ cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s
 cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
+// Clusters of `size` attention CTAs that can be resident at once on the current device (0 if none).
+int attn_max_clusters(int size);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
 
 // Clears an error that an earlier runtime call of another component left in this thread's last-error
