@@ -521,9 +521,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-# Per-launch DRAM bytes (read + write) of kernels from ncu captures: {(workload, kernel): bytes}.
-# Empty until a capture of the current kernels is taken.
-TRAFFIC = {}
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels from one
+# ncu capture of a one-replica run of the same workload (profiles/*_decode_64k_b32_h64.md):
+# {(workload, kernel): bytes}. An entry must be removed when its kernel changes.
+TRAFFIC = {
+    ("decode_64k_b32_h64", "sparse_attn"): 25_351_936 + 1_024,
+    ("decode_64k_b32_h64", "index_score"): 75_611_904 + 1_398_528,
+}
 
 
 # ------------------------------------------------------------------------------------------------
