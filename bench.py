@@ -597,7 +597,6 @@ def e2e_pipelined(w, host_in, args, world, device, comp):
 # ncu capture of a one-replica run of the same workload (profiles/*_decode_64k_b32_h64.md):
 # {(workload, kernel): bytes}. An entry must be removed when its kernel changes.
 TRAFFIC = {
-    ("decode_64k_b32_h64", "sparse_attn"): 25_351_936 + 1_024,
     ("decode_64k_b32_h64", "index_score"): 75_611_904 + 1_398_528,
 }
 

@@ -13,16 +13,17 @@
 //   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (values)
 // S and O accumulate in tensor memory; the row sums l are added up by one warp from the fp16
 // probabilities in shared memory (the same values the tensor core multiplies).
-//   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk into one of two
+//   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk into one of three
 //   raw stages. Two groups of four warps dequantise every tile: group A writes the logits operand
 //   straight into tensor memory (thread = row, 64-column panels, a four-panel ring); group B
-//   writes the values operand into a three-slot shared-memory ring of [128 latent x 64 row] units in the
+//   writes the values operand into a two-slot shared-memory ring of [128 latent x 64 row] units in the
 //   128-byte-swizzled MN-major layout.
 //   Window tiles: a tensor-map copy (TMA, 128-byte swizzle) lands the 128 bf16 rows in panel layout over
 //   the raw and ring areas; they are converted to fp16 in place and serve both products.
-// Pipelining: S is double-buffered in tensor memory and P in shared memory, and the logits and the
-// values have separate issuing threads, so that the logits of tile t+1 run while the softmax of tile t
-// works and the values of tile t run while the softmax of tile t+1 works.
+// Pipelining: S is double-buffered in tensor memory and the logits and the values have separate issuing
+// threads, so that the logits of tile t+1 run while the softmax of tile t works; the softmax of tile t+1
+// computes its probabilities while the values of tile t run and writes them once those have read P. A
+// third raw stage lets the copy of tile t+2 start while tile t's values operand is still being built.
 //
 // Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-7 group A, 8-11 group B, 12 gather,
 // 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps, per head, a
@@ -57,20 +58,23 @@ constexpr float kMaxProb = 256.0f;                         // 2^kRescaleSlack
 // shared-memory map (bytes); the operand regions start on 1024-byte boundaries
 constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB
 constexpr int kQOff = 0;                                   // queries: 8 K-major panels, 64 KB
-constexpr int kPBytes = kRows * 128;                       // one P^T buffer: 16 KB
-constexpr int kPOff = kQOff + kPanels * kQPanel;           // 65,536: two P^T buffers
+constexpr int kPBytes = kRows * 128;                       // the P^T buffer: 16 KB
+constexpr int kPOff = kQOff + kPanels * kQPanel;           // 65,536
 // Staged blocks are padded by 16 bytes so that the same byte of a row falls in a different bank in each
 // of 8 consecutive blocks.
 constexpr int kRawBlk = kLatBlk + 16;                      // 2,320
 constexpr int kRawStage = kTileBlocks * kRawBlk;           // 37,120
-constexpr int kRawOff = kPOff + 2 * kPBytes;               // 98,304
+constexpr int kRawStages = 3;
+constexpr int kRawOff = kPOff + kPBytes;                   // 81,920
 constexpr int kUnitBytes = 2 * 64 * 128;                   // values unit: 128 latent columns x 64 rows
-constexpr int kRing = 3;
-constexpr int kRingOff = (kRawOff + 2 * kRawStage + 1023) & ~1023;   // 173,056
+constexpr int kRing = 2;
+constexpr int kRingOff = (kRawOff + kRawStages * kRawStage + 1023) & ~1023;   // 193,536
 constexpr int kPanelBytes = kRows * 128;                   // 16 KB: one 64-column panel of a whole tile
 constexpr int kWinOff = kRawOff;                           // window tile: 8 panels over the raw and ring areas
-constexpr int kBarOff = kWinOff + kPanels * kPanelBytes;   // 229,376
-constexpr int kNumBars = 32;
+constexpr int kWinEnd = kWinOff + kPanels * kPanelBytes;   // 212,992: window panels, or the staged o
+constexpr int kRingEnd = kRingOff + kRing * kUnitBytes;    // 226,304
+constexpr int kBarOff = kRingEnd > kWinEnd ? kRingEnd : kWinEnd;
+constexpr int kNumBars = 36;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
 constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort
 constexpr int kMOff = kFlagOff + 16;                       // float m[64]
@@ -78,19 +82,20 @@ constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[2][64]
 constexpr int kRedOff = kAlphaOff + 2 * 64 * 4;            // float red[4][64]
 constexpr int kLsumOff = kRedOff + 4 * 64 * 4;             // float lsum[64]: final row sums
 constexpr int kSmemBytes = kLsumOff + 64 * 4;
-static_assert(kRingOff + kRing * kUnitBytes <= kBarOff, "the ring must lie inside the window overlay");
+static_assert(kWinOff % 1024 == 0 && kRingOff % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 constexpr int kTRing = 4;
 enum Bar {
-  RAW_FULL = 0, RAW_EMPTY = 2,          // raw stages: gather -> both dequantisation groups
-  TRING_FULL = 4,                       // logits operand panels in tensor memory: group A <-> logits issuer
+  RAW_FULL = 0,                         // raw stages: gather -> both dequantisation groups
+  RAW_EMPTY = RAW_FULL + kRawStages,
+  TRING_FULL = RAW_EMPTY + kRawStages,  // logits operand panels in tensor memory: group A <-> logits issuer
   TRING_EMPTY = TRING_FULL + kTRing,
   RING_FULL = TRING_EMPTY + kTRing,     // values operand units in shared memory: group B <-> values issuer
   RING_EMPTY = RING_FULL + kRing,
   S_FULL = RING_EMPTY + kRing,          // logits buffers: logits issuer <-> softmax
   S_EMPTY = S_FULL + 2,
-  P_FULL = S_EMPTY + 2,                 // probability buffers: softmax <-> values issuer and row-sum warp
+  P_FULL = S_EMPTY + 2,                 // the P buffer, per tile parity: softmax <-> values issuer, row sums
   PV_DONE = P_FULL + 2,
   WIN_FULL = PV_DONE + 2, WIN_CVT, WIN_EMPTY,
   FIN_L, FIN_V, NUM_BARS
@@ -301,9 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       mbar_init(&bars[TRING_FULL + i], 4);
       mbar_init(&bars[TRING_EMPTY + i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kRawStages; ++i) {
       mbar_init(&bars[RAW_FULL + i], 1);
       mbar_init(&bars[RAW_EMPTY + i], kDqWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[S_FULL + i], 1);
       mbar_init(&bars[S_EMPTY + i], 4);
       mbar_init(&bars[P_FULL + i], 4);
@@ -361,8 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     if (lane == 0) {
       int issued = 0, win_issued = 0;
       for (int it = 0; it < n_cache; ++it) {
-        const int stage = it & 1;
-        if (it >= 2 && !wait_bar(&bars[RAW_EMPTY + stage], ((it >> 1) - 1) & 1, abort_flag, p.hdr, 1)) break;
+        const int stage = it % kRawStages;
+        if (it >= kRawStages && !wait_bar(&bars[RAW_EMPTY + stage], (it / kRawStages - 1) & 1, abort_flag, p.hdr, 1)) break;
         const int t = c0 + it;
         uint8_t* dst = smem + kRawOff + stage * kRawStage;
         uint32_t bytes = 0;
@@ -385,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           mbar_arrive(&bars[RAW_FULL + stage]);
         }
         ++issued;
-        if (it == 1 || (it == 0 && n_cache == 1)) {
+        if (it == kRawStages - 1 || (it < kRawStages - 1 && it == n_cache - 1)) {
           // the later tiles of this CTA go to L2 now, so that refilling a raw stage costs an L2 read
-          for (int t2 = c0 + 2; t2 < c1; ++t2) {
+          for (int t2 = c0 + kRawStages; t2 < c1; ++t2) {
             for (int j = 0; j < kTileBlocks; ++j) {
               const int slot = t2 * kTileBlocks + j;
               const int64_t id = slot < p.top_k ? (int64_t)__ldg(p.idx + u.unit * p.top_k + slot) : -1;
@@ -411,7 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
       }
       // no copy into this CTA's shared memory may still be in flight when it exits
-      for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it) drain_bar(&bars[RAW_FULL + (it & 1)], (it >> 1) & 1);
+      for (int it = issued - kRawStages < 0 ? 0 : issued - kRawStages; it < issued; ++it)
+        drain_bar(&bars[RAW_FULL + it % kRawStages], (it / kRawStages) & 1);
       if (win_issued > 0) drain_bar(&bars[WIN_FULL], (win_issued - 1) & 1);
     }
   } else if (warp >= kGrpA0 && warp < kGrpA0 + kDqWarps) {
@@ -428,10 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       uint32_t t_k = 0;
       int id_next = n_cache > 0 ? cache_id(p, u, c0, r) : -1;
       for (int it = 0; it < n_cache && !stop; ++it) {
-        const int stage = it & 1;
+        const int stage = it % kRawStages;
         const bool vr = cache_ok(u, id_next, r);
         if (it + 1 < n_cache) id_next = cache_id(p, u, c0 + it + 1, r);
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it / kRawStages) & 1, abort_flag, p.hdr, 2))) break;
         const uint8_t* raw = smem + kRawOff + stage * kRawStage + blk * kRawBlk;
         const uint8_t* codes = raw + sl * 256;
         const uint8_t* scales = raw + 2048 + sl * 32;
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
       for (int q = 0; q < 4; ++q) ids_next[q] = n_cache > 0 ? cache_id(p, u, c0, 8 * (8 * (q >> 1) + 2 * bsel + (q & 1))) : -1;
       for (int it = 0; it < n_cache && !stop; ++it) {
-        const int stage = it & 1;
+        const int stage = it % kRawStages;
         uint32_t vmask = 0;       // bit 4 rh + (k & 3): row attended
 #pragma unroll
         for (int rh = 0; rh < 2; ++rh) {
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
           for (int q = 0; q < 4; ++q) ids_next[q] = cache_id(p, u, c0 + it + 1, 8 * (8 * (q >> 1) + 2 * bsel + (q & 1)));
         }
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it >> 1) & 1, abort_flag, p.hdr, 2))) break;
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it / kRawStages) & 1, abort_flag, p.hdr, 2))) break;
         const uint8_t* raw = smem + kRawOff + stage * kRawStage;
         for (int unit = 0; unit < 8; ++unit) {
           const int ch = unit >> 1, rh = unit & 1;
@@ -621,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       for (int it = 0; it < n_tiles; ++it) {
         const int pb = it & 1;
         const bool cache = it < n_cache;
-        const uint32_t p_addr = s_base + kPOff + pb * kPBytes;
+        const uint32_t p_addr = s_base + kPOff;
         if (!wait_bar(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 5)) break;
         tc::fence_after();
         bool ok = true;
@@ -674,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         l0 *= alpha[64 * pb + h0];
         l1 *= alpha[64 * pb + h0 + 1];
       }
-      const uint8_t* pbuf = smem + kPOff + pb * kPBytes + (lane & 3) * 4;
+      const uint8_t* pbuf = smem + kPOff + (lane & 3) * 4;
       float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
 #pragma unroll 8
       for (int r = 0; r < kRows; r += 2) {
@@ -713,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       }
       const uint32_t s_col = kColS + 64 * sb;
       if (!all_softmax(wait_bar(&bars[S_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
-      // P buffer sb, alpha[sb] and flag[sb] were last read by the values and row sums of tile it - 2
+      // alpha[sb] and flag[sb] were last read by the row sums of tile it - 2
       if (it >= 2) {
         if (!all_softmax(wait_bar(&bars[PV_DONE + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
       }
@@ -811,8 +819,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
+      // P was read by the values and the row sums of tile it - 1
+      if (it >= 1) {
+        if (!all_softmax(wait_bar(&bars[PV_DONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 14))) {
+          ok = false;
+          break;
+        }
+      }
       // probabilities, fp16, row `row` of P (MN-major: 64 heads contiguous, 128-byte swizzle)
-      uint8_t* prow = smem + kPOff + sb * kPBytes + row * 128;
+      uint8_t* prow = smem + kPOff + row * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
