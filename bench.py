@@ -751,7 +751,8 @@ def run_reference(args):
     line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "launch": "CUDA graph per step", "sample": what},
+            "config": {"workload": args.workload, "launch": "the oracle (numpy, fp64) on the host cores",
+                       "sample": what},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": what},
