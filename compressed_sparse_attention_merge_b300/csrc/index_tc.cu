@@ -16,7 +16,8 @@
 // four epilogue warps (thread = entry) write the keys' scale factors into tensor memory before the product
 // and afterwards apply ReLU, the head weights, the ordered head sum and the causal mask, and take the block
 // maximum across the 8 lanes that hold one block. The accumulator is double-buffered so that the epilogue
-// of one stage overlaps the product of the next.
+// of one stage overlaps the product of the next, and the copy warp starts the first stages before the
+// queries are prepared.
 #include <cuda.h>
 
 #include <cstring>
@@ -185,7 +186,8 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
   const int64_t k1 = stages_per_unit * (blockIdx.x + 1) / splits;
   const int n = (int)(k1 - k0);
 
-  // ---------------- setup: barriers, tensor memory, the unit's FP4 queries ----------------
+  // ---------------- setup: barriers and tensor memory; then the copies start while the other warps
+  // prepare the unit's FP4 queries ----------------
   if (warp == 1) tc::alloc(tmem_ptr, C::kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); mbar_init(&sfr[i], 4); }
@@ -194,53 +196,10 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
     fence_mbar_init();
     *abort_flag = 0;
   }
-  uint8_t* qcodes = smem + C::kQOff;
-  uint8_t* qsc = smem + C::kQScOff;
-  int32_t* pos_sh = reinterpret_cast<int32_t*>(smem + C::kPosOff);
-  for (int q = tid; q < NQ; q += kThreads)
-    pos_sh[q] = (p.q_pos != nullptr && q < u.nq) ? __ldg(p.q_pos + u.b * p.n_query + u.j0 + q) : INT32_MAX;
-  for (int t = tid; t < N * C::kRowScales; t += kThreads) {
-    const int row = t / C::kRowScales, g = t % C::kRowScales;       // row = q * HI + h
-    const int q = row / HI, h = row % HI;
-    float v[16];
-    const bool have = q < u.nq && h < HI;
-    const float* src = p.q_idx + ((u.b * p.n_query + u.j0 + q) * HI + h) * (int64_t)DI + g * 16;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = have ? __ldg(src + j) : 0.0f;
-    uint32_t lo, hi;
-    const uint32_t sb = quantize16_pow2(v, &lo, &hi);
-    const int chunk = (g * 8) >> 4, within = (g * 8) & 15;
-    uint8_t* dst = qcodes + row * C::kRowCodes + ((chunk ^ ((row >> C::kSwzShift) & C::kSwzMask)) << 4) + within;
-    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-    qsc[row * C::kRowScales + g] = (uint8_t)sb;
-  }
-  tc::fence_proxy_async();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tmem_ptr;
-
-  if (warp >= 2) {
-    // query scale factors: column n at lane 32 j + n % 32, column kColSFB + 4 s + n / 32, for every
-    // subpartition j (each epilogue warp writes its own copy)
-    const int sp = warp & 3;
-    const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
-#pragma unroll
-    for (int s = 0; s < C::kMmas; ++s) {
-#pragma unroll
-      for (int c = 0; c < (N + 31) / 32; ++c) {
-        const int nn = lane + 32 * c;
-        uint32_t w = 0;
-        if (nn < N) w = *reinterpret_cast<const uint32_t*>(qsc + nn * C::kRowScales + 4 * s);
-        st_32x1(tbase + lane_base + C::kColSFB + 4 * s + c, w);
-      }
-    }
-    tc::wait_st();
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-
   const uint32_t s_base = smem_addr(smem);
   if (warp == 0) {
     // ---------------- tensor-map copies of the key stages ----------------
@@ -267,7 +226,54 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
       for (int k = issued - kStages < 0 ? 0 : issued - kStages; k < issued; ++k)
         drain(&full[k % kStages], (k / kStages) & 1);
     }
-  } else if (warp == 1) {
+  } else {
+  constexpr int kSetupThreads = kThreads - 32;
+  const int qt = tid - 32;
+  uint8_t* qcodes = smem + C::kQOff;
+  uint8_t* qsc = smem + C::kQScOff;
+  int32_t* pos_sh = reinterpret_cast<int32_t*>(smem + C::kPosOff);
+  for (int q = qt; q < NQ; q += kSetupThreads)
+    pos_sh[q] = (p.q_pos != nullptr && q < u.nq) ? __ldg(p.q_pos + u.b * p.n_query + u.j0 + q) : INT32_MAX;
+  for (int t = qt; t < N * C::kRowScales; t += kSetupThreads) {
+    const int row = t / C::kRowScales, g = t % C::kRowScales;       // row = q * HI + h
+    const int q = row / HI, h = row % HI;
+    float v[16];
+    const bool have = q < u.nq && h < HI;
+    const float* src = p.q_idx + ((u.b * p.n_query + u.j0 + q) * HI + h) * (int64_t)DI + g * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = have ? __ldg(src + j) : 0.0f;
+    uint32_t lo, hi;
+    const uint32_t sb = quantize16_pow2(v, &lo, &hi);
+    const int chunk = (g * 8) >> 4, within = (g * 8) & 15;
+    uint8_t* dst = qcodes + row * C::kRowCodes + ((chunk ^ ((row >> C::kSwzShift) & C::kSwzMask)) << 4) + within;
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+    qsc[row * C::kRowScales + g] = (uint8_t)sb;
+  }
+  tc::fence_proxy_async();
+  asm volatile("bar.sync 1, %0;" :: "n"(kSetupThreads) : "memory");
+
+  if (warp >= 2) {
+    // query scale factors: column n at lane 32 j + n % 32, column kColSFB + 4 s + n / 32, for every
+    // subpartition j (each epilogue warp writes its own copy)
+    const int sp = warp & 3;
+    const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
+#pragma unroll
+    for (int s = 0; s < C::kMmas; ++s) {
+#pragma unroll
+      for (int c = 0; c < (N + 31) / 32; ++c) {
+        const int nn = lane + 32 * c;
+        uint32_t w = 0;
+        if (nn < N) w = *reinterpret_cast<const uint32_t*>(qsc + nn * C::kRowScales + 4 * s);
+        st_32x1(tbase + lane_base + C::kColSFB + 4 * s + c, w);
+      }
+    }
+    tc::wait_st();
+  }
+  tc::fence_before();
+  asm volatile("bar.sync 1, %0;" :: "n"(kSetupThreads) : "memory");
+  tc::fence_after();
+
+  if (warp == 1) {
     // ---------------- products ----------------
     if (lane == 0) {
       for (int k = 0; k < n; ++k) {
@@ -364,6 +370,7 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
       __syncwarp();
       if (lane == 0) mbar_arrive(&dempty[db]);
     }
+  }
   }
   tc::fence_before();
   __syncthreads();
