@@ -378,51 +378,71 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
   if (warp == 1) tc::dealloc(tbase, C::kTmemCols);
 }
 
-// Super-block scores: one warp per (unit, super-block), lanes over the feature index; the query is the
-// same FP4 rounding (power-of-two scale per 16 elements) as in the block products.
+// Super-block scores. A CTA takes one unit and kCoarsePerCta super-blocks: it rounds the unit's queries
+// to FP4 once (16-element groups, power-of-two scales: the rounding the block products use) into shared
+// memory, then each warp scores its super-blocks with lanes over the feature index (per-lane fused
+// multiply-adds in feature order, then a butterfly sum), the ReLU, the head weights and the ordered head
+// sum.
+constexpr int kCoarsePerWarp = 8;
+constexpr int kCoarsePerCta = 8 * kCoarsePerWarp;
+
 __global__ void __launch_bounds__(256) coarse_score_kernel(CoarseScoreParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t units = p.batch * p.n_query;
-  if (gw >= units * p.n_super) return;
-  const int64_t unit = gw / p.n_super, g = gw % p.n_super;
+  extern __shared__ float xq_sh[];                 // [heads][dim]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t unit = blockIdx.y;
   const int64_t b = unit / p.n_query;
   const int64_t n_e = p.n_entries[b];
-  float* dst = p.scores + unit * p.n_super + g;
-  if (g * (int64_t)kSuper * kBlockEntries >= n_e) {
-    if (lane == 0) *dst = -INFINITY;
-    return;
-  }
-  const float* crow = p.coarse + b * p.coarse_stride_b + g * p.dim;
-  float s = 0.0f;
-  for (int h = 0; h < p.heads; ++h) {
-    const float* qrow = p.q_idx + (unit * p.heads + h) * (int64_t)p.dim;
-    float d = 0.0f;
-    for (int i0 = 0; i0 < p.dim; i0 += 32) {
-      // lanes i0 .. i0+31 hold two 16-element groups; round each to FP4 like the block products do
-      const float x = __ldg(qrow + i0 + lane);
-      float amax = fabsf(x);
+  const int groups = p.heads * p.dim / 16;
+  for (int t = threadIdx.x; t < groups; t += blockDim.x) {
+    const float* src = p.q_idx + unit * p.heads * (int64_t)p.dim + t * 16;
+    float v[16];
 #pragma unroll
-      for (int off = 1; off < 16; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float sf = __fdiv_rn(amax, 6.0f);
-      float sc = 0.0f;
-      if (sf > 0.0f) pow2_scale(sf, &sc);
+    for (int j = 0; j < 16; ++j) v[j] = __ldg(src + j);
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    const float sf = __fdiv_rn(amax, 6.0f);
+    float sc = 0.0f;
+    if (sf > 0.0f) pow2_scale(sf, &sc);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
       float xq = 0.0f;
       if (sc > 0.0f) {
-        const uint32_t code = e2m1_code(__fdiv_rn(x, sc));
-        const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-        xq = __fmul_rn((code & 8u) ? -mag[code & 7u] : mag[code & 7u], sc);
+        const uint32_t h2 = e2m1x2_to_f16x2(e2m1_code(__fdiv_rn(v[j], sc)));
+        xq = __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))), sc);
       }
-      d = fmaf(xq, __ldg(crow + i0 + lane), d);
+      xq_sh[t * 16 + j] = xq;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    if (p.relu) d = fmaxf(d, 0.0f);
-    const float wgt = p.head_w ? __ldg(p.head_w + h) : 1.0f;
-    const float t = __fmul_rn(wgt, d);
-    s = (h == 0) ? t : __fadd_rn(s, t);
   }
-  if (lane == 0) *dst = __fadd_rn(s, 0.0f);
+  __syncthreads();
+  for (int j = 0; j < kCoarsePerWarp; ++j) {
+    const int64_t g = (int64_t)blockIdx.x * kCoarsePerCta + warp * kCoarsePerWarp + j;
+    if (g >= p.n_super) break;
+    float* dst = p.scores + unit * p.n_super + g;
+    if (g * (int64_t)kSuper * kBlockEntries >= n_e) {
+      if (lane == 0) *dst = -INFINITY;
+      continue;
+    }
+    const float* crow = p.coarse + b * p.coarse_stride_b + g * p.dim;
+    float c[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = 32 * k < p.dim ? __ldg(crow + 32 * k + lane) : 0.0f;
+    float s = 0.0f;
+    for (int h = 0; h < p.heads; ++h) {
+      const float* xq = xq_sh + h * p.dim;
+      float d = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (32 * k < p.dim) d = fmaf(xq[32 * k + lane], c[k], d);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      if (p.relu) d = fmaxf(d, 0.0f);
+      const float wgt = p.head_w ? __ldg(p.head_w + h) : 1.0f;
+      const float t = __fmul_rn(wgt, d);
+      s = (h == 0) ? t : __fadd_rn(s, t);
+    }
+    if (lane == 0) *dst = __fadd_rn(s, 0.0f);
+  }
 }
 
 template <int DI, int HI, int N>
@@ -509,12 +529,13 @@ cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s
 }
 
 cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s) {
-  const int64_t warps = p.batch * p.n_query * p.n_super;
-  if (warps == 0) return cudaSuccess;
+  const int64_t units = p.batch * p.n_query;
+  if (units == 0 || p.n_super == 0) return cudaSuccess;
+  if (units > 65535 || p.dim > 256) return cudaErrorInvalidValue;
   ProfScope prof("coarse_score", s);
-  const int64_t blocks = (warps + 7) / 8;
   clear_stale_error();
-  coarse_score_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  dim3 grid((unsigned)((p.n_super + kCoarsePerCta - 1) / kCoarsePerCta), (unsigned)units);
+  coarse_score_kernel<<<grid, 256, (size_t)p.heads * p.dim * sizeof(float), s>>>(p);
   return cudaGetLastError();
 }
 

@@ -99,12 +99,13 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
 // coarse_sum[b][g][d] = fp32 sum, ascending entry order, of the dequantised element d of entries
 // [512 g, min(512 (g + 1), first + n_new)), for every super-block g touched by this call. One CTA per
 // (super-block, sequence), one thread per element d: the super-block's packed bytes are staged through
-// shared memory in chunks with coalesced 16-byte loads, and each thread then sums its element over the
-// chunk's entries in ascending order.
+// shared memory in chunks, each one bulk copy, and each thread then sums its element over the chunk's
+// entries in ascending order.
 constexpr int kCoarseStage = 36864;
 
 __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touched) {
   __shared__ __align__(16) uint8_t stage[kCoarseStage];
+  __shared__ __align__(8) uint64_t bar;
   const int d = threadIdx.x;                     // blockDim.x == dim
   const int gl = blockIdx.x;
   const int64_t b = blockIdx.y;
@@ -120,26 +121,41 @@ __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touc
   const int half = p.dim / 2, groups = p.dim / kGroup;
   const int chunk_blocks = kCoarseStage / bb < kSuper ? kCoarseStage / bb : kSuper;
   const uint8_t* seq = p.cache + b * p.cache_stride_b;
-  const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+  if (d == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
   float acc = 0.0f;
+  uint32_t phase = 0;
   for (int64_t blk0 = g * kSuper; blk0 * kBlockEntries < e_hi; blk0 += chunk_blocks) {
     const int64_t n_e = e_hi - blk0 * kBlockEntries;
     const int nb = (int)((n_e + kBlockEntries - 1) / kBlockEntries < chunk_blocks
                              ? (n_e + kBlockEntries - 1) / kBlockEntries : chunk_blocks);
-    __syncthreads();
-    const uint4* src = reinterpret_cast<const uint4*>(seq + blk0 * bb);
-    for (int i = d; i < nb * bb / 16; i += blockDim.x) reinterpret_cast<uint4*>(stage)[i] = __ldg(src + i);
-    __syncthreads();
+    __syncthreads();                             // the previous chunk has been read (and bar initialised)
+    if (d == 0) {
+      mbar_arrive_expect_tx(&bar, (uint32_t)(nb * bb));
+      bulk_g2s(stage, seq + blk0 * bb, (uint32_t)(nb * bb), &bar);
+    }
+    if (!__syncthreads_and(mbar_wait(&bar, phase))) {
+      // give up: report, let the copy land (bounded), leave without writing a sum
+      if (d == 0) {
+        report(p.hdr, CSA_ERR_TIMEOUT, KID_COARSE_SUM, (uint32_t)b);
+        mbar_wait(&bar, phase);
+      }
+      return;
+    }
+    phase ^= 1u;
     const int ne = (int)(n_e < (int64_t)nb * kBlockEntries ? n_e : (int64_t)nb * kBlockEntries);
 #pragma unroll 8
     for (int i = 0; i < ne; ++i) {
       const uint8_t* blk = stage + (i >> 3) * bb;
       const int slot = i & 7;
-      const uint32_t byte = blk[slot * half + d / 2];
-      const uint32_t code = (d & 1) ? (byte >> 4) : (byte & 0xFu);
+      // both nibbles of the byte to fp16 (exact), this thread's element, times the group scale (exact in
+      // fp32), added in ascending entry order
+      const uint32_t h2 = e2m1x2_to_f16x2(blk[slot * half + d / 2]);
+      const float x = __half2float(__ushort_as_half((unsigned short)((d & 1) ? (h2 >> 16) : (h2 & 0xFFFFu))));
       const float sc = e4m3_to_float(blk[kBlockEntries * half + slot * groups + d / kGroup]);
-      const float v = __fmul_rn((code & 8u) ? -mag[code & 7u] : mag[code & 7u], sc);
-      acc = __fadd_rn(acc, v);
+      acc = __fadd_rn(acc, __fmul_rn(x, sc));
     }
   }
   p.coarse_sum[b * p.coarse_stride_b + g * p.dim + d] = acc;
