@@ -264,8 +264,16 @@ class PrefillWorkload:
         return {"q": self.q, "q_idx": self.q_idx, "new_tokens": self.chunk, "new_keys": self.chunk_keys}
 
 
-def make_workload(name, device, replicas, keep_inputs=False):
+def shard_case(name, shard):
+    """The workload's case for one rank: rank r draws its own sequences (seed offset by 1000 r), so that N
+    ranks hold N different shards of one global batch."""
+    import dataclasses
     case = _cases()[name]
+    return dataclasses.replace(case, seed=case.seed + 1000 * shard) if shard else case
+
+
+def make_workload(name, device, replicas, keep_inputs=False, shard=0):
+    case = shard_case(name, shard)
     if name.startswith("prefill"):
         return PrefillWorkload(case, device, replicas, keep_inputs)
     return DecodeWorkload(case, device, replicas, keep_inputs)
@@ -370,7 +378,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     csa.lib()
 
-    w = make_workload(args.workload, device, args.replicas)
+    w = make_workload(args.workload, device, args.replicas, shard=rank)
     R = args.replicas
     stream = torch.cuda.current_stream(device)
 
