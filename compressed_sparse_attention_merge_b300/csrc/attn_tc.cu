@@ -76,7 +76,7 @@ constexpr int kRingEnd = kRingOff + kRing * kUnitBytes;    // 226,304
 constexpr int kBarOff = kRingEnd > kWinEnd ? kRingEnd : kWinEnd;
 constexpr int kNumBars = 36;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
-constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort
+constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort, int have (cluster staging)
 constexpr int kMOff = kFlagOff + 16;                       // float m[64]
 constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[2][64]: per P buffer
 constexpr int kRedOff = kAlphaOff + 2 * 64 * 4;            // float red[4][64]
@@ -188,6 +188,12 @@ __device__ __forceinline__ bool cache_ok(const UnitCtx& u, int64_t id, int r) {
 // Bulk prefetch of a global range into L2 (no shared-memory destination, no completion).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
+// Prefetch of one [1 x 128 x 64] box of a tensor map into L2.
+__device__ __forceinline__ void prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
 }
 
 // First window-buffer row of window tile tw (may be negative or past the buffer: those rows are filled
@@ -400,6 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
               const int64_t id = slot < p.top_k ? (int64_t)__ldg(p.idx + u.unit * p.top_k + slot) : -1;
               if (id >= 0 && id < u.n_b) prefetch_l2(seq + id * kLatBlk, kLatBlk);
             }
+          }
+          // and the window rows, read once the cache tiles are done (boxes inside the buffer only)
+          for (int tw = 0; tw < nw; ++tw) {
+            const int64_t y0 = window_row0(p, u, tw);
+            if (y0 < 0 || y0 + kRows > p.swa_rows) continue;
+            for (int pp = 0; pp < kPanels; ++pp) prefetch_l2_3d(&swa_map, pp * 64, (int)y0, (int)u.b);
           }
         }
       }
@@ -847,20 +859,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const int64_t prow_base = (u.unit * p.splits + split) * H;
     if (p.cluster) {
-      // stage o as [head][512] fp32 over the operand area (every product has completed); m and l are
-      // already in shared memory
-      float* stage = reinterpret_cast<float*>(smem + kRawOff);
-#pragma unroll 1
-      for (int k = 0; k < 8; ++k) {
-        uint32_t o[32];
-        if (have) {
-          tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
-          tc::wait_ld();
-        }
-        const int d = 128 * (k >> 1) + tid;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) stage[(32 * (k & 1) + j) * kLatent + d] = have ? __uint_as_float(o[j]) : 0.0f;
-      }
+      // o is staged by every warp after the roles end; m and l are already in shared memory
+      if (tid == 0) flag[3] = have ? 1 : 0;
       if (!have && tid < 64) msh[tid] = -INFINITY;
     }
 #pragma unroll 1
@@ -897,10 +897,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   }
 
   if (p.cluster) {
+    // ---------------- staging of o: [head][512] fp32 over the operand area ----------------
+    // Every product has completed (the softmax saw the last values finish). Warp w reads tensor-memory
+    // subpartition w % 4 (latent columns 32 (w % 4) .. of each 128-column chunk), 32-column pieces
+    // 2 (w / 4) and 2 (w / 4) + 1.
+    __syncwarp();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    {
+      const bool had = flag[3] != 0;
+      float* stage = reinterpret_cast<float*>(smem + kRawOff);
+      const uint32_t sp_base = (uint32_t)((warp & 3) * 32) << 16;
+#pragma unroll 1
+      for (int k = 2 * (warp >> 2); k < 2 * (warp >> 2) + 2; ++k) {
+        uint32_t o[32];
+        if (had) {
+          tc::ld_32x32(tbase + sp_base + kColO + 32 * k, o);
+          tc::wait_ld();
+        }
+        const int d = 128 * (k >> 1) + 32 * (warp & 3) + lane;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) stage[(32 * (k & 1) + j) * kLatent + d] = had ? __uint_as_float(o[j]) : 0.0f;
+      }
+    }
     // ---------------- merge of the cluster's splits ----------------
     // Thread = (head tid / 8, every eighth float4 column of this CTA's slice); the weights of the splits
     // for its head are computed once: w_s = 2^(m_s - M) / sum_s 2^(m_s - M) l_s over splits with l_s > 0.
-    __syncwarp();
     cluster_sync();
     const int S = p.splits;
     const int h = tid >> 3, t8 = tid & 7;
