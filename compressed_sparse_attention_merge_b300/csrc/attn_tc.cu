@@ -296,8 +296,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 
   // this CTA's tiles: cache tiles [c0, c1), then nw window tiles
   const bool win_only = p.win_split && split == p.splits - 1;
-  const int c0 = win_only ? 0 : (int)((int64_t)split * p.n_ct / p.cache_splits);
-  const int c1 = win_only ? 0 : (int)((int64_t)(split + 1) * p.n_ct / p.cache_splits);
+  int c0 = 0, c1 = 0;
+  if (!win_only) {
+    if (p.last_ct >= 0) {
+      const int rest = p.n_ct - p.last_ct, others = p.cache_splits - 1;
+      c0 = split < others ? split * rest / others : rest;
+      c1 = split < others ? (split + 1) * rest / others : p.n_ct;
+    } else {
+      c0 = (int)((int64_t)split * p.n_ct / p.cache_splits);
+      c1 = (int)((int64_t)(split + 1) * p.n_ct / p.cache_splits);
+    }
+  }
   const int nw = (win_only || (!p.win_split && split == p.cache_splits - 1)) ? p.n_wt : 0;
   const int n_cache = c1 - c0;
   const int n_tiles = n_cache + nw;

@@ -73,7 +73,7 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 // ---------------------------------------------------------------------------------------------
 struct AttnLayout {
   int64_t units;
-  int n_ct, n_wt, splits, cache_splits, win_split, cluster;
+  int n_ct, n_wt, splits, cache_splits, win_split, cluster, last_ct;
   size_t o_off, ml_off, total;
 };
 
@@ -89,6 +89,16 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   // the window tiles get a split of their own only if it still fits the one wave of CTAs
   L.win_split = (L.n_wt > 0 && L.units * (L.cache_splits + 1) <= num_sms) ? 1 : 0;
   L.splits = L.cache_splits + L.win_split;
+  // When the last cache split also takes the window tiles, it gets fewer cache tiles: a window tile
+  // (converted in place, its copy not overlapped with a previous tile) costs about 1.5 cache tiles.
+  L.last_ct = -1;
+  if (!L.win_split && L.n_wt > 0 && L.cache_splits > 1) {
+    const double per = (L.n_ct + 1.5 * L.n_wt) / L.cache_splits;
+    int last = (int)(per - 1.5 * L.n_wt + 0.5);
+    if (last < 0) last = 0;
+    if (last > L.n_ct - (L.cache_splits - 1)) last = L.n_ct - (L.cache_splits - 1);
+    L.last_ct = last;
+  }
   // the splits of a unit merge in shared memory when they fit a portable cluster and every unit's
   // cluster can be resident at once; otherwise through partials in the workspace and a combine kernel
   L.cluster = (L.splits >= 2 && L.splits <= 8 && L.units <= attn_max_clusters(L.splits)) ? 1 : 0;
@@ -427,6 +437,7 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.swa_len = a->swa_len; p.swa_first_pos = a->swa_first_pos;
   p.splits = L.splits; p.cache_splits = L.cache_splits; p.win_split = L.win_split; p.n_ct = L.n_ct; p.n_wt = L.n_wt;
   p.cluster = L.cluster;
+  p.last_ct = L.last_ct;
   p.part_o = reinterpret_cast<float*>(w + L.o_off);
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
   p.out = a->out; p.out_lse = a->out_lse;

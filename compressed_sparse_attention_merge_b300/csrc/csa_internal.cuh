@@ -236,6 +236,9 @@ struct AttnParams {
   // blocks = 128 rows each); the n_wt window tiles (128 rows each) go to a split of their own when
   // win_split is set, else to the last cache split.
   int splits, cache_splits, win_split, n_ct, n_wt;
+  // last_ct >= 0: the last cache split, which then also takes the window tiles, gets cache tiles
+  // [n_ct - last_ct, n_ct) and the others share the rest evenly; -1: every cache split gets an even share.
+  int last_ct;
   // cluster = 1: the splits of a unit form one thread-block cluster and are merged through distributed
   // shared memory by the attention kernel itself (no partials, no combine launch).
   int cluster;
