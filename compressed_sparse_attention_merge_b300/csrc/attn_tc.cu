@@ -26,9 +26,9 @@
 // third raw stage lets the copy of tile t+2 start while tile t's values operand is still being built.
 //
 // Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-7 group A, 8-11 group B, 12 gather,
-// 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps, per head, a
-// reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in log2
-// units), so the probabilities stay below 2^8 and the accumulators are rescaled rarely. Splits write
+// 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps,
+// per head, a reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in
+// log2 units), so the probabilities stay below 2^8 and the accumulators are rescaled rarely. Splits write
 // unnormalised partials (o, m, l); the combine kernel merges them in split order. When the splits of a
 // unit form one thread-block cluster, each CTA stages its (o, m, l) in its own shared memory instead and
 // CTA r merges latent columns [512 r / S, 512 (r + 1) / S) of every split, in split order, through
