@@ -9,8 +9,9 @@ import torch
 
 from oracle import attention as o_attn
 from oracle import fp4 as o_fp4
+from oracle import indexer as o_idx
 
-from _pipeline import (SCALE, assert_attn_close, assert_lse_close, gpu_decode_attn, gpu_pack_sequences,
+from _pipeline import (SCALE, assert_attn_close, assert_lse_close, gpu_decode_attn, gpu_index, gpu_pack_sequences,
                        gpu_prefill_attn, to_np)
 
 pytestmark = pytest.mark.gpu
@@ -73,6 +74,40 @@ def test_decode_matches_oracle(csa, heads, top_k, batch):
                                                sf[b, :int(swa_len[b])], SCALE)
         assert_attn_close(out[b, 0], ref, f"seq {b}")
         assert_lse_close(lse[b, 0], ref_lse, f"seq {b}")
+
+
+def test_multi_token_decode_end_to_end(csa):
+    # speculative verification: four query positions per sequence in one decode call, each with its own
+    # indexer query and Top-K; in decode every query sees the whole cache prefix and the same window
+    g = torch.Generator(device=DEV).manual_seed(31)
+    tokens, B, Q, H, K, W, HI, DI = [1800, 640], 2, 4, 64, 32, 128, 4, 128
+    T = max(tokens)
+    E = T // 2
+    n_e = [t // 2 for t in tokens]
+    x = _latents(g, B, T)
+    keys = torch.randint(-4, 5, (B, E, DI), generator=g, device=DEV).float()
+    q_idx = torch.randint(-4, 5, (B, Q, HI, DI), generator=g, device=DEV).float()
+    q = torch.randn(B, Q, H, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa = torch.randn(B, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa_len = torch.tensor([W, 60], dtype=torch.int32, device=DEV)
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, tokens, E, 512, 2, csa.SCALE_AMAX, ws)
+    kcache = gpu_pack_sequences(csa, keys, n_e, E, DI, 1, csa.SCALE_POW2, ws)
+    n_entries = torch.tensor(n_e, dtype=torch.int32, device=DEV)
+    idx, _ = gpu_index(csa, q_idx, kcache, n_entries, E, K)
+    out, lse = gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, E, W)
+    idx, out, lse = idx.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy()
+    xf, qf, sf, kf, qi = to_np(x), to_np(q), to_np(swa), keys.cpu().numpy(), q_idx.cpu().numpy()
+    for b in range(B):
+        deq_k = o_fp4.dequantize(o_fp4.pack(kf[b, :n_e[b]], 1, "pow2", n_blocks=-(-E // 8)), DI, E)
+        ref_idx, _ = o_idx.flat_topk(qi[b], deq_k, n_e[b], K)
+        np.testing.assert_array_equal(idx[b], ref_idx, err_msg=f"seq {b}")
+        entries = o_fp4.dequantize(o_fp4.pack(xf[b, :tokens[b]], 2, "amax", n_blocks=-(-E // 8)), 512, E)
+        for j in range(Q):
+            ref, ref_lse = o_attn.decode_attention(qf[b, j].astype(np.float64), entries, n_e[b], ref_idx[j],
+                                                   sf[b, :int(swa_len[b])], SCALE)
+            assert_attn_close(out[b, j], ref, f"seq {b} query {j}")
+            assert_lse_close(lse[b, j], ref_lse, f"seq {b} query {j}")
 
 
 def test_split_and_unsplit_agree(csa):
