@@ -7,64 +7,61 @@
 // is stated in include/csa.h; every fp32 step uses an explicit round-to-nearest intrinsic so that the
 // bytes do not depend on contraction or fast-math choices.
 //
-// One thread quantises one 16-element group: a warp covers 32 consecutive groups (a whole 512-d entry),
-// so loads (2 x 32 B or 1 x 32 B per thread) and stores (8 code bytes + 1 scale byte per thread) are
-// contiguous across the warp. The kernel is HBM-bound.
+// Four threads (a quad) quantise one 16-element group, four elements each: the group maximum is taken with
+// two shuffles inside the quad, each thread divides and encodes its own four elements and stores their two
+// code bytes, and the quad's first thread stores the scale byte. A warp covers 8 consecutive groups, so
+// loads and stores are contiguous across the warp.
 #include "csa_internal.cuh"
 
 namespace csa {
 namespace {
 
-__device__ __forceinline__ void load16(const void* base, int dtype, int64_t elem_off, float* v) {
+__device__ __forceinline__ void load4(const void* base, int dtype, int64_t elem_off, float* v) {
   if (dtype == CSA_DTYPE_BF16) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem_off);
-    uint4 a = __ldg(p), b = __ldg(p + 1);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem_off));
+    v[0] = __uint_as_float(w.x << 16);
+    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16);
+    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
   } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float4 f = __ldg(p + i);
-      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
-    }
+    const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off));
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
   }
 }
 
 __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
   const int groups = p.dim / kGroup;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t gt = t >> 2;                     // the group of this thread's quad
+  const int j = (int)(t & 3);                    // elements 4 j .. 4 j + 3 of the group
   const int64_t total = p.batch * p.n_new * groups;
-  if (t >= total) return;
-  const int g = (int)(t % groups);
-  const int64_t i = (t / groups) % p.n_new;
-  const int64_t b = t / ((int64_t)groups * p.n_new);
+  if (gt >= total) return;                       // whole quads leave together
+  const int g = (int)(gt % groups);
+  const int64_t i = (gt / groups) % p.n_new;
+  const int64_t b = gt / ((int64_t)groups * p.n_new);
 
   const int64_t first = p.first_entry ? (int64_t)p.first_entry[b] : 0;
   if (first < 0 || first + p.n_new > p.max_entries) {
-    if (i == 0 && g == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_PACK, (uint32_t)b);
+    if (i == 0 && g == 0 && j == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_PACK, (uint32_t)b);
     return;
   }
 
-  float m[16];
-  const int64_t row0 = b * p.x_stride_b + (int64_t)g * kGroup;
+  float m[4];
+  const int64_t el = b * p.x_stride_b + (int64_t)g * kGroup + 4 * j;
   if (p.merge == 2) {
-    float a[16], c[16];
-    load16(p.x, p.x_dtype, row0 + (2 * i) * p.x_stride_t, a);
-    load16(p.x, p.x_dtype, row0 + (2 * i + 1) * p.x_stride_t, c);
+    float a[4], c[4];
+    load4(p.x, p.x_dtype, el + (2 * i) * p.x_stride_t, a);
+    load4(p.x, p.x_dtype, el + (2 * i + 1) * p.x_stride_t, c);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m[j] = __fmul_rn(__fadd_rn(a[j], c[j]), 0.5f);
+    for (int k = 0; k < 4; ++k) m[k] = __fmul_rn(__fadd_rn(a[k], c[k]), 0.5f);
   } else {
-    load16(p.x, p.x_dtype, row0 + i * p.x_stride_t, m);
+    load4(p.x, p.x_dtype, el + i * p.x_stride_t, m);
   }
 
-  float amax = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(m[j]));
+  float amax = fmaxf(fmaxf(fabsf(m[0]), fabsf(m[1])), fmaxf(fabsf(m[2]), fabsf(m[3])));
+  const unsigned quad = 0xFu << (threadIdx.x & 28u);
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
   const float sf = __fdiv_rn(amax, 6.0f);
 
   uint32_t sbyte = 0;
@@ -78,22 +75,17 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
     }
   }
 
-  uint32_t lo = 0, hi = 0;
+  uint32_t codes = 0;                            // two bytes: elements 4 j .. 4 j + 3, low nibble first
   if (s > 0.0f) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t c0 = e2m1_code(__fdiv_rn(m[2 * j], s));
-      const uint32_t c1 = e2m1_code(__fdiv_rn(m[2 * j + 1], s));
-      const uint32_t byte = c0 | (c1 << 4);
-      if (j < 4) lo |= byte << (8 * j); else hi |= byte << (8 * (j - 4));
-    }
+    for (int k = 0; k < 4; ++k) codes |= e2m1_code(__fdiv_rn(m[k], s)) << (4 * k);
   }
 
   const int64_t e = first + i;
   uint8_t* blk = p.cache + b * p.cache_stride_b + (e / kBlockEntries) * (int64_t)block_bytes(p.dim);
   const int slot = (int)(e % kBlockEntries);
-  *reinterpret_cast<uint2*>(blk + slot * (p.dim / 2) + g * 8) = make_uint2(lo, hi);
-  blk[kBlockEntries * (p.dim / 2) + slot * groups + g] = (uint8_t)sbyte;
+  *reinterpret_cast<uint16_t*>(blk + slot * (p.dim / 2) + g * 8 + 2 * j) = (uint16_t)codes;
+  if (j == 0) blk[kBlockEntries * (p.dim / 2) + slot * groups + g] = (uint8_t)sbyte;
 }
 
 // coarse_sum[b][g][d] = fp32 sum, ascending entry order, of the dequantised element d of entries
@@ -164,7 +156,7 @@ __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touc
 }  // namespace
 
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
-  const int64_t total = p.batch * p.n_new * (p.dim / kGroup);
+  const int64_t total = 4 * p.batch * p.n_new * (p.dim / kGroup);      // four threads per group
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
