@@ -7,35 +7,56 @@
 // is stated in include/csa.h; every fp32 step uses an explicit round-to-nearest intrinsic so that the
 // bytes do not depend on contraction or fast-math choices.
 //
-// Four threads (a quad) quantise one 16-element group, four elements each: the group maximum is taken with
-// two shuffles inside the quad, each thread divides and encodes its own four elements and stores their two
-// code bytes, and the quad's first thread stores the scale byte. A warp covers 8 consecutive groups, so
-// loads and stores are contiguous across the warp.
+// TPG threads quantise one 16-element group, 16 / TPG elements each. With TPG = 4 (small calls, such as
+// the per-step append) the group maximum is taken with two shuffles inside the quad and each thread
+// divides and encodes four elements, which shortens the per-thread chain; with TPG = 1 (bulk calls) a
+// thread takes a whole group with two 32-byte loads, which keeps the loads wide. Either way a warp's loads
+// and stores are contiguous, and the first thread of a group stores its scale byte.
 #include "csa_internal.cuh"
 
 namespace csa {
 namespace {
 
-__device__ __forceinline__ void load4(const void* base, int dtype, int64_t elem_off, float* v) {
+// n (4 or 16) consecutive elements from elem_off (a multiple of n) as fp32.
+template <int n>
+__device__ __forceinline__ void load_n(const void* base, int dtype, int64_t elem_off, float* v) {
   if (dtype == CSA_DTYPE_BF16) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem_off));
-    v[0] = __uint_as_float(w.x << 16);
-    v[1] = __uint_as_float(w.x & 0xFFFF0000u);
-    v[2] = __uint_as_float(w.y << 16);
-    v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    uint32_t w[n / 2];
+    if (n >= 8) {
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + elem_off);
+#pragma unroll
+      for (int i = 0; i < n / 8; ++i) {
+        const uint4 x = __ldg(p + i);
+        w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+      }
+    } else {
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem_off));
+      w[0] = x.x; w[1] = x.y;
+    }
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
   } else {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off));
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off);
+#pragma unroll
+    for (int i = 0; i < n / 4; ++i) {
+      const float4 f = __ldg(p + i);
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
   }
 }
 
+template <int TPG>
 __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
+  constexpr int EPT = kGroup / TPG;              // elements per thread
   const int groups = p.dim / kGroup;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t gt = t >> 2;                     // the group of this thread's quad
-  const int j = (int)(t & 3);                    // elements 4 j .. 4 j + 3 of the group
+  const int64_t gt = t / TPG;                    // this thread's group
+  const int j = (int)(t % TPG);                  // elements EPT j .. EPT j + EPT - 1 of the group
   const int64_t total = p.batch * p.n_new * groups;
-  if (gt >= total) return;                       // whole quads leave together
+  if (gt >= total) return;                       // the threads of a group leave together
   const int g = (int)(gt % groups);
   const int64_t i = (gt / groups) % p.n_new;
   const int64_t b = gt / ((int64_t)groups * p.n_new);
@@ -46,22 +67,26 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
     return;
   }
 
-  float m[4];
-  const int64_t el = b * p.x_stride_b + (int64_t)g * kGroup + 4 * j;
+  float m[EPT];
+  const int64_t el = b * p.x_stride_b + (int64_t)g * kGroup + EPT * j;
   if (p.merge == 2) {
-    float a[4], c[4];
-    load4(p.x, p.x_dtype, el + (2 * i) * p.x_stride_t, a);
-    load4(p.x, p.x_dtype, el + (2 * i + 1) * p.x_stride_t, c);
+    float a[EPT], c[EPT];
+    load_n<EPT>(p.x, p.x_dtype, el + (2 * i) * p.x_stride_t, a);
+    load_n<EPT>(p.x, p.x_dtype, el + (2 * i + 1) * p.x_stride_t, c);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) m[k] = __fmul_rn(__fadd_rn(a[k], c[k]), 0.5f);
+    for (int k = 0; k < EPT; ++k) m[k] = __fmul_rn(__fadd_rn(a[k], c[k]), 0.5f);
   } else {
-    load4(p.x, p.x_dtype, el + i * p.x_stride_t, m);
+    load_n<EPT>(p.x, p.x_dtype, el + i * p.x_stride_t, m);
   }
 
-  float amax = fmaxf(fmaxf(fabsf(m[0]), fabsf(m[1])), fmaxf(fabsf(m[2]), fabsf(m[3])));
-  const unsigned quad = 0xFu << (threadIdx.x & 28u);
-  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < EPT; ++k) amax = fmaxf(amax, fabsf(m[k]));
+  if (TPG == 4) {
+    const unsigned quad = 0xFu << (threadIdx.x & 28u);
+    amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(quad, amax, 2));
+  }
   const float sf = __fdiv_rn(amax, 6.0f);
 
   uint32_t sbyte = 0;
@@ -75,16 +100,18 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
     }
   }
 
-  uint32_t codes = 0;                            // two bytes: elements 4 j .. 4 j + 3, low nibble first
+  uint32_t codes[EPT / 8 > 0 ? EPT / 8 : 1] = {};    // EPT / 2 code bytes, low nibble first
   if (s > 0.0f) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) codes |= e2m1_code(__fdiv_rn(m[k], s)) << (4 * k);
+    for (int k = 0; k < EPT; ++k) codes[k / 8] |= e2m1_code(__fdiv_rn(m[k], s)) << (4 * (k % 8));
   }
 
   const int64_t e = first + i;
   uint8_t* blk = p.cache + b * p.cache_stride_b + (e / kBlockEntries) * (int64_t)block_bytes(p.dim);
   const int slot = (int)(e % kBlockEntries);
-  *reinterpret_cast<uint16_t*>(blk + slot * (p.dim / 2) + g * 8 + 2 * j) = (uint16_t)codes;
+  uint8_t* dst = blk + slot * (p.dim / 2) + g * 8 + (EPT / 2) * j;
+  if (EPT == 16) *reinterpret_cast<uint2*>(dst) = make_uint2(codes[0], codes[EPT / 8 > 1 ? 1 : 0]);
+  else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)codes[0];
   if (j == 0) blk[kBlockEntries * (p.dim / 2) + slot * groups + g] = (uint8_t)sbyte;
 }
 
@@ -156,13 +183,18 @@ __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touc
 }  // namespace
 
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
-  const int64_t total = 4 * p.batch * p.n_new * (p.dim / kGroup);      // four threads per group
-  if (total == 0) return cudaSuccess;
+  const int64_t groups = p.batch * p.n_new * (p.dim / kGroup);
+  if (groups == 0) return cudaSuccess;
   const int threads = 256;
-  const int64_t blocks = (total + threads - 1) / threads;
   ProfScope prof("pack_fp4", s);
   clear_stale_error();
-  pack_fp4_kernel<<<(unsigned)blocks, threads, 0, s>>>(p);
+  // a quad per group while the call is smaller than eight 256-thread CTAs on each of 148 SMs (the modes
+  // write the same bytes; the choice only trades per-thread latency against load width)
+  if (groups * 4 <= (int64_t)8 * threads * 148) {
+    pack_fp4_kernel<4><<<(unsigned)((groups * 4 + threads - 1) / threads), threads, 0, s>>>(p);
+  } else {
+    pack_fp4_kernel<1><<<(unsigned)((groups + threads - 1) / threads), threads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
