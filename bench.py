@@ -132,10 +132,11 @@ class DecodeWorkload:
         new_keys = self.new_keys if new_keys is None else new_keys
         out = self.out if out is None else out
         cache, kcache, coarse = self.caches[r], self.kcaches[r], self.coarses[r]
-        csa.pack_fp4(new_tokens, cache, merge=2, scale_rule=csa.SCALE_AMAX, max_entries=self.E, ws=self.ws_pack,
-                     first_entry=self.first)
-        csa.pack_fp4(new_keys, kcache, merge=1, scale_rule=csa.SCALE_POW2, max_entries=self.E, ws=self.ws_pack,
-                     first_entry=self.first, coarse_sum=coarse)
+        # both appends (latent pair, index key) in one launch
+        csa.pack_fp4_multi([
+            (new_tokens, cache, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=self.E, first_entry=self.first)),
+            (new_keys, kcache, dict(merge=1, scale_rule=csa.SCALE_POW2, max_entries=self.E, first_entry=self.first,
+                                    coarse_sum=coarse))], ws=self.ws_pack)
         src, n_idx = 0, 0
         for layer, mode in enumerate(self.modes):
             if mode != "reuse":
@@ -227,10 +228,10 @@ class PrefillWorkload:
         ckeys = self.chunk_keys if new_keys is None else new_keys
         out = self.out if out is None else out
         cache, kcache = self.caches[r], self.kcaches[r]
-        csa.pack_fp4(chunk, cache, merge=2, scale_rule=csa.SCALE_AMAX, max_entries=self.E, ws=self.ws_pack,
-                     first_entry=self.first)
-        csa.pack_fp4(ckeys, kcache, merge=1, scale_rule=csa.SCALE_POW2, max_entries=self.E, ws=self.ws_pack,
-                     first_entry=self.first)
+        csa.pack_fp4_multi([
+            (chunk, cache, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=self.E, first_entry=self.first)),
+            (ckeys, kcache, dict(merge=1, scale_rule=csa.SCALE_POW2, max_entries=self.E, first_entry=self.first))],
+            ws=self.ws_pack)
         csa.index_topk(q_idx, kcache, self.n_entries, self.idx, max_entries=self.E, top_k=c.top_k,
                        ws=self.ws_index, q_pos=self.q_pos)
         csa.sparse_attn_prefill(q, cache, self.n_entries, self.idx, out, q_pos=self.q_pos, max_entries=self.E,
@@ -470,6 +471,11 @@ def run_ours(args):
     e2e_eager_ms = timed(e2e_step)
     del e2e_graphs, graphs
     e2e_ms = e2e_pipelined(w, host_in, args, world, device, stream)
+    # a device check or a bounded wait that gave up in any run above voids the measurement
+    for ws_name in ("ws_pack", "ws_index", "ws_attn"):
+        st = csa.device_status(getattr(w, ws_name))
+        if st != csa.OK:
+            raise RuntimeError(f"{ws_name}: device status {st} after the timed runs")
 
     peaks = _peaks()
     kernels = {}
@@ -508,7 +514,8 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp4-e2m1/e4m3 cache, fp16 mma f32 accumulate", "data": "synthetic",
-        "config": {"workload": args.workload, "launch": "CUDA graph per step", "batch_per_gpu": w.case.batch if hasattr(w.case, "batch") else 1,
+        "config": {"workload": args.workload, "launch": "CUDA graph per step",
+                   "batch_per_gpu": w.case.batch if hasattr(w.case, "batch") else 1,
                    "queries_per_step_per_gpu": w.queries_per_step, "layers": len(w.modes),
                    "l2": f"{R} cache replicas in rotation, {round(R * touched_bytes(w) / 1e6, 1)} MB touched "
                          f"per rotation > 126 MB L2",

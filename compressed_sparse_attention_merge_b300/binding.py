@@ -90,6 +90,8 @@ def lib():
         L.csa_get_device_status.argtypes = [P, P]
         L.csa_pack_fp4.restype = I32
         L.csa_pack_fp4.argtypes = [I64, ctypes.POINTER(PackArgs), P, SZ, P]
+        L.csa_pack_fp4_multi.restype = I32
+        L.csa_pack_fp4_multi.argtypes = [I32, ctypes.POINTER(I64), ctypes.POINTER(PackArgs), P, SZ, P]
         L.csa_index_topk_workspace_size.restype = SZ
         L.csa_index_topk_workspace_size.argtypes = [I64, ctypes.POINTER(IndexArgs)]
         L.csa_index_topk.restype = I32
@@ -213,6 +215,26 @@ def pack_fp4(x, cache, *, merge, scale_rule, max_entries, ws, first_entry=None, 
     a = pack_args(x, cache, merge=merge, scale_rule=scale_rule, max_entries=max_entries,
                   first_entry=first_entry, coarse_sum=coarse_sum)
     _check(lib().csa_pack_fp4(x.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "csa_pack_fp4")
+
+
+PACK_MAX_JOBS = 4
+
+
+def pack_fp4_multi(jobs, *, ws, stream=None):
+    """csa_pack_fp4_multi: several pack_fp4 calls in one launch. jobs is a list of (x, cache, kwargs),
+    kwargs being pack_fp4's keyword arguments other than ws and stream. No two jobs may write the same
+    cache entries."""
+    if not 1 <= len(jobs) <= PACK_MAX_JOBS:
+        raise ValueError(f"1..{PACK_MAX_JOBS} jobs")
+    arr = (PackArgs * len(jobs))()
+    batches = (ctypes.c_int64 * len(jobs))()
+    for j, (x, cache, kw) in enumerate(jobs):
+        if not x.is_cuda:
+            raise ValueError("x must be a CUDA tensor")
+        arr[j] = pack_args(x, cache, **kw)
+        batches[j] = x.shape[0]
+    _check(lib().csa_pack_fp4_multi(len(jobs), batches, arr, _ptr(ws), ws.numel(), _stream(stream)),
+           "csa_pack_fp4_multi")
 
 
 def index_args(q_idx, keys, n_entries, out_idx, *, max_entries, top_k, head_w=None, relu=True, q_pos=None,

@@ -257,7 +257,8 @@ csa_status csa_get_device_status(void* ws, cudaStream_t stream) {
 }
 
 // ------------------------------------------------------------------------------------------------
-csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+// Host-side checks of one pack call and its kernel parameters; *empty is set when there is nothing to pack.
+static csa_status pack_params(int64_t batch, const csa_pack_args* a, void* ws, PackParams* p, bool* empty) {
   if (a == nullptr || batch < 0) return CSA_ERR_INVALID_ARG;
   if (a->x_dtype != CSA_DTYPE_BF16 && a->x_dtype != CSA_DTYPE_F32) return CSA_ERR_INVALID_ARG;
   if (a->merge != 1 && a->merge != 2) return CSA_ERR_INVALID_ARG;
@@ -265,12 +266,9 @@ csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* a, void* ws, size_t 
   if (a->dim <= 0 || a->dim % 64 != 0 || a->dim > 1024) return CSA_ERR_INVALID_ARG;
   if (a->n_tokens < 0 || a->max_entries < 0) return CSA_ERR_INVALID_ARG;
   if (batch > 65535) return CSA_ERR_INVALID_ARG;
-  csa_status st = current_device(nullptr);
-  if (st != CSA_OK) return st;
-  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
-  if (st != CSA_OK) return st;
   const int64_t n_new = a->n_tokens / a->merge;
-  if (batch == 0 || n_new == 0) return CSA_OK;
+  *empty = batch == 0 || n_new == 0;
+  if (*empty) return CSA_OK;
   if (a->x == nullptr || a->cache == nullptr) return CSA_ERR_INVALID_ARG;
   const int esz = a->x_dtype == CSA_DTYPE_BF16 ? 2 : 4;
   if (!aligned(a->x, 16) || !aligned(a->cache, 16)) return CSA_ERR_ALIGNMENT;
@@ -286,16 +284,50 @@ csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* a, void* ws, size_t 
     if (batch > 1 && a->coarse_stride_b < n_super * a->dim) return CSA_ERR_INVALID_ARG;
     if (ceil_div(n_new, per_super) + 1 > 65535) return CSA_ERR_INVALID_ARG;
   }
+  *p = PackParams{};
+  p->x = a->x; p->x_dtype = a->x_dtype; p->dim = a->dim; p->merge = a->merge; p->scale_rule = a->scale_rule;
+  p->x_stride_b = a->x_stride_b; p->x_stride_t = a->x_stride_t; p->n_new = n_new; p->batch = batch;
+  p->max_entries = a->max_entries; p->first_entry = a->first_entry;
+  p->cache = a->cache; p->cache_stride_b = a->cache_stride_b;
+  p->coarse_sum = a->coarse_sum; p->coarse_stride_b = a->coarse_stride_b;
+  p->hdr = static_cast<uint32_t*>(ws);
+  return CSA_OK;
+}
 
-  PackParams p{};
-  p.x = a->x; p.x_dtype = a->x_dtype; p.dim = a->dim; p.merge = a->merge; p.scale_rule = a->scale_rule;
-  p.x_stride_b = a->x_stride_b; p.x_stride_t = a->x_stride_t; p.n_new = n_new; p.batch = batch;
-  p.max_entries = a->max_entries; p.first_entry = a->first_entry;
-  p.cache = a->cache; p.cache_stride_b = a->cache_stride_b;
-  p.coarse_sum = a->coarse_sum; p.coarse_stride_b = a->coarse_stride_b;
-  p.hdr = static_cast<uint32_t*>(ws);
+csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  PackParams p;
+  bool empty = false;
+  csa_status st = pack_params(batch, a, ws, &p, &empty);
+  if (st != CSA_OK) return st;
+  st = current_device(nullptr);
+  if (st != CSA_OK) return st;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  if (empty) return CSA_OK;
   if (cudaError_t e = launch_pack(p, stream)) return cuda_fail(e, "pack");
   if (cudaError_t e = launch_coarse_sum(p, stream)) return cuda_fail(e, "coarse_sum");
+  return CSA_OK;
+}
+
+csa_status csa_pack_fp4_multi(int n_jobs, const int64_t* batch, const csa_pack_args* args, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  if (n_jobs < 1 || n_jobs > CSA_PACK_MAX_JOBS || batch == nullptr || args == nullptr) return CSA_ERR_INVALID_ARG;
+  PackParams jobs[CSA_PACK_MAX_JOBS];
+  int n = 0;
+  for (int j = 0; j < n_jobs; ++j) {
+    bool empty = false;
+    const csa_status st = pack_params(batch[j], &args[j], ws, &jobs[n], &empty);
+    if (st != CSA_OK) return st;
+    if (!empty) ++n;
+  }
+  csa_status st = current_device(nullptr);
+  if (st != CSA_OK) return st;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  if (n == 0) return CSA_OK;
+  if (cudaError_t e = launch_pack_multi(jobs, n, stream)) return cuda_fail(e, "pack");
+  for (int j = 0; j < n; ++j)
+    if (cudaError_t e = launch_coarse_sum(jobs[j], stream)) return cuda_fail(e, "coarse_sum");
   return CSA_OK;
 }
 

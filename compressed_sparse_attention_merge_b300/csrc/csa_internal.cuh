@@ -167,6 +167,13 @@ struct PackParams {
   uint32_t* hdr;
 };
 
+// Several pack jobs in one launch: job j covers CTAs [cta_begin[j], cta_begin[j + 1]).
+struct PackMulti {
+  PackParams job[CSA_PACK_MAX_JOBS];
+  int64_t cta_begin[CSA_PACK_MAX_JOBS + 1];
+  int n;
+};
+
 struct ScoreParams {
   // queries
   const float* q_idx;          // [batch][n_query][heads][dim]
@@ -253,6 +260,7 @@ struct AttnParams {
 // Launchers (one per kernel file). Each returns the launch error, if any.
 // ------------------------------------------------------------------------------------------------
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
+cudaError_t launch_pack_multi(const PackParams* jobs, int n, cudaStream_t s);
 cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s);
 cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s);

@@ -48,11 +48,11 @@ __device__ __forceinline__ void load_n(const void* base, int dtype, int64_t elem
   }
 }
 
+// Thread t of a pack job: element slice j = t % TPG of group t / TPG.
 template <int TPG>
-__global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
+__device__ __forceinline__ void pack_thread(const PackParams& p, int64_t t) {
   constexpr int EPT = kGroup / TPG;              // elements per thread
   const int groups = p.dim / kGroup;
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t gt = t / TPG;                    // this thread's group
   const int j = (int)(t % TPG);                  // elements EPT j .. EPT j + EPT - 1 of the group
   const int64_t total = p.batch * p.n_new * groups;
@@ -113,6 +113,19 @@ __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
   if (EPT == 16) *reinterpret_cast<uint2*>(dst) = make_uint2(codes[0], codes[EPT / 8 > 1 ? 1 : 0]);
   else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)codes[0];
   if (j == 0) blk[kBlockEntries * (p.dim / 2) + slot * groups + g] = (uint8_t)sbyte;
+}
+
+template <int TPG>
+__global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
+  pack_thread<TPG>(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+}
+
+// Several jobs in one launch; each CTA belongs to one job (its CTA range in m.cta_begin).
+template <int TPG>
+__global__ void __launch_bounds__(256) pack_fp4_multi_kernel(const __grid_constant__ PackMulti m) {
+  int j = 0;
+  while (j + 1 < m.n && (int64_t)blockIdx.x >= m.cta_begin[j + 1]) ++j;
+  pack_thread<TPG>(m.job[j], ((int64_t)blockIdx.x - m.cta_begin[j]) * blockDim.x + threadIdx.x);
 }
 
 // coarse_sum[b][g][d] = fp32 sum, ascending entry order, of the dequantised element d of entries
@@ -195,6 +208,31 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
   } else {
     pack_fp4_kernel<1><<<(unsigned)((groups + threads - 1) / threads), threads, 0, s>>>(p);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_multi(const PackParams* jobs, int n, cudaStream_t s) {
+  const int threads = 256;
+  int64_t total = 0;
+  for (int j = 0; j < n; ++j) total += jobs[j].batch * jobs[j].n_new * (jobs[j].dim / kGroup);
+  if (total == 0) return cudaSuccess;
+  // the same per-group choice as launch_pack, taken on the jobs' total
+  const int tpg = total * 4 <= (int64_t)8 * threads * 148 ? 4 : 1;
+  PackMulti m{};
+  int64_t ctas = 0;
+  for (int j = 0; j < n; ++j) {
+    const int64_t groups = jobs[j].batch * jobs[j].n_new * (jobs[j].dim / kGroup);
+    if (groups == 0) continue;
+    m.job[m.n] = jobs[j];
+    m.cta_begin[m.n] = ctas;
+    ctas += (groups * tpg + threads - 1) / threads;
+    ++m.n;
+  }
+  m.cta_begin[m.n] = ctas;
+  ProfScope prof("pack_fp4", s);
+  clear_stale_error();
+  if (tpg == 4) pack_fp4_multi_kernel<4><<<(unsigned)ctas, threads, 0, s>>>(m);
+  else pack_fp4_multi_kernel<1><<<(unsigned)ctas, threads, 0, s>>>(m);
   return cudaGetLastError();
 }
 

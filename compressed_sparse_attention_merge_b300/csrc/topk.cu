@@ -142,43 +142,54 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
 }
 
 // Register-resident variant for n <= 1024 * KPT: thread t holds the keys of ids [t KPT, t KPT + KPT), so
-// thread order is id order. Histogram atomics are aggregated per warp over equal digits (long runs of
-// equal scores are common), the bin search runs in one warp, and one block scan of packed
-// (equal-count, greater-count) pairs places every selected id.
+// thread order is id order. Each pass adds its digits to one of two shared histograms with plain atomics
+// (on this hardware they beat warp-aggregated ones even when every key has the same digit) and clears the
+// other for the next pass, so a pass needs two barriers; one warp finds the bin, and one block scan of
+// packed (equal-count, greater-count) pairs places every selected id.
 template <int KPT>
-__global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkParams p) {
-  __shared__ uint32_t hist[256];
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(TopkParams p) {
+  __shared__ uint32_t hist[2][256];
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_prefix, s_krem, s_ncand;
   const int64_t unit = blockIdx.x;
   const float* sc = p.scores + unit * p.score_stride;
   int32_t* out = p.out + unit * p.out_stride;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 512; i += kTopkThreads) (&hist[0][0])[i] = 0u;
 
   uint32_t key[KPT];
+  const int64_t id0 = (int64_t)tid * KPT;
+  if (id0 + KPT <= p.n && (reinterpret_cast<uintptr_t>(sc) & 15u) == 0) {
 #pragma unroll
-  for (int i = 0; i < KPT; ++i) {
-    const int64_t id = (int64_t)tid * KPT + i;
-    key[i] = id < p.n ? order_key(__ldg(sc + id)) : 0u;     // 0 < key of -inf: never a candidate
+    for (int i = 0; i < KPT / 4; ++i) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(sc + id0) + i);
+      key[4 * i] = order_key(f.x);
+      key[4 * i + 1] = order_key(f.y);
+      key[4 * i + 2] = order_key(f.z);
+      key[4 * i + 3] = order_key(f.w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) key[i] = id0 + i < p.n ? order_key(__ldg(sc + id0 + i)) : 0u;   // 0: no candidate
   }
+  __syncthreads();
+
   const uint32_t k = (uint32_t)p.k;
   uint32_t prefix = 0u, mask = 0u, krem = k, ncand = 0u;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
-    __syncthreads();
+  int cur = 0;
+  for (int shift = 24; shift >= 0; shift -= 8, cur ^= 1) {
 #pragma unroll
     for (int i = 0; i < KPT; ++i) {
-      const bool in = key[i] > kNegInfKey && (key[i] & mask) == prefix;
-      const uint32_t digit = in ? (key[i] >> shift) & 0xFFu : 256u;
-      const uint32_t same = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(same) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(same));
+      if (key[i] > kNegInfKey && (key[i] & mask) == prefix)
+        atomicAdd(&hist[cur][(key[i] >> shift) & 0xFFu], 1u);
     }
+    for (int i = tid; i < 256; i += kTopkThreads) hist[cur ^ 1][i] = 0u;   // the next pass's bins
     __syncthreads();
     if (warp == 0) {
       // lane l owns bins 255 - 8 l .. 248 - 8 l (descending)
       uint32_t b[8], own = 0u;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { b[i] = hist[255 - 8 * lane - i]; own += b[i]; }
+      for (int i = 0; i < 8; ++i) { b[i] = hist[cur][255 - 8 * lane - i]; own += b[i]; }
       uint32_t incl = own;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -189,14 +200,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkParams p) {
       if (shift == 24 && lane == 0) s_ncand = total;
       const uint32_t hit = __ballot_sync(0xffffffffu, incl >= krem);
       if (hit != 0u && lane == __ffs(hit) - 1) {
-        uint32_t cum = incl - own;
-        int i = 0;
-        for (; i < 7; ++i) {
-          if (cum + b[i] >= krem) break;
+        // the first of this lane's bins where the running count reaches krem (the last one otherwise)
+        uint32_t cum = incl - own, before = 0u;
+        int sel = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (sel < 0 && (cum + b[i] >= krem || i == 7)) { sel = i; before = cum; }
           cum += b[i];
         }
-        s_krem = krem - cum;
-        s_prefix = prefix | ((uint32_t)(255 - 8 * lane - i) << shift);
+        s_krem = krem - before;
+        s_prefix = prefix | ((uint32_t)(255 - 8 * lane - sel) << shift);
       }
       if (hit == 0u && lane == 0) { s_krem = 0u; s_prefix = prefix; }   // fewer candidates than k
     }
@@ -208,7 +221,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkParams p) {
     krem = s_krem;
     prefix = s_prefix;
     mask |= 0xFFu << shift;
-    __syncthreads();
   }
   const bool take_all = ncand <= k;
   const uint32_t T = take_all ? kNegInfKey : prefix;
@@ -252,7 +264,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_reg_kernel(TopkParams p) {
       ++eq_before;
     }
     if (take) {
-      const int64_t idx = (int64_t)tid * KPT + i;
+      const int64_t idx = id0 + i;
       int32_t id = (int32_t)idx;
       if (p.map_super != nullptr) {
         const int32_t g = p.map_super[unit * p.map_stride + idx / kSuper];

@@ -156,6 +156,21 @@ typedef struct csa_pack_args {
 csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* args, void* ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+/* csa_pack_fp4_multi -- n_jobs csa_pack_fp4 calls (job j: batch[j] sequences, args[j]) in as few
+ * launches as their sizes allow. A decode step appends to the latent cache and to the index-key cache, and
+ * this call does both in one launch. The result equals the calls made one after another in job order,
+ * provided no two jobs write the same cache entry or the same coarse sums. If they do, the bytes are
+ * undefined. Every job is validated as csa_pack_fp4 validates it before anything is launched; a job
+ * that fails validation fails the whole call, and nothing is launched.
+ *   n_jobs  1..CSA_PACK_MAX_JOBS.
+ *   batch   host int64 [n_jobs].
+ *   args    host [n_jobs].
+ *   ws      one workspace header, shared by all jobs; it records the first device check of any job.
+ * Jobs whose batch or new-entry count is 0 are skipped. */
+#define CSA_PACK_MAX_JOBS 4
+csa_status csa_pack_fp4_multi(int n_jobs, const int64_t* batch, const csa_pack_args* args, void* ws,
+                              size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------------------------------
  * csa_index_topk -- score cache blocks with an indexer query and select the Top-K blocks.
  *

@@ -26,9 +26,10 @@ def declared_functions():
     return sorted(n for n in names if not n.endswith("_t"))
 
 
-def test_header_declares_the_four_entry_points():
+def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("csa_pack_fp4", "csa_index_topk", "csa_sparse_attn_decode", "csa_sparse_attn_prefill"):
+    for n in ("csa_pack_fp4", "csa_pack_fp4_multi", "csa_index_topk", "csa_sparse_attn_decode",
+              "csa_sparse_attn_prefill"):
         assert n in names
 
 
@@ -61,6 +62,15 @@ def test_validation_rejects_before_any_device_call(lib):
     pa = b.PackArgs()
     pa.x_dtype, pa.dim, pa.merge, pa.scale_rule = 0, 100, 2, 0       # dim not a multiple of 64
     assert lib.csa_pack_fp4(1, ctypes.byref(pa), None, 0, None) == b.ERR_INVALID_ARG
+    # multi-job pack: job count out of range, missing arrays, one bad job fails the call
+    jobs = (b.PackArgs * 2)()
+    batches = (ctypes.c_int64 * 2)(1, 1)
+    assert lib.csa_pack_fp4_multi(0, batches, jobs, None, 0, None) == b.ERR_INVALID_ARG
+    assert lib.csa_pack_fp4_multi(b.PACK_MAX_JOBS + 1, batches, jobs, None, 0, None) == b.ERR_INVALID_ARG
+    assert lib.csa_pack_fp4_multi(1, None, jobs, None, 0, None) == b.ERR_INVALID_ARG
+    jobs[0].x_dtype, jobs[0].dim, jobs[0].merge, jobs[0].scale_rule = 0, 512, 2, 0
+    jobs[1].x_dtype, jobs[1].dim, jobs[1].merge, jobs[1].scale_rule = 0, 512, 3, 0     # merge 3
+    assert lib.csa_pack_fp4_multi(2, batches, jobs, None, 0, None) == b.ERR_INVALID_ARG
     # unsupported indexer shape / attention head count
     ia = b.IndexArgs()
     ia.n_query, ia.heads, ia.dim, ia.top_k, ia.flags = 1, 3, 128, 8, b.IDX_RELU

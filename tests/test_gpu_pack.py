@@ -105,3 +105,68 @@ def test_capacity_overflow_is_reported_not_written(csa):
     assert csa.device_status(ws) == csa.ERR_DEVICE_CHECK
     assert int(cache.sum()) == 0
     assert csa.device_status(ws) == csa.OK                       # reading clears the status word
+
+
+def test_multi_job_pack_equals_the_single_calls(csa):
+    # a decode step's two appends in one launch (latent pair-merge under AMAX at first_entry, index keys
+    # under POW2 with coarse sums), plus a job with no whole pair, which is skipped
+    g = torch.Generator(device=DEV).manual_seed(6)
+    B, E, D = 3, 1200, 128
+    lat_prior = torch.randn(B, 2 * 900, 512, generator=g, device=DEV).to(torch.bfloat16)
+    lat_new = torch.randn(B, 2 * 3, 512, generator=g, device=DEV).to(torch.bfloat16)
+    keys = torch.randint(-4, 5, (B, 903, D), generator=g, device=DEV).float()
+    ws = csa.workspace(256, DEV)
+    cache = csa.empty_cache(B, E, 512, DEV)
+    kcache = csa.empty_cache(B, E, D, DEV)
+    coarse = csa.empty_coarse(B, E, D, DEV)
+    csa.pack_fp4(lat_prior, cache, merge=2, scale_rule=csa.SCALE_AMAX, max_entries=E, ws=ws)
+    csa.pack_fp4(keys[:, :900].contiguous(), kcache, merge=1, scale_rule=csa.SCALE_POW2, max_entries=E, ws=ws,
+                 coarse_sum=coarse)
+    first = torch.full((B,), 900, dtype=torch.int32, device=DEV)
+    odd = torch.ones(B, 1, 512, dtype=torch.bfloat16, device=DEV)
+    spare = csa.empty_cache(B, E, 512, DEV)
+    csa.pack_fp4_multi([
+        (lat_new, cache, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=E, first_entry=first)),
+        (keys[:, 900:].contiguous(), kcache, dict(merge=1, scale_rule=csa.SCALE_POW2, max_entries=E,
+                                                  first_entry=first, coarse_sum=coarse)),
+        (odd, spare, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=E)),
+    ], ws=ws)
+    assert csa.device_status(ws) == csa.OK
+    assert int(spare.sum()) == 0
+    lp, ln, kc = to_np(lat_prior), to_np(lat_new), keys.cpu().numpy()
+    for b in range(B):
+        ref = o_fp4.pack(lp[b], 2, "amax", n_blocks=cache.shape[1])
+        ref = o_fp4.pack(ln[b], 2, "amax", first_entry=900, base=ref)
+        np.testing.assert_array_equal(cache[b].cpu().numpy(), ref, err_msg=f"latent {b}")
+        kref = o_fp4.pack(kc[b], 1, "pow2", n_blocks=kcache.shape[1])
+        np.testing.assert_array_equal(kcache[b].cpu().numpy(), kref, err_msg=f"keys {b}")
+        c_ref = o_idx.coarse_keys(o_fp4.dequantize(kref, D, 903), 903)
+        np.testing.assert_array_equal(coarse[b, :c_ref.shape[0]].cpu().numpy(), c_ref)
+
+
+def test_multi_job_pack_bulk_and_overflow(csa):
+    # a bulk job (one thread per group) next to a small one, then a job that overflows its capacity next
+    # to one that fits: the overflow is reported and leaves its cache untouched, the other job is written
+    g = torch.Generator(device=DEV).manual_seed(7)
+    big = torch.randn(1, 2 * 3000, 512, generator=g, device=DEV).to(torch.bfloat16)
+    small = torch.randn(2, 5, 256, generator=g, device=DEV)
+    ws = csa.workspace(256, DEV)
+    c_big = csa.empty_cache(1, 3000, 512, DEV)
+    c_small = csa.empty_cache(2, 5, 256, DEV)
+    csa.pack_fp4_multi([(big, c_big, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=3000)),
+                        (small, c_small, dict(merge=1, scale_rule=csa.SCALE_AMAX, max_entries=5))], ws=ws)
+    assert csa.device_status(ws) == csa.OK
+    np.testing.assert_array_equal(c_big[0].cpu().numpy(), o_fp4.pack(to_np(big)[0], 2, "amax"))
+    sm = small.cpu().numpy()
+    for b in range(2):
+        np.testing.assert_array_equal(c_small[b].cpu().numpy(), o_fp4.pack(sm[b], 1, "amax"))
+
+    over = torch.ones(1, 64, 512, dtype=torch.bfloat16, device=DEV)
+    c_over = csa.empty_cache(1, 64, 512, DEV)
+    first = torch.tensor([40], dtype=torch.int32, device=DEV)      # 40 + 32 > 64
+    c_ok = csa.empty_cache(2, 5, 256, DEV)
+    csa.pack_fp4_multi([(over, c_over, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=64, first_entry=first)),
+                        (small, c_ok, dict(merge=1, scale_rule=csa.SCALE_AMAX, max_entries=5))], ws=ws)
+    assert csa.device_status(ws) == csa.ERR_DEVICE_CHECK
+    assert int(c_over.sum()) == 0
+    np.testing.assert_array_equal(c_ok.cpu().numpy(), c_small.cpu().numpy())
