@@ -45,6 +45,23 @@ def test_dominant_row_and_no_rows():
     assert np.all(out == 0) and lse[0] == -np.inf
 
 
+def test_attend_equals_torch_sdpa_in_fp64():
+    # torch's scaled-dot-product attention (its CPU math path, fp64) is an implementation independent of
+    # the oracle; each row serves as both key and value, and the log-sum-exp comes from torch.logsumexp
+    import torch
+    rng = np.random.default_rng(5)
+    for n, d, h, scale in ((1, 8, 1, 1.0), (37, 64, 4, 0.125), (300, 512, 16, 1 / math.sqrt(512))):
+        rows = rng.standard_normal((n, d)) * 3
+        q = rng.standard_normal((h, d)) * 2
+        out, lse = attention.attend(q, rows, scale)
+        tq = torch.from_numpy(q)[None, None]
+        tr = torch.from_numpy(rows)[None, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(tq, tr, tr, scale=scale)[0, 0].numpy()
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+        ref_lse = torch.logsumexp(torch.from_numpy(q) @ torch.from_numpy(rows).T * scale, dim=-1).numpy()
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-13, atol=1e-13)
+
+
 def test_row_permutation_invariance():
     rng = np.random.default_rng(1)
     rows = rng.standard_normal((50, 32))
