@@ -52,6 +52,7 @@ def _cases():
         "decode_1m_b4_h64_hier2048": synth.DECODE_1M_B4_HIER,
         "chain20_128k_b64_h64": synth.CHAIN_128K_B64,
         "prefill_2048_at_128k_h64": synth.PREFILL_2K_AT_128K,
+        "decode_64k_b32_h64_q4": synth.DECODE_64K_B32_Q4,
     }
 
 

@@ -1,4 +1,4 @@
-"""The five workloads of the method at full size, built and run exactly as bench.py times them (one
+"""The workloads of the method at full size, built and run exactly as bench.py times them (one
 step of the path), checked against the oracle on sampled sequences, positions and layers:
 
   * FP4 cache bytes of sampled entries (latent and index key), bit-exact;
@@ -129,6 +129,10 @@ def test_tiny_decode_4k():
 
 def test_decode_64k_batch32():
     _decode_case("decode_64k_b32_h64", samples=[0, 31])
+
+
+def test_decode_64k_batch32_four_query_positions():
+    _decode_case("decode_64k_b32_h64_q4", samples=[0, 31])
 
 
 def test_decode_1m_hierarchical():
