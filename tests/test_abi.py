@@ -95,3 +95,34 @@ def test_workspace_sizes_are_host_only(lib):
     ia.flags, ia.keep_blocks, ia.max_entries = b.IDX_RELU | b.IDX_HIER, 2048, 1 << 19
     n = lib.csa_index_topk_workspace_size(4, ctypes.byref(ia))
     assert n >= 256 + 4 * 2048 * 4 + 4 * 1024 * 4 + 4 * 32 * 4
+
+
+def test_misaligned_pointers_rejected_before_any_device_call(lib):
+    # pointers that are never dereferenced on the host: an 8-byte offset from a 16-byte boundary
+    from compressed_sparse_attention_merge_b300 import binding as b
+    bad, good = 0x10008, 0x10000
+    pa = b.PackArgs()
+    pa.x, pa.cache, pa.x_dtype, pa.dim, pa.merge, pa.scale_rule = bad, good, b.DTYPE_BF16, 512, 2, b.SCALE_AMAX
+    pa.x_stride_b, pa.x_stride_t, pa.n_tokens, pa.max_entries = 4 * 512, 512, 4, 8
+    assert lib.csa_pack_fp4(1, ctypes.byref(pa), None, 0, None) == b.ERR_ALIGNMENT
+    pa.x, pa.x_stride_t = good, 516                      # a row stride of 1,032 bytes
+    assert lib.csa_pack_fp4(1, ctypes.byref(pa), None, 0, None) == b.ERR_ALIGNMENT
+    pa.x_stride_t = 512
+    jobs = (b.PackArgs * 2)(pa, pa)
+    jobs[1].cache = bad
+    assert lib.csa_pack_fp4_multi(2, (ctypes.c_int64 * 2)(1, 1), jobs, None, 0, None) == b.ERR_ALIGNMENT
+    ia = b.IndexArgs()
+    ia.n_query, ia.heads, ia.dim, ia.top_k, ia.flags, ia.max_entries = 1, 4, 128, 8, b.IDX_RELU, 64
+    ia.q_idx, ia.keys, ia.n_entries, ia.out_idx, ia.keys_stride_b = bad, good, good, good, 8 * 576
+    assert lib.csa_index_topk(1, ctypes.byref(ia), None, 0, None) == b.ERR_ALIGNMENT
+    aa = b.AttnArgs()
+    aa.n_query, aa.heads, aa.top_k, aa.window, aa.scale, aa.max_entries = 1, 64, 8, 0, 0.04, 64
+    aa.q, aa.cache, aa.n_entries, aa.idx, aa.out = good, good, good, good, bad
+    assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_ALIGNMENT
+    aa.out, aa.window, aa.swa, aa.swa_len, aa.swa_rows = good, 128, bad, good, 128
+    assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_ALIGNMENT
+    # and the argument checks that come first
+    aa.swa, aa.window = good, 2048                       # window above 1,024 rows
+    assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
+    aa.window, aa.scale = 128, float("nan")
+    assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
