@@ -126,3 +126,19 @@ def test_misaligned_pointers_rejected_before_any_device_call(lib):
     assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
     aa.window, aa.scale = 128, float("nan")
     assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
+
+
+def test_attention_workspace_size_is_host_only(lib):
+    # without a device the size is the partials layout (no cluster merge), 148 SMs assumed: 4 queries of
+    # 16 cache tiles take 16 cache splits and a window split each, so 17 partials of (o, m, l) per head
+    from compressed_sparse_attention_merge_b300 import binding as b
+    aa = b.AttnArgs()
+    aa.n_query, aa.heads, aa.top_k, aa.window, aa.scale = 1, 64, 256, 128, 0.04
+    aa.max_entries, aa.swa_rows = 1 << 19, 128
+    n = lib.csa_sparse_attn_workspace_size(4, ctypes.byref(aa))
+    assert n % 256 == 0 and n >= 256 + 4 * 17 * 64 * (512 * 4 + 2 * 4)
+    # one cache tile and one window tile: two splits, so partials; no window: one split, no partials
+    aa.top_k = 16
+    assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) >= 256 + 2 * 64 * (512 * 4 + 2 * 4)
+    aa.swa_rows, aa.window = 0, 0
+    assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) == 256
