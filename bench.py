@@ -97,13 +97,19 @@ class DecodeWorkload:
                      coarse_sum=coarse)
         if csa.device_status(ws) != csa.OK:
             raise RuntimeError("cache construction reported a device check")
-        # the newest pair of tokens and the newest index key: re-packing them rewrites the last entry
-        self.new_tokens = d["tokens"][:, T - 2:T].contiguous()
-        self.new_keys = d["keys"][:, E - 1:E].contiguous()
-        self.first = (d["n_entries"] - 1).contiguous()
+        # the step's new tokens and index keys: the tokens of the entries the step's query positions complete
+        # (the newest pair for one query; the pairs of the drafts for causal draft positions); re-packing
+        # them rewrites those entries with the same bytes
+        lo = 2 * ((T - case.n_query) // 2)
+        self.new_tokens = d["tokens"][:, lo:T].contiguous()
+        n_new = (T - lo) // 2
+        self.new_keys = d["keys"][:, E - n_new:E].contiguous()
+        self.first = (d["n_entries"] - n_new).contiguous()
         del d["tokens"], d["keys"]
         self.n_entries = d["n_entries"]
         self.q, self.q_idx, self.swa, self.swa_len = d["q"], d["q_idx"], d["swa"], d["swa_len"]
+        self.causal = case.causal_drafts
+        self.q_pos, self.swa_first_pos = d.get("q_pos"), d.get("swa_first_pos")
         self.caches = [cache] + [cache.clone() for _ in range(replicas - 1)]
         self.kcaches = [kcache] + [kcache.clone() for _ in range(replicas - 1)]
         self.coarses = [coarse] * replicas if coarse is None else [coarse] + [coarse.clone() for _ in
@@ -115,10 +121,15 @@ class DecodeWorkload:
         self.idx = [torch.empty(B, case.n_query, K, dtype=torch.int32, device=device) for _ in range(n_idx_layers)]
         self.out = torch.empty(B, case.n_query, case.heads, 512, dtype=torch.float32, device=device)
         ia = csa.index_args(self.q_idx[0], kcache, self.n_entries, self.idx[0], max_entries=E, top_k=K,
-                            coarse_sum=coarse, keep_blocks=case.hier_keep)
+                            coarse_sum=coarse, keep_blocks=case.hier_keep, q_pos=self.q_pos)
         self.ws_index = csa.workspace(csa.index_topk_workspace_size(B, ia), device)
-        aa = csa.attn_args(self.q[0], cache, self.n_entries, self.idx[0], self.out, max_entries=E,
-                           window=case.window, scale=SCALE, swa=self.swa[0], swa_len=self.swa_len)
+        if self.causal:
+            aa = csa.attn_args(self.q[0], cache, self.n_entries, self.idx[0], self.out, max_entries=E,
+                               window=case.window, scale=SCALE, swa=self.swa[0], swa_first_pos=self.swa_first_pos,
+                               q_pos=self.q_pos)
+        else:
+            aa = csa.attn_args(self.q[0], cache, self.n_entries, self.idx[0], self.out, max_entries=E,
+                               window=case.window, scale=SCALE, swa=self.swa[0], swa_len=self.swa_len)
         self.ws_attn = csa.workspace(csa.sparse_attn_workspace_size(B, aa), device)
         self.ws_pack = ws
         self.queries_per_step = B * case.n_query
@@ -144,12 +155,18 @@ class DecodeWorkload:
                 src = n_idx
                 csa.index_topk(q_idx[n_idx % q_idx.shape[0]], kcache, self.n_entries, self.idx[src],
                                max_entries=self.E, top_k=c.top_k, ws=self.ws_index, coarse_sum=coarse,
-                               keep_blocks=c.hier_keep)
+                               keep_blocks=c.hier_keep, q_pos=self.q_pos)
                 n_idx += 1
             o = out if layer_outs is None else layer_outs[layer]
-            csa.sparse_attn_decode(q[layer], cache, self.n_entries, self.idx[src], o, max_entries=self.E,
-                                   window=c.window, scale=SCALE, ws=self.ws_attn, swa=self.swa[layer],
-                                   swa_len=self.swa_len)
+            if self.causal:
+                # draft positions: each sees the entries and window rows at or before its own token
+                csa.sparse_attn_prefill(q[layer], cache, self.n_entries, self.idx[src], o, q_pos=self.q_pos,
+                                        max_entries=self.E, window=c.window, scale=SCALE, ws=self.ws_attn,
+                                        swa=self.swa[layer], swa_first_pos=self.swa_first_pos)
+            else:
+                csa.sparse_attn_decode(q[layer], cache, self.n_entries, self.idx[src], o, max_entries=self.E,
+                                       window=c.window, scale=SCALE, ws=self.ws_attn, swa=self.swa[layer],
+                                       swa_len=self.swa_len)
         return out
 
     def algorithmic_bytes(self):
@@ -637,15 +654,22 @@ class OracleDecodeSample:
         self.case, self.E = case, E
         tokens = synth.latent_tokens(g, (T, 512), "cpu", case.outlier_frac).float().numpy()
         keys = synth.int_values(g, (1, E, case.idx_dim), "cpu")
-        q_idx = synth.int_values(g, (1, case.n_query, case.idx_heads, case.idx_dim), "cpu")
-        synth.plant_needles(g, keys, q_idx, case.needle_frac)
+        nq = case.distinct_index_queries
+        q_idx = synth.int_values(g, (nq, 1, case.n_query, case.idx_heads, case.idx_dim), "cpu")
+        synth.plant_needles(g, keys, q_idx[0], case.needle_frac)
         self.keys_f = keys[0].numpy()
-        self.q_idx = q_idx[0].numpy()
-        self.q = synth.normal_bf16(g, (case.layers, case.n_query, case.heads, 512), "cpu").float().numpy()
-        self.swa = synth.normal_bf16(g, (case.layers, case.window, 512), "cpu").float().numpy()
+        self.q_idx = q_idx[:, 0].numpy()                 # [distinct queries, Q, H_i, D_i]
+        Q = case.n_query
+        self.q = synth.normal_bf16(g, (case.layers, Q, case.heads, 512), "cpu").float().numpy()
+        swa_rows = case.window + (Q - 1 if case.causal_drafts else 0)
+        self.swa = synth.normal_bf16(g, (case.layers, swa_rows, 512), "cpu").float().numpy()
+        self.q_pos = np.arange(T - Q, T) if case.causal_drafts else None
+        self.swa_first_pos = T - Q - case.window + 1
         nb = -(-E // 8)
-        self.new_tokens = tokens[T - 2:T]
-        self.new_key = self.keys_f[E - 1:E]
+        lo = 2 * ((T - Q) // 2)
+        self.first = E - (T - lo) // 2
+        self.new_tokens = tokens[lo:T]
+        self.new_key = self.keys_f[self.first:E]
         self.cache = o_fp4.pack(tokens, 2, "amax", n_blocks=nb)
         self.kcache = o_fp4.pack(self.keys_f, 1, "pow2", n_blocks=nb)
         self.coarse = None
@@ -659,23 +683,27 @@ class OracleDecodeSample:
         from oracle import fp4 as o_fp4
         from oracle import indexer as o_idx
         c, E = self.case, self.E
-        cache = o_fp4.pack(self.new_tokens, 2, "amax", first_entry=E - 1, base=self.cache)
-        kcache = o_fp4.pack(self.new_key, 1, "pow2", first_entry=E - 1, base=self.kcache)
+        cache = o_fp4.pack(self.new_tokens, 2, "amax", first_entry=self.first, base=self.cache)
+        kcache = o_fp4.pack(self.new_key, 1, "pow2", first_entry=self.first, base=self.kcache)
         keys = o_fp4.dequantize(kcache, c.idx_dim, E)
         entries = o_fp4.dequantize(cache, 512, E)
         outs, idx = [], None
         n_idx = 0
         for layer, mode in enumerate(self.modes):
             if mode != "reuse":
-                q_idx = self.q_idx
+                q_idx = self.q_idx[n_idx % self.q_idx.shape[0]]
                 if c.hier_keep:
                     idx, _ = o_idx.hierarchical_topk(q_idx, keys, E, c.top_k, c.hier_keep, coarse=self.coarse)
                 else:
-                    idx, _ = o_idx.flat_topk(q_idx, keys, E, c.top_k)
+                    idx, _ = o_idx.flat_topk(q_idx, keys, E, c.top_k, q_pos=self.q_pos)
                 n_idx += 1
             for j in range(c.n_query):
-                out, _ = o_attn.decode_attention(self.q[layer, j].astype(np.float64), entries, E, idx[j],
-                                                 self.swa[layer], SCALE)
+                qj = self.q[layer, j].astype(np.float64)
+                if self.q_pos is not None:
+                    out, _ = o_attn.prefill_attention(qj, entries, E, idx[j], self.swa[layer], self.swa_first_pos,
+                                                      int(self.q_pos[j]), c.window, SCALE)
+                else:
+                    out, _ = o_attn.decode_attention(qj, entries, E, idx[j], self.swa[layer], SCALE)
                 outs.append(out)
         return outs
 

@@ -65,7 +65,9 @@ def plant_needles(g, keys, q_idx, frac, block=8):
 @dataclass
 class DecodeCase:
     """A decode workload: batch sequences with tokens[b] tokens each (pair-merged into tokens[b] // 2
-    entries), n_query queries per sequence."""
+    entries), n_query queries per sequence. With `causal_drafts`, the n_query queries of a sequence are
+    the draft positions of a multi-token decode step (speculative verification): the last n_query tokens
+    of the sequence, each seeing only the cache entries and window rows at or before its own position."""
     name: str
     tokens: list
     heads: int = 64
@@ -79,6 +81,7 @@ class DecodeCase:
     hier_keep: int = 0            # > 0: hierarchical selection keeping this many blocks
     layers: int = 1               # > 1: layer chain with per-layer queries and windows
     distinct_index_queries: int = 1
+    causal_drafts: bool = False
     seed: int = 0
     swa_len: list = field(default_factory=list)
 
@@ -98,7 +101,10 @@ class DecodeCase:
 def make_decode(case, device):
     """Returns a dict of tensors on `device`:
     tokens [B, T, 512] bf16, keys [B, E, D_i] f32, n_entries [B] i32, q [L, B, Q, H, 512] bf16,
-    q_idx [Lq, B, Q, H_i, D_i] f32, swa [L, B, W, 512] bf16, swa_len [B] i32."""
+    q_idx [Lq, B, Q, H_i, D_i] f32, swa [L, B, W, 512] bf16, swa_len [B] i32.
+    With causal_drafts (every sequence T tokens long): q_pos [B, Q] i32 = T - Q .. T - 1, and the window
+    buffer holds the W + Q - 1 tokens T - Q - W + 1 .. T - 1: swa [L, B, W + Q - 1, 512] bf16 with
+    swa_first_pos [B] i32 = T - Q - W + 1."""
     g = generator(case.seed, device)
     B, T, E = case.batch, case.max_tokens, case.max_entries
     tokens = torch.empty(B, T, LATENT, dtype=torch.bfloat16, device=device)
@@ -113,10 +119,18 @@ def make_decode(case, device):
     plant_needles(g, keys, q_idx[0], case.needle_frac)
     L = case.layers
     q = normal_bf16(g, (L, B, case.n_query, case.heads, LATENT), device)
-    swa = normal_bf16(g, (L, B, case.window, LATENT), device)
+    Q = case.n_query
+    swa_rows = case.window + (Q - 1 if case.causal_drafts else 0)
+    swa = normal_bf16(g, (L, B, swa_rows, LATENT), device)
     sl = case.swa_len or [case.window] * B
     swa_len = torch.tensor(sl, dtype=torch.int32, device=device)
-    return dict(tokens=tokens, keys=keys, n_entries=n_entries, q=q, q_idx=q_idx, swa=swa, swa_len=swa_len)
+    out = dict(tokens=tokens, keys=keys, n_entries=n_entries, q=q, q_idx=q_idx, swa=swa, swa_len=swa_len)
+    if case.causal_drafts:
+        if any(t != T for t in case.tokens):
+            raise ValueError("causal drafts need sequences of equal length")
+        out["q_pos"] = torch.arange(T - Q, T, dtype=torch.int32, device=device)[None, :].repeat(B, 1).contiguous()
+        out["swa_first_pos"] = torch.full((B,), T - Q - case.window + 1, dtype=torch.int32, device=device)
+    return out
 
 
 @dataclass
@@ -173,6 +187,7 @@ DECODE_1M_B4_HIER = DecodeCase("decode_1m_b4_h64_hier2048", tokens=[1 << 20] * 4
 CHAIN_128K_B64 = DecodeCase("chain20_128k_b64_h64", tokens=[131072] * 64, outlier_frac=0.01, needle_frac=0.01,
                             layers=20, distinct_index_queries=5, seed=20264)
 PREFILL_2K_AT_128K = PrefillCase("prefill_2048_at_128k_h64", context=131072, chunk=2048, seed=20265)
-# Multi-token decode (four query positions per sequence, as in speculative verification) at the 64K shape.
+# Multi-token decode at the 64K shape: four draft positions per sequence (speculative verification), the
+# last four tokens of each sequence, causal among themselves.
 DECODE_64K_B32_Q4 = DecodeCase("decode_64k_b32_h64_q4", tokens=[65536] * 32, n_query=4, outlier_frac=0.01,
-                               needle_frac=0.01, seed=20266)
+                               needle_frac=0.01, causal_drafts=True, seed=20266)

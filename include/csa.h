@@ -288,8 +288,17 @@ csa_status csa_index_topk_static(int64_t batch, const csa_index_args* args, int3
  * at most 2^-25 absolute; larger ones overflow, so |q|, |window| must stay below 65504); products are
  * accumulated in fp32, probabilities are rounded to fp16 for the value product, sums are fp32.
  *
+ * Causal and independent queries. csa_sparse_attn_prefill is the causal multi-query call: query j of
+ * sequence b sits at token q_pos[b][j] and sees only what exists at that position. It serves prefill
+ * chunks and also the draft positions of a multi-token decode step (speculative verification, [card] Key
+ * ideas, "Near-flat decode cost": DSpark speculative decoding): drafts at tokens p .. p + Q - 1 pass
+ * q_pos = p .. p + Q - 1 (to csa_index_topk as well), so draft j sees the entries with 2e + 1 <= p + j,
+ * including an entry completed by an earlier draft, and the window tokens up to p + j.
+ * csa_sparse_attn_decode with n_query > 1 instead runs independent queries that all see the whole cache
+ * prefix (n_entries[b]) and the same window rows.
+ *
  * Arguments:
- *   n_query   queries per sequence (decode may use more than one; all see the whole cache prefix).
+ *   n_query   queries per sequence (decode: independent queries over the whole prefix; prefill: causal).
  *   heads     16, 32, 48 or 64.   scale: softmax scale (1/sqrt(512) for the pages' latent).
  *   q         device bf16 [batch][n_query][heads][512], contiguous, 16-byte aligned.
  *   cache     device packed latent cache (csa_pack_fp4, dim 512), 16-byte aligned; stride in bytes,

@@ -12,6 +12,8 @@ embedding, sink or output projection. Duplicates between the window and the cach
 
 import numpy as np
 
+from .indexer import eligibility
+
 BLOCK = 8
 
 
@@ -47,8 +49,8 @@ def selected_rows(entries, idx, eligible):
 
 def decode_attention(q, entries, n_entries, idx, swa_rows, scale):
     """One decode query: q [H, D]; entries [n_cap, D]; idx [K]; swa_rows [w, D] (already cut to the
-    rows in use). Returns (out, lse)."""
-    el = np.arange(entries.shape[0]) < n_entries
+    rows in use). Every entry below n_entries is eligible. Returns (out, lse)."""
+    el = eligibility(n_entries, entries.shape[0])[0]
     rows = np.concatenate([selected_rows(entries, idx, el), np.asarray(swa_rows, np.float64)], axis=0)
     return attend(q, rows, scale)
 
@@ -61,9 +63,11 @@ def prefill_window(swa, swa_first_pos, p, window):
 
 
 def prefill_attention(q, entries, n_entries, idx, swa, swa_first_pos, p, window, scale):
-    """One prefill query at token position p (causal: entry e is visible iff 2e + 1 <= p)."""
-    e = np.arange(entries.shape[0])
-    el = (e < n_entries) & (2 * e + 1 <= p)
+    """One causal query at token position p: the entries of the listed blocks that the indexer's
+    eligibility rule admits at p (e < n_entries and 2e + 1 <= p), then the window rows of tokens
+    max(p - window + 1, swa_first_pos) .. p. Used for prefill positions and for the draft positions of a
+    multi-token decode step (speculative verification), which follow the same rule."""
+    el = eligibility(n_entries, entries.shape[0], q_pos=[p])[0]
     rows = np.concatenate([selected_rows(entries, idx, el),
                            prefill_window(swa, swa_first_pos, p, window)], axis=0)
     return attend(q, rows, scale)

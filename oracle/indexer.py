@@ -7,14 +7,16 @@ query" (Reindex) or reuse "Top-K indices" (Reuse); selection is over "blocks of 
 hierarchical sparse indexer (up to 2,048 blocks of 8 positions) trims decoder indexing". The pages give
 no score function, tie rule or hierarchy shape; the readings taken here:
 
-  * both operands of the indexer product are FP4: k_e is the dequantised index key shared by all
-    indexer heads, and the query q_h is rounded to the same FP4 format with the POW2 scale rule (one
-    power-of-two scale per 16 elements), q^_h = dequant(quant_pow2(q_h)). For integer-valued queries
-    in [-4, 4] the rounding is the identity.
-  * entry score s_e = sum over heads h (in order 0, 1, ...) of fl32(w_h * r_h), r_h = max(0, q^_h . k_e)
-    with ReLU, plain q^_h . k_e without. The dot products are taken in fp64 and rounded to fp32 (exact
-    for the integer-valued inputs used throughout); the weighted head sum is taken in fp32 in that fixed
-    order, and -0 is made +0.
+  * entry score (the plain definition, `entry_scores`): s_e = sum over heads h (in order 0, 1, ...) of
+    fl32(w_h * r_h), r_h = max(0, q_h . k_e) with ReLU, plain q_h . k_e without, where k_e is the
+    dequantised index key shared by all indexer heads. The dot products are taken in fp64 and rounded to
+    fp32 (exact for the integer-valued inputs used throughout); the weighted head sum is taken in fp32 in
+    that fixed order, and -0 is made +0.
+  * query rounding (a separate step, `round_query`): before scoring, the selection calls
+    (`flat_topk`, `hierarchical_topk`) round every indexer query to the cache's FP4 format with the POW2
+    scale rule (one power-of-two scale per 16 elements), q^_h = dequant(quant_pow2(q_h)), and score with
+    q^_h. This is part of the indexer call's contract, because its product takes both operands in FP4.
+    For integer-valued queries in [-4, 4] the rounding is the identity.
   * a block's score is the maximum over its eligible entries; a block with no eligible entry is not a
     candidate (score -inf here).
   * Top-K: the min(K, #candidates) candidates with the largest scores, ties to the lower block id,
@@ -34,9 +36,16 @@ SUPER = 64
 ENTRIES_PER_SUPER = BLOCK * SUPER
 
 
+def round_query(q):
+    """The indexer query as the selection calls score it: every group of 16 elements rounded to FP4 with
+    the POW2 scale rule and dequantised (float32, same shape). The identity on integers in [-4, 4]."""
+    return fp4.round_trip(np.asarray(q, dtype=np.float32), "pow2")
+
+
 def entry_scores(q, keys, head_w=None, relu=True):
-    """q: [Q, H, D] (rounded to FP4 here), keys: [n_e, D] dequantised. Returns float32 [Q, n_e]."""
-    q = fp4.round_trip(np.asarray(q, dtype=np.float32), "pow2").astype(np.float64)
+    """q: [Q, H, D] indexer queries, keys: [n_e, D] dequantised keys. Returns float32 [Q, n_e]:
+    s_e = sum_h fl32(w_h * max(0, q_h . k_e)) in head order (no rounding of q here)."""
+    q = np.asarray(q, dtype=np.float64)
     keys = np.asarray(keys, dtype=np.float64)
     nq, nh, d = q.shape
     w = np.ones(nh, np.float32) if head_w is None else np.asarray(head_w, np.float32)
@@ -82,8 +91,9 @@ def topk(scores, k):
 
 def flat_topk(q, keys, n_entries, k, head_w=None, relu=True, q_pos=None):
     """Index + Top-K for one sequence. q: [Q, H, D]; keys: dequantised [n_cap, D] (entries beyond
-    n_entries are ignored). Returns (idx int32 [Q, k], block scores float32 [Q, n_b])."""
-    s = entry_scores(q, keys, head_w, relu)
+    n_entries are ignored). The queries are rounded by `round_query` first. Returns (idx int32 [Q, k],
+    block scores float32 [Q, n_b])."""
+    s = entry_scores(round_query(q), keys, head_w, relu)
     el = eligibility(n_entries, keys.shape[0], q_pos)
     el = np.broadcast_to(el, s.shape)
     S = block_scores(s, el)
@@ -108,7 +118,9 @@ def coarse_keys(keys, n_entries):
 
 def hierarchical_topk(q, keys, n_entries, k, keep_blocks, head_w=None, relu=True, coarse=None):
     """Two-stage selection for one sequence (decode). q: [Q, H, D]; keys: dequantised [n_cap, D].
-    Returns (idx int32 [Q, k], kept super-block ids int32 [Q, keep_blocks // 64])."""
+    The queries are rounded by `round_query` first, for both stages. Returns (idx int32 [Q, k], kept
+    super-block ids int32 [Q, keep_blocks // 64])."""
+    q = round_query(q)
     if coarse is None:
         coarse = coarse_keys(keys, n_entries)
     n_super = coarse.shape[0]

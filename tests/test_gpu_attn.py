@@ -76,9 +76,9 @@ def test_decode_matches_oracle(csa, heads, top_k, batch):
         assert_lse_close(lse[b, 0], ref_lse, f"seq {b}")
 
 
-def test_multi_token_decode_end_to_end(csa):
-    # speculative verification: four query positions per sequence in one decode call, each with its own
-    # indexer query and Top-K; in decode every query sees the whole cache prefix and the same window
+def test_multi_query_decode_end_to_end(csa):
+    # several independent queries per sequence in one decode call, each with its own indexer query and
+    # Top-K; in decode every query sees the whole cache prefix and the same window
     g = torch.Generator(device=DEV).manual_seed(31)
     tokens, B, Q, H, K, W, HI, DI = [1800, 640], 2, 4, 64, 32, 128, 4, 128
     T = max(tokens)
@@ -108,6 +108,58 @@ def test_multi_token_decode_end_to_end(csa):
                                                    sf[b, :int(swa_len[b])], SCALE)
             assert_attn_close(out[b, j], ref, f"seq {b} query {j}")
             assert_lse_close(lse[b, j], ref_lse, f"seq {b} query {j}")
+
+
+@pytest.mark.parametrize("prefix", [1001, 640])
+def test_speculative_drafts_are_causal(csa, prefix):
+    # multi-token decode for speculative verification: four draft tokens at positions p .. p + 3 follow a
+    # prefix of p tokens. Draft j sees the cache entries with 2e + 1 <= p + j and the window tokens
+    # p + j - 127 .. p + j. The drafts complete new entries (the pair (p - 1, p) for odd p, then the later
+    # pairs), each visible from its completing draft on. All drafts share one indexer query and the new
+    # entries' index keys are needles for it, so every draft's Top-K picks them as soon as they are visible.
+    g = torch.Generator(device=DEV).manual_seed(41 + prefix)
+    B, Q, H, K, W, HI, DI = 2, 4, 64, 24, 128, 4, 128
+    T = prefix + Q
+    E = T // 2
+    x = _latents(g, B, T)
+    keys = torch.randint(-4, 5, (B, E, DI), generator=g, device=DEV).float()
+    q_idx = torch.randint(-4, 5, (B, 1, HI, DI), generator=g, device=DEV).float().expand(B, Q, HI, DI).contiguous()
+    new_first = (prefix - 1) // 2                                   # first entry a draft completes or joins
+    for b in range(B):
+        keys[b, new_first:E] = 4.0 * torch.sign(q_idx[b, 0, 0])
+    q = torch.randn(B, Q, H, 512, generator=g, device=DEV).to(torch.bfloat16)
+    first_tok = prefix - W + 1                                      # window buffer: tokens p - 127 .. p + 3
+    swa = torch.randn(B, W + Q - 1, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa_first_pos = torch.full((B,), first_tok, dtype=torch.int32, device=DEV)
+    q_pos = torch.arange(prefix, prefix + Q, dtype=torch.int32, device=DEV)[None].repeat(B, 1).contiguous()
+    ws = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T] * B, E, 512, 2, csa.SCALE_AMAX, ws)
+    kcache = gpu_pack_sequences(csa, keys, [E] * B, E, DI, 1, csa.SCALE_POW2, ws)
+    n_entries = torch.full((B,), E, dtype=torch.int32, device=DEV)
+    idx, _ = gpu_index(csa, q_idx, kcache, n_entries, E, K, q_pos=q_pos)
+    out, lse = gpu_prefill_attn(csa, q, cache, n_entries, idx, q_pos, swa, swa_first_pos, E, W)
+    idx, out, lse = idx.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy()
+    xf, qf, sf, kf, qi = to_np(x), to_np(q), to_np(swa), keys.cpu().numpy(), q_idx.cpu().numpy()
+    pos = np.arange(prefix, prefix + Q)
+    for b in range(B):
+        deq_k = o_fp4.dequantize(o_fp4.pack(kf[b], 1, "pow2", n_blocks=-(-E // 8)), DI, E)
+        ref_idx, _ = o_idx.flat_topk(qi[b], deq_k, E, K, q_pos=pos)
+        np.testing.assert_array_equal(idx[b], ref_idx, err_msg=f"seq {b}")
+        entries = o_fp4.dequantize(o_fp4.pack(xf[b], 2, "amax", n_blocks=-(-E // 8)), 512, E)
+        seen = []
+        for j in range(Q):
+            p = int(pos[j])
+            ref, ref_lse = o_attn.prefill_attention(qf[b, j].astype(np.float64), entries, E, ref_idx[j], sf[b],
+                                                    first_tok, p, W, SCALE)
+            assert_attn_close(out[b, j], ref, f"seq {b} draft {j}")
+            assert_lse_close(lse[b, j], ref_lse, f"seq {b} draft {j}")
+            listed = {8 * int(blk) + s for blk in ref_idx[j] if blk >= 0 for s in range(8)}
+            seen.append({e for e in range(new_first, E) if e in listed and 2 * e + 1 <= p})
+        # each new entry enters exactly at the draft whose token completes it
+        for j in range(Q):
+            want = {e for e in range(new_first, E) if 2 * e + 1 <= prefix + j}
+            assert seen[j] == want, (j, seen[j], want)
+        assert seen[0] != seen[Q - 1]
 
 
 def test_split_and_unsplit_agree(csa):

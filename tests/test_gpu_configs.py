@@ -99,6 +99,7 @@ def _decode_case(name, samples, layer_checks=None):
         _check_pack(w.caches[0][b].cpu().numpy(), tok, keys_np, w.kcaches[0][b].cpu().numpy(), probe, c.idx_dim)
         sources, n_idx, src = [], 0, 0
         ref_idx = {}
+        q_pos = d["q_pos"][b].cpu().numpy() if c.causal_drafts else None
         for layer, mode in enumerate(w.modes):
             if mode != "reuse":
                 src = n_idx
@@ -106,18 +107,23 @@ def _decode_case(name, samples, layer_checks=None):
                 if c.hier_keep:
                     ref, _ = o_idx.hierarchical_topk(q_idx, keys, E, c.top_k, c.hier_keep)
                 else:
-                    ref, _ = o_idx.flat_topk(q_idx, keys, E, c.top_k)
+                    ref, _ = o_idx.flat_topk(q_idx, keys, E, c.top_k, q_pos=q_pos)
                 np.testing.assert_array_equal(w.idx[src][b].cpu().numpy(), ref, err_msg=f"{name} seq {b} layer {layer}")
                 ref_idx[src] = ref
                 n_idx += 1
             sources.append(src)
         for layer in (layer_checks if layer_checks is not None else range(L)):
             ref = ref_idx[sources[layer]]
-            swa = to_np(d["swa"][layer, b])[:int(d["swa_len"][b])]
             for j in range(c.n_query):
-                rows = _oracle_rows(tok, ref[j], lambda e: e < E)
+                if q_pos is None:
+                    swa = to_np(d["swa"][layer, b])[:int(d["swa_len"][b])].astype(np.float64)
+                    rows = _oracle_rows(tok, ref[j], lambda e: e < E)
+                else:
+                    p = int(q_pos[j])
+                    swa = o_attn.prefill_window(to_np(d["swa"][layer, b]), int(d["swa_first_pos"][b]), p, c.window)
+                    rows = _oracle_rows(tok, ref[j], lambda e, p=p: e < E and 2 * e + 1 <= p)
                 q = to_np(d["q"][layer, b, j]).astype(np.float64)
-                want, _ = o_attn.attend(q, np.concatenate([rows, swa.astype(np.float64)]), SCALE)
+                want, _ = o_attn.attend(q, np.concatenate([rows, swa]), SCALE)
                 assert_attn_close(outs[layer][b, j, :c.heads].cpu().numpy(), want[:c.heads],
                                   f"{name} seq {b} layer {layer} ({w.modes[layer]})")
     return w

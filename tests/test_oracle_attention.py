@@ -124,3 +124,55 @@ def test_chain_modes_and_reuse_indices():
     for layer, mode in enumerate(m):
         np.testing.assert_array_equal(per_layer_idx[layer], per_layer_idx[src[layer]])
     assert not np.array_equal(per_layer_idx[0], per_layer_idx[4])     # Reindex really rescored
+
+
+def _row_count(lse):
+    # with a zero query every logit is 0, so lse = log(number of rows)
+    return int(round(math.exp(lse)))
+
+
+def test_prefill_rows_counted_by_hand():
+    # a hand-built cache of 20 entries (3 blocks, all listed) whose entry e holds the value e + 1 in every
+    # column, and a window buffer that starts at token 0 with rows of zeros. At position p the entries
+    # with 2e + 1 <= p are 0 .. floor((p - 1) / 2), i.e. floor((p + 1) / 2) of them, and the window has
+    # the p + 1 rows of tokens 0 .. p (p < 128):
+    #   p:        0  1  2  15  16  17
+    #   entries:  0  1  1   8   8   9
+    #   window:   1  2  3  16  17  18
+    #   rows:     1  3  4  24  25  27
+    entries = (np.arange(20, dtype=np.float64)[:, None] + 1) * np.ones((1, 16))
+    swa = np.zeros((200, 16))
+    q = np.zeros((2, 16))
+    idx = np.array([2, 0, 1, -1])
+    for p, n_ent, n_rows in [(0, 0, 1), (1, 1, 3), (2, 1, 4), (15, 8, 24), (16, 8, 25), (17, 9, 27)]:
+        out, lse = attention.prefill_attention(q, entries, 20, idx, swa, 0, p, 128, 0.5)
+        assert _row_count(lse[0]) == n_rows and _row_count(lse[1]) == n_rows
+        # the output is the mean of the rows: sum of (e + 1) over the visible entries / rows
+        want = sum(e + 1 for e in range(n_ent)) / n_rows
+        np.testing.assert_allclose(out, want, rtol=0, atol=1e-14)
+    # n_entries still bounds the visible entries at late positions, and the window keeps its last 128
+    out, lse = attention.prefill_attention(q, entries, 13, idx, swa, 0, 199, 128, 0.5)
+    assert _row_count(lse[0]) == 13 + 128
+    np.testing.assert_allclose(out, sum(range(1, 14)) / (13 + 128), rtol=0, atol=1e-14)
+
+
+def test_prefill_equals_decode_once_every_entry_is_visible():
+    # at a position p >= 2 n_entries - 1 every entry below n_entries is visible, so the causal query equals
+    # the decode query over the same blocks with the window rows of tokens p - 127 .. p
+    rng = np.random.default_rng(4)
+    entries, n_e = _cache(rng, 2 * 90)                # 90 entries, 12 blocks (the last ragged)
+    swa = rng.standard_normal((1000, 512))
+    first = 10                                        # token of window row 0; p - 127 >= first below
+    q = rng.standard_normal((4, 512))
+    idx = np.array([11, 3, -1, 7, 0, 5])
+    scale = 1 / math.sqrt(512)
+    for p in (2 * n_e - 1, 2 * n_e + 40, 900):
+        a, la = attention.prefill_attention(q, entries, n_e, idx, swa, first, p, 128, scale)
+        b, lb = attention.decode_attention(q, entries, n_e, idx, swa[p - 127 - first:p + 1 - first], scale)
+        np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(la, lb, rtol=1e-13)
+    # one position earlier the last entry (2e + 1 = 2 n_e - 1 > p) drops out, so the two differ
+    p = 2 * n_e - 2
+    a, _ = attention.prefill_attention(q, entries, n_e, np.array([11]), swa, first, p, 128, scale)
+    b, _ = attention.decode_attention(q, entries, n_e, np.array([11]), swa[p - 127 - first:p + 1 - first], scale)
+    assert not np.allclose(a, b)

@@ -123,7 +123,7 @@ def test_query_rounding_is_identity_on_small_integers():
             g = rng.integers(-a, a + 1, 16).astype(np.float32)
             if a:
                 g[rng.integers(16)] = a * (1 if rng.random() < 0.5 else -1)
-            np.testing.assert_array_equal(fp4.round_trip(g[None], "pow2")[0], g)
+            np.testing.assert_array_equal(indexer.round_query(g[None, None])[0, 0], g)
 
 
 def test_query_rounding_hand_worked():
@@ -131,16 +131,42 @@ def test_query_rounding_hand_worked():
     # amax 7 -> 7/6 -> scale 2; 7/2 = 3.5 lies halfway between 3 (code 5) and 4 (code 6) -> 4 -> 8
     # amax 0.3 -> 0.05 -> scale 2^-4; 0.3 / 2^-4 = 4.8 -> nearest grid value 4 -> 0.25
     for v, want in [(5.0, 4.0), (-5.0, -4.0), (7.0, 8.0), (0.3, 0.25)]:
-        g = np.zeros(16, np.float32)
-        g[3] = v
-        out = fp4.round_trip(g[None], "pow2")[0]
-        assert out[3] == want and np.all(np.delete(out, 3) == 0)
+        g = np.zeros((1, 1, 32), np.float32)
+        g[0, 0, 3] = v
+        g[0, 0, 16 + 5] = 1.0                         # the second group of 16 has its own scale
+        out = indexer.round_query(g)[0, 0]
+        assert out[3] == want and out[21] == 1.0
+        assert np.all(np.delete(out, [3, 21]) == 0)
 
 
-def test_scores_use_the_rounded_query():
-    # a query of 5s scores exactly like a query of 4s (its FP4 rounding), against integer brute force
+def test_entry_scores_do_not_round_the_query():
+    # the plain score definition takes the query as given: 5s score as 5s (integer brute force)
     rng = np.random.default_rng(12)
     k = rng.integers(-4, 5, (64, 64))
     q = np.full((1, 1, 64), 5.0, np.float32)
     got = indexer.entry_scores(q, k)
-    np.testing.assert_array_equal(got.astype(np.int64), _int_scores(np.full((1, 1, 64), 4), k, [1], True))
+    np.testing.assert_array_equal(got.astype(np.int64), _int_scores(np.full((1, 1, 64), 5), k, [1], True))
+
+
+def test_selection_scores_the_rounded_query():
+    # flat and hierarchical selection score with round_query(q): a query of 5s is rounded to 4s, so it
+    # selects exactly like a query of 4s and its block scores equal the integer brute force of the 4s
+    # query (a selection that skipped the rounding would report scores 5/4 as large)
+    rng = np.random.default_rng(13)
+    n_e = 512 * 3
+    k = rng.integers(-4, 5, (n_e, 64)).astype(np.float32)
+    q5 = np.full((1, 1, 64), 5.0, np.float32)
+    q4 = np.full((1, 1, 64), 4.0, np.float32)
+    a5, S5 = indexer.flat_topk(q5, k, n_e, 24)
+    a4, S4 = indexer.flat_topk(q4, k, n_e, 24)
+    np.testing.assert_array_equal(a5, a4)
+    np.testing.assert_array_equal(S5, S4)
+    h5, kept5 = indexer.hierarchical_topk(q5, k, n_e, 24, keep_blocks=128)
+    h4, kept4 = indexer.hierarchical_topk(q4, k, n_e, 24, keep_blocks=128)
+    np.testing.assert_array_equal(h5, h4)
+    np.testing.assert_array_equal(kept5, kept4)
+    # with rounding, block scores are the integer brute force of the rounded query
+    s_int = _int_scores(np.full((1, 1, 64), 4), k.astype(np.int64), [1], True)
+    el = np.arange(n_e) < n_e
+    want = np.where(el, s_int[0], np.iinfo(np.int64).min).reshape(-1, 8).max(axis=1)
+    np.testing.assert_array_equal(S5[0].astype(np.int64), want)
