@@ -6,39 +6,36 @@
 // (sliding window of 128), and "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" (card),
 // Key ideas ("Every layer keeps its own query and sliding-window KV").
 //
-// Design. A CTA owns one query (all heads) and some 128-row tiles of its row list: a range of cache
-// tiles (16 selected blocks each) and/or the window tiles. Because one latent row c is both key and
-// value, both products are taken with the rows as the 128-wide M side and the heads as N:
+// Design. A CTA owns one query (all heads) and some 128-row tiles of its row list: the window tiles first,
+// then a range of cache tiles (16 selected blocks each). Because one latent row c is both key and value,
+// both products are taken with the rows as the 128-wide M side and the heads as N:
 //   S^T [rows x heads]  = C [rows x 512] . Q^T                   (logits)
 //   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (values)
 // S and O accumulate in tensor memory; the row sums l are added up by one warp from the fp16
 // probabilities in shared memory (the same values the tensor core multiplies).
-//   Cache tiles: the gather warp copies the 16 raw FP4 blocks (36 KB) with cp.async.bulk into one of three
-//   raw stages. Two groups of four warps dequantise every tile: group A writes the logits operand
-//   straight into tensor memory (thread = row, 64-column panels, a four-panel ring); group B
-//   writes the values operand into a two-slot shared-memory ring of [128 latent x 64 row] units in the
-//   128-byte-swizzled MN-major layout.
-//   Window tiles: a tensor-map copy (TMA, 128-byte swizzle) lands the 128 bf16 rows in panel layout over
-//   the raw and ring areas; they are converted to fp16 in place and serve both products.
-// Pipelining: S is double-buffered in tensor memory and the logits and the values have separate issuing
-// threads, so that the logits of tile t+1 run while the softmax of tile t works; the softmax of tile t+1
-// computes its probabilities while the values of tile t run and writes them once those have read P. A
-// third raw stage lets the copy of tile t+2 start while tile t's values operand is still being built.
+//   Every tile is dequantised once. Eight converter warps (thread = tensor-memory lane = tile row) read
+//   their row's FP4 codes and scales straight from global memory (the gather warp prefetches the CTA's
+//   blocks into L2 at the start, and each converter loads the next tile's bytes into registers while it
+//   works on the current one), convert a 64-column panel to fp16 and write it twice: into the logits
+//   operand ring in tensor memory, and into the values buffer in shared memory, a whole tile of C^T in the
+//   128-byte-swizzled MN-major layout, recycled per 128-latent chunk as the value products finish with it.
+//   Window tiles come first: their bf16 rows are copied by tensor map straight into the values buffer and
+//   converted to fp16 in place by the same threads, which also write the logits panels.
+// Pipelining: S and P are double-buffered, so the logits and softmax of tile t+1 run while the values of
+// tile t are multiplied; the converters of tile t+1 wait only for the value products of the chunk they
+// overwrite. Both products are issued by whole warps (one elected lane issues).
 //
-// Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-7 group A, 8-11 group B, 12 gather,
-// 13 logits MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps,
-// per head, a reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in
-// log2 units), so the probabilities stay below 2^8 and the accumulators are rescaled rarely. Splits write
-// unnormalised partials (o, m, l); the combine kernel merges them in split order. When the splits of a
-// unit form one thread-block cluster, each CTA stages its (o, m, l) in its own shared memory instead and
-// CTA r merges latent columns [512 r / S, 512 (r + 1) / S) of every split, in split order, through
-// distributed shared memory.
+// Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-11 converters (warp 4 + 4 h + s covers
+// subpartition s, panels of parity h), 12 gather (window copies, L2 prefetch, block-id checks), 13 logits
+// MMA issue and tensor-memory allocation, 14 values MMA issue, 15 row sums. The softmax keeps, per head, a
+// reference maximum that is raised only when a tile's maximum exceeds it by more than 8 (in log2 units),
+// so the probabilities stay below 2^8 and the accumulators are rescaled rarely. When a query's rows are
+// split over several CTAs, every split writes its unnormalised partial (o, m, l) and the combine kernel
+// merges them in split order (measured faster than merging inside the kernel across a thread-block
+// cluster, through distributed shared memory or through L2 copies).
 #include <cuda.h>
 
 #include <cstring>
-#include <map>
-#include <mutex>
-#include <utility>
 
 #include "csa_internal.cuh"
 #include "tc.cuh"
@@ -50,82 +47,62 @@ constexpr int kRows = 128;                                 // rows per tile: M o
 constexpr int kTileBlocks = kRows / kBlockEntries;         // 16 cache blocks per tile
 constexpr int kHeadsPad = 64;                              // N of both products (heads, zero-padded)
 constexpr int kPanels = kLatent / 64;                      // 8 panels of 64 latent columns
+constexpr int kChunks = kLatent / 128;                     // 4 chunks of 128 latent columns (M of a value product)
 constexpr int kLatBlk = block_bytes(kLatent);              // 2304
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack = 8.0f;                      // log2 headroom before the reference max moves
 constexpr float kMaxProb = 256.0f;                         // 2^kRescaleSlack
 
 // shared-memory map (bytes); the operand regions start on 1024-byte boundaries
-constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB
+constexpr int kQPanel = kHeadsPad * 128;                   // 8 KB: [64 heads x 64 latent] fp16
 constexpr int kQOff = 0;                                   // queries: 8 K-major panels, 64 KB
-constexpr int kPBytes = kRows * 128;                       // the P^T buffer: 16 KB
-constexpr int kPOff = kQOff + kPanels * kQPanel;           // 65,536
-// Staged blocks are padded by 16 bytes so that the same byte of a row falls in a different bank in each
-// of 8 consecutive blocks.
-constexpr int kRawBlk = kLatBlk + 16;                      // 2,320
-constexpr int kRawStage = kTileBlocks * kRawBlk;           // 37,120
-constexpr int kRawStages = 3;
-constexpr int kRawOff = kPOff + kPBytes;                   // 81,920
-constexpr int kUnitBytes = 2 * 64 * 128;                   // values unit: 128 latent columns x 64 rows
-constexpr int kRing = 2;
-constexpr int kRingOff = (kRawOff + kRawStages * kRawStage + 1023) & ~1023;   // 193,536
-constexpr int kPanelBytes = kRows * 128;                   // 16 KB: one 64-column panel of a whole tile
-constexpr int kWinOff = kRawOff;                           // window tile: 8 panels over the raw and ring areas
-constexpr int kWinEnd = kWinOff + kPanels * kPanelBytes;   // 212,992: window panels, or the staged o
-constexpr int kRingEnd = kRingOff + kRing * kUnitBytes;    // 226,304
-constexpr int kBarOff = kRingEnd > kWinEnd ? kRingEnd : kWinEnd;
-constexpr int kNumBars = 36;
+constexpr int kHalfBytes = kRows * 128;                    // 16 KB: 64 latent columns of a whole tile
+constexpr int kChunkBytes = 2 * kHalfBytes;                // 32 KB: 128 latent columns of a whole tile
+constexpr int kVOff = kQOff + kPanels * kQPanel;           // 65,536: the values buffer, 4 chunks
+constexpr int kPBytes = kRows * 128;                       // 16 KB: one P^T buffer
+constexpr int kPOff = kVOff + kChunks * kChunkBytes;       // 196,608: two P^T buffers
+constexpr int kBarOff = kPOff + 2 * kPBytes;               // 229,376
+constexpr int kNumBars = 32;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
-constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort, int have (cluster staging)
+constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort, int have
 constexpr int kMOff = kFlagOff + 16;                       // float m[64]
 constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[2][64]: per P buffer
 constexpr int kRedOff = kAlphaOff + 2 * 64 * 4;            // float red[4][64]
 constexpr int kLsumOff = kRedOff + 4 * 64 * 4;             // float lsum[64]: final row sums
 constexpr int kSmemBytes = kLsumOff + 64 * 4;
-static_assert(kWinOff % 1024 == 0 && kRingOff % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
+static_assert(kVOff % 1024 == 0 && kPOff % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 constexpr int kTRing = 4;
 enum Bar {
-  RAW_FULL = 0,                         // raw stages: gather -> both dequantisation groups
-  RAW_EMPTY = RAW_FULL + kRawStages,
-  TRING_FULL = RAW_EMPTY + kRawStages,  // logits operand panels in tensor memory: group A <-> logits issuer
+  TRING_FULL = 0,                       // logits operand panels in tensor memory: converters <-> logits issuer
   TRING_EMPTY = TRING_FULL + kTRing,
-  RING_FULL = TRING_EMPTY + kTRing,     // values operand units in shared memory: group B <-> values issuer
-  RING_EMPTY = RING_FULL + kRing,
-  S_FULL = RING_EMPTY + kRing,          // logits buffers: logits issuer <-> softmax
+  V_FULL = TRING_EMPTY + kTRing,        // values buffer chunks: converters <-> values issuer
+  V_EMPTY = V_FULL + kChunks,
+  S_FULL = V_EMPTY + kChunks,           // logits buffers: logits issuer <-> softmax
   S_EMPTY = S_FULL + 2,
-  P_FULL = S_EMPTY + 2,                 // the P buffer, per tile parity: softmax <-> values issuer, row sums
-  PV_DONE = P_FULL + 2,
-  WIN_FULL = PV_DONE + 2, WIN_CVT, WIN_EMPTY,
+  P_FULL = S_EMPTY + 2,                 // P buffers: softmax <-> values issuer and row sums
+  P_EMPTY = P_FULL + 2,
+  WIN_FULL = P_EMPTY + 2,               // a window tile's rows have landed in the values buffer
   FIN_L, FIN_V, NUM_BARS
 };
 
 static_assert(NUM_BARS <= kNumBars, "barrier area");
 
-constexpr int kGrpA0 = 4, kGrpB0 = 8;          // first warps of the two dequantisation groups
-constexpr int kDqWarps = 8;
+constexpr int kConv0 = 4, kConvWarps = 8;      // converter warps 4..11
 constexpr int kGatherWarp = 12, kLogitsWarp = 13, kValuesWarp = 14, kSumWarp = 15;
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColA = 128, kColO = 256;   // S: two buffers of 64 columns; A: four panels
 
-constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
+constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major (tensor memory), Q K-major
 constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
-
-// Row of a cache tile held by tensor-memory lane l (0..127) in the logits. The 8 lanes of a quarter warp
-// take 8 different blocks and 8 different slots, so that their raw loads and their P^T stores fall in
-// different banks.
-__device__ __forceinline__ int lane_row(int l) {
-  const int h = l >> 3, i = l & 7;
-  const int blk = i + 8 * (h & 1), slot = (i + (h >> 1)) & 7;
-  return 8 * blk + slot;
-}
 
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          uint32_t* hdr, uint32_t detail) {
   const uint32_t a = smem_addr(bar);
+  if (mbar_test_wait(a, parity)) return true;      // the common case: the phase completed already
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 7u) == 7u && *abort_flag) return false;
@@ -133,6 +110,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   *abort_flag = 1;
   report(hdr, CSA_ERR_TIMEOUT, KID_ATTN, detail);
   return false;
+}
+
+// The same wait taken by a whole warp; the result is the same on every lane.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* hdr, uint32_t detail) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, hdr, detail));
 }
 
 // Bounded wait that ignores the abort flag (draining copies that must land before the CTA exits).
@@ -151,14 +134,6 @@ __device__ __forceinline__ bool all_softmax(bool v) {
   return r != 0;
 }
 
-// Tensor-map copy of a [1 x 128 x 64] box (batch, row, latent column) into shared memory.
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
-  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-               " [%0], [%1, {%2, %3, %4}], [%5];"
-               :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
-                  "r"(smem_addr(bar)) : "memory");
-}
-
 // OR of v over the 128 softmax threads (named barrier 1).
 __device__ __forceinline__ bool any_softmax(bool v) {
   uint32_t r;
@@ -167,12 +142,20 @@ __device__ __forceinline__ bool any_softmax(bool v) {
   return r != 0;
 }
 
+// Tensor-map copy of a [1 x 128 x 64] box (batch, row, latent column) into shared memory.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+                  "r"(smem_addr(bar)) : "memory");
+}
+
 struct UnitCtx {
   int64_t unit, b, n_e, n_b, nb_cap, pos, swa_first, swa_len;
   bool prefill;
 };
 
-// Block id of row r of cache tile t as stored in the index list (-1 past the list).
+// Block id of row r of the CTA's global cache tile t as stored in the index list (-1 past the list).
 __device__ __forceinline__ int cache_id(const AttnParams& p, const UnitCtx& u, int t, int r) {
   const int slot = t * kTileBlocks + (r >> 3);
   return slot < p.top_k ? __ldg(p.idx + u.unit * p.top_k + slot) : -1;
@@ -214,29 +197,16 @@ __device__ __forceinline__ bool window_row(const AttnParams& p, const UnitCtx& u
   return declared;
 }
 
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
-  return v;
-}
-
-// Every thread of every CTA of the cluster arrives; shared-memory writes before it are visible after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Copies window tile tw (128 rows x 512 bf16) into the values buffer: eight [128 x 64] boxes, box k going
+// to chunk k / 2, half k % 2, in the buffer's 128-byte-swizzled layout.
+__device__ __forceinline__ void copy_window_tile(const AttnParams& p, const UnitCtx& u, int tw, uint8_t* smem,
+                                                 const CUtensorMap* map, uint64_t* bar) {
+  const int64_t y0 = window_row0(p, u, tw);
+  const int y = (int)(y0 < -(int64_t)kRows ? -kRows : (y0 > p.swa_rows ? p.swa_rows : y0));
+  mbar_arrive_expect_tx(bar, kChunks * kChunkBytes);
+#pragma unroll
+  for (int k = 0; k < 2 * kChunks; ++k)
+    tma_load_3d(smem + kVOff + k * kHalfBytes, map, 64 * k, y, (int)u.b, bar);
 }
 
 // 2^x by the hardware approximation (relative error near 2^-22; subnormal results flush to zero). The
@@ -264,6 +234,21 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* h) {
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
 }
 
+// One 64-column panel of a cache row: 32 code bytes (a, b) and 4 scale bytes (sc) -> 32 f16x2, exact.
+// Zero codes and a zero scale (rows that are not attended) give exact zeros.
+__device__ __forceinline__ void dequant_panel(const uint4& a, const uint4& b, uint32_t sc, uint32_t* h) {
+  e2m1x8_to_f16x8(a.x, h);      e2m1x8_to_f16x8(a.y, h + 4);
+  e2m1x8_to_f16x8(a.z, h + 8);  e2m1x8_to_f16x8(a.w, h + 12);
+  e2m1x8_to_f16x8(b.x, h + 16); e2m1x8_to_f16x8(b.y, h + 20);
+  e2m1x8_to_f16x8(b.z, h + 24); e2m1x8_to_f16x8(b.w, h + 28);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t s2 = e4m3_to_f16x2_bcast((sc >> (8 * g)) & 0xFFu);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[8 * g + k] = hmul2_u32(h[8 * g + k], s2);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap swa_map) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -274,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   float* msh = reinterpret_cast<float*>(smem + kMOff);
   float* alpha = reinterpret_cast<float*>(smem + kAlphaOff);
   float* red = reinterpret_cast<float*>(smem + kRedOff);
+  float* lsh = reinterpret_cast<float*>(smem + kLsumOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x;
@@ -294,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   u.swa_first = (u.prefill && p.window > 0) ? (int64_t)__ldg(p.swa_first_pos + u.b) : 0;
   u.swa_len = (!u.prefill && p.window > 0) ? (int64_t)__ldg(p.swa_len + u.b) : 0;
 
-  // this CTA's tiles: cache tiles [c0, c1), then nw window tiles
+  // this CTA's tiles: nw window tiles first, then cache tiles [c0, c1)
   const bool win_only = p.win_split && split == p.splits - 1;
   int c0 = 0, c1 = 0;
   if (!win_only) {
@@ -309,45 +295,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   }
   const int nw = (win_only || (!p.win_split && split == p.cache_splits - 1)) ? p.n_wt : 0;
   const int n_cache = c1 - c0;
-  const int n_tiles = n_cache + nw;
+  const int n_tiles = nw + n_cache;
   const uint8_t* seq = p.cache + u.b * p.cache_stride_b;
 
   // ---------------- setup ----------------
-  // The barriers first, so that the gather warp can start the first tiles' copies while the other warps
-  // load and convert the queries.
   if (warp == kLogitsWarp) tc::alloc(tmem_ptr, kTmemCols);
   if (tid == 0) {
     for (int i = 0; i < kTRing; ++i) {
       mbar_init(&bars[TRING_FULL + i], 4);
       mbar_init(&bars[TRING_EMPTY + i], 1);
     }
-    for (int i = 0; i < kRawStages; ++i) {
-      mbar_init(&bars[RAW_FULL + i], 1);
-      mbar_init(&bars[RAW_EMPTY + i], kDqWarps);
+    for (int i = 0; i < kChunks; ++i) {
+      mbar_init(&bars[V_FULL + i], kConvWarps);
+      mbar_init(&bars[V_EMPTY + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[S_FULL + i], 1);
       mbar_init(&bars[S_EMPTY + i], 4);
       mbar_init(&bars[P_FULL + i], 4);
-      mbar_init(&bars[PV_DONE + i], 2);        // the values' commit and the row-sum warp
-    }
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(&bars[RING_FULL + i], 4);
-      mbar_init(&bars[RING_EMPTY + i], 1);
+      mbar_init(&bars[P_EMPTY + i], 2);        // the values' commit and the row-sum warp
     }
     mbar_init(&bars[WIN_FULL], 1);
-    mbar_init(&bars[WIN_CVT], kDqWarps);
-    mbar_init(&bars[WIN_EMPTY], 1);
     mbar_init(&bars[FIN_L], 1);
     mbar_init(&bars[FIN_V], 1);
     fence_mbar_init();
-    flag[0] = 0; flag[1] = 0; *abort_flag = 0;
+    flag[0] = 0; flag[1] = 0; *abort_flag = 0; flag[3] = 0;
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tmem_ptr;
   const uint32_t s_base = smem_addr(smem);
+
+  // The first window tile lands in the values buffer while the queries are loaded.
+  if (warp == kGatherWarp && lane == 0 && nw > 0) copy_window_tile(p, u, 0, smem, &swa_map, &bars[WIN_FULL]);
+
+  // Converters: their rows' block ids of the first two cache tiles and the raw bytes of the first two panels,
+  // so that these loads are in flight during the query load. The raw bytes of the next two panels a
+  // converter handles form a queue in registers (q0 is the next panel to convert): each step converts q0,
+  // shifts the queue and loads the panel two steps ahead into q1 (the same tile's chunk c + 2, or the next
+  // cache tile's chunk c - 2).
+  const bool is_conv = warp >= kConv0 && warp < kConv0 + kConvWarps;
+  const int sp = warp & 3;                         // tensor-memory subpartition of this warp
+  const int hp = (warp - kConv0) >> 2;             // converters: panel parity
+  const int row = sp * 32 + lane;                  // converters and softmax: tile row = tensor-memory lane
+  uint4 qa0 = make_uint4(0, 0, 0, 0), qa1 = qa0, qb0 = qa0, qb1 = qa0;
+  uint32_t qs0 = 0, qs1 = 0;
+  int64_t id_cur = -1, id_nxt = -1;
+  bool v_cur = false;
+  if (is_conv) {
+    id_cur = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
+    id_nxt = n_cache > 1 ? cache_id(p, u, c0 + 1, row) : -1;
+    v_cur = n_cache > 0 && cache_ok(u, id_cur, row);
+    if (v_cur) {
+      const uint8_t* e = seq + id_cur * kLatBlk + (row & 7) * 256 + hp * 32;
+      const uint32_t* sc = reinterpret_cast<const uint32_t*>(seq + id_cur * kLatBlk + 2048 + (row & 7) * 32 + hp * 4);
+      qa0 = __ldg(reinterpret_cast<const uint4*>(e));       qb0 = __ldg(reinterpret_cast<const uint4*>(e + 16));
+      qa1 = __ldg(reinterpret_cast<const uint4*>(e + 64));  qb1 = __ldg(reinterpret_cast<const uint4*>(e + 80));
+      qs0 = __ldg(sc); qs1 = __ldg(sc + 2);
+    }
+  }
+
   if (warp != kGatherWarp) {
     // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero. Every load of a
     // thread is issued before the first conversion.
@@ -379,331 +387,179 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   }
 
   if (warp == kGatherWarp) {
-    // ---------------- gather: cache blocks (cp.async.bulk), window rows (tensor map) ----------------
-    if (lane == 0) {
-      int issued = 0, win_issued = 0;
-      for (int it = 0; it < n_cache; ++it) {
-        const int stage = it % kRawStages;
-        if (it >= kRawStages && !wait_bar(&bars[RAW_EMPTY + stage], (it / kRawStages - 1) & 1, abort_flag, p.hdr, 1)) break;
-        const int t = c0 + it;
-        uint8_t* dst = smem + kRawOff + stage * kRawStage;
-        uint32_t bytes = 0;
-        int64_t ids[kTileBlocks];
-#pragma unroll
-        for (int j = 0; j < kTileBlocks; ++j) {
-          const int slot = t * kTileBlocks + j;
-          int64_t id = -1;
-          if (slot < p.top_k) id = __ldg(p.idx + u.unit * p.top_k + slot);
-          if (id < -1 || id >= u.nb_cap) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
-          ids[j] = (id >= 0 && id < u.n_b) ? id : -1;
-          if (ids[j] >= 0) bytes += kLatBlk;
-        }
-        if (bytes) {
-          mbar_arrive_expect_tx(&bars[RAW_FULL + stage], bytes);
-#pragma unroll
-          for (int j = 0; j < kTileBlocks; ++j)
-            if (ids[j] >= 0) bulk_g2s(dst + j * kRawBlk, seq + ids[j] * kLatBlk, kLatBlk, &bars[RAW_FULL + stage]);
-        } else {
-          mbar_arrive(&bars[RAW_FULL + stage]);
-        }
-        ++issued;
-        if (it == kRawStages - 1 || (it < kRawStages - 1 && it == n_cache - 1)) {
-          // the later tiles of this CTA go to L2 now, so that refilling a raw stage costs an L2 read
-          for (int t2 = c0 + kRawStages; t2 < c1; ++t2) {
-            for (int j = 0; j < kTileBlocks; ++j) {
-              const int slot = t2 * kTileBlocks + j;
-              const int64_t id = slot < p.top_k ? (int64_t)__ldg(p.idx + u.unit * p.top_k + slot) : -1;
-              if (id >= 0 && id < u.n_b) prefetch_l2(seq + id * kLatBlk, kLatBlk);
-            }
-          }
-          // and the window rows, read once the cache tiles are done (boxes inside the buffer only)
-          for (int tw = 0; tw < nw; ++tw) {
-            const int64_t y0 = window_row0(p, u, tw);
-            if (y0 < 0 || y0 + kRows > p.swa_rows) continue;
-            for (int pp = 0; pp < kPanels; ++pp) prefetch_l2_3d(&swa_map, pp * 64, (int)y0, (int)u.b);
-          }
-        }
+    // ---------------- gather: block-id checks, L2 prefetch, later window tiles ----------------
+    // the blocks of cache tile k go to L2 when the converters start tile k - 2 (the first three at once), so
+    // that the early tiles are not queued behind the later ones; lanes 0-15 take one block each
+    for (int k = 0; k < n_cache; ++k) {
+      const int t = nw + k - 3;           // the tile whose first values chunk paces this prefetch
+      if (t >= 0 && !wait_bar_warp(&bars[V_FULL], t & 1, abort_flag, p.hdr, 16)) break;
+      const int slot = (c0 + k) * kTileBlocks + lane;
+      if (lane < kTileBlocks && slot < p.top_k) {
+        const int64_t id = __ldg(p.idx + u.unit * p.top_k + slot);
+        if (id < -1 || id >= u.nb_cap) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
+        if (id >= 0 && id < u.n_b) prefetch_l2(seq + id * kLatBlk, kLatBlk);
       }
-      if (issued == n_cache) {
-        for (int tw = 0; tw < nw; ++tw) {
-          // the window panels overlay the raw and ring buffers: wait until every earlier product is done
-          const int need = tw + (n_cache > 0 ? 1 : 0);
-          if (need > 0 && !wait_bar(&bars[WIN_EMPTY], (need - 1) & 1, abort_flag, p.hdr, 9)) break;
-          const int64_t y0 = window_row0(p, u, tw);
-          const int y = (int)(y0 < -(int64_t)kRows ? -kRows : (y0 > p.swa_rows ? p.swa_rows : y0));
-          mbar_arrive_expect_tx(&bars[WIN_FULL], kPanels * kPanelBytes);
-#pragma unroll
-          for (int pp = 0; pp < kPanels; ++pp)
-            tma_load_3d(smem + kWinOff + pp * kPanelBytes, &swa_map, pp * 64, y, (int)u.b, &bars[WIN_FULL]);
-          ++win_issued;
-        }
+    }
+    if (lane == 0) {
+      for (int tw = 1; tw < nw; ++tw) {
+        const int64_t y0 = window_row0(p, u, tw);
+        if (y0 < 0 || y0 + kRows > p.swa_rows) continue;
+        for (int pp = 0; pp < kPanels; ++pp) prefetch_l2_3d(&swa_map, pp * 64, (int)y0, (int)u.b);
+      }
+      int copied = nw > 0 ? 1 : 0;
+      for (int tw = 1; tw < nw; ++tw) {
+        // the values buffer holds the previous tile until its value products are done
+        bool ok = true;
+        for (int c = 0; c < kChunks && ok; ++c) ok = wait_bar(&bars[V_EMPTY + c], (tw - 1) & 1, abort_flag, p.hdr, 9);
+        if (!ok) break;
+        copy_window_tile(p, u, tw, smem, &swa_map, &bars[WIN_FULL]);
+        ++copied;
       }
       // no copy into this CTA's shared memory may still be in flight when it exits
-      for (int it = issued - kRawStages < 0 ? 0 : issued - kRawStages; it < issued; ++it)
-        drain_bar(&bars[RAW_FULL + it % kRawStages], (it / kRawStages) & 1);
-      if (win_issued > 0) drain_bar(&bars[WIN_FULL], (win_issued - 1) & 1);
+      if (copied > 0) drain_bar(&bars[WIN_FULL], (copied - 1) & 1);
     }
-  } else if (warp >= kGrpA0 && warp < kGrpA0 + kDqWarps) {
-    // ---------------- dequantisation ----------------
+  } else if (is_conv) {
+    // ---------------- converters: one 64-column panel of every chunk of every tile ----------------
+    const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
     bool stop = false;
-    if (warp < kGrpB0) {
-      // group A: one warp per tensor-memory subpartition, thread = lane = row lane_row(lane); writes the 8
-      // logits panels of a tile into the two-slot tensor-memory ring
-      const int sp = warp & 3;
-      const int l = sp * 32 + lane;
-      const int r = lane_row(l);
-      const int blk = r >> 3, sl = r & 7;
-      const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
-      uint32_t t_k = 0;
-      int id_next = n_cache > 0 ? cache_id(p, u, c0, r) : -1;
-      for (int it = 0; it < n_cache && !stop; ++it) {
-        const int stage = it % kRawStages;
-        const bool vr = cache_ok(u, id_next, r);
-        if (it + 1 < n_cache) id_next = cache_id(p, u, c0 + it + 1, r);
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it / kRawStages) & 1, abort_flag, p.hdr, 2))) break;
-        const uint8_t* raw = smem + kRawOff + stage * kRawStage + blk * kRawBlk;
-        const uint8_t* codes = raw + sl * 256;
-        const uint8_t* scales = raw + 2048 + sl * 32;
-        // Panels go out in pairs: both are converted and stored, then one wait covers both stores. The
-        // next panel's raw words are loaded while the current one is converted.
-        uint4 wa = *reinterpret_cast<const uint4*>(codes);
-        uint4 wb = *reinterpret_cast<const uint4*>(codes + 16);
-        uint32_t ws = vr ? *reinterpret_cast<const uint32_t*>(scales) : 0u;
-#pragma unroll 1
-        for (int pp = 0; pp < kPanels && !stop; pp += 2) {
-          uint32_t slots[2];
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            uint32_t h[32];
-            e2m1x8_to_f16x8(wa.x, h);      e2m1x8_to_f16x8(wa.y, h + 4);
-            e2m1x8_to_f16x8(wa.z, h + 8);  e2m1x8_to_f16x8(wa.w, h + 12);
-            e2m1x8_to_f16x8(wb.x, h + 16); e2m1x8_to_f16x8(wb.y, h + 20);
-            e2m1x8_to_f16x8(wb.z, h + 24); e2m1x8_to_f16x8(wb.w, h + 28);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              // a zero scale (rows that are not attended) gives exact zeros: E2M1 has no infinities or NaNs
-              const uint32_t sc = e4m3_to_f16x2_bcast((ws >> (8 * g)) & 0xFFu);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) h[8 * g + k] = hmul2_u32(h[8 * g + k], sc);
-            }
-            const int nx = pp + q + 1;
-            if (nx < kPanels) {
-              wa = *reinterpret_cast<const uint4*>(codes + nx * 32);
-              wb = *reinterpret_cast<const uint4*>(codes + nx * 32 + 16);
-              ws = vr ? *reinterpret_cast<const uint32_t*>(scales + nx * 4) : 0u;
-            }
-            const uint32_t slot = t_k % kTRing, n = t_k / kTRing;
-            if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
-              stop = true;
-              break;
-            }
-            tc::fence_after();
-            tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
-            slots[q] = slot;
-            ++t_k;
-          }
-          if (stop) break;
-          tc::wait_st();
-          tc::fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars[TRING_FULL + slots[0]]);
-            mbar_arrive(&bars[TRING_FULL + slots[1]]);
-          }
-        }
-        tc::wait_st();      // no tensor-memory store may be in flight if the loop gave up
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
-      }
-    } else {
-      // group B: writes the values operand as 8 units of [128 latent columns x 64 rows] per tile (unit
-      // 2 ch + rh: latent chunk ch, rows 64 rh ..). Per unit a thread converts 8 chunks of 8 elements:
-      // column chunk c of block 8 rh + 2 bsel + (k & 1), slot 2 wl + ((k >> 1) & 1), panel half k >> 2.
-      const int wl = warp - kGrpB0;
-      const int c = lane & 7, bsel = lane >> 3;
-      uint32_t u_k = 0;
-      // the 4 blocks of this thread's rows in a tile: 8 rh + 2 bsel + j (rh, j in {0, 1})
-      int ids_next[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) ids_next[q] = n_cache > 0 ? cache_id(p, u, c0, 8 * (8 * (q >> 1) + 2 * bsel + (q & 1))) : -1;
-      for (int it = 0; it < n_cache && !stop; ++it) {
-        const int stage = it % kRawStages;
-        uint32_t vmask = 0;       // bit 4 rh + (k & 3): row attended
-#pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = 8 * (8 * rh + 2 * bsel + (k & 1)) + 2 * wl + (k >> 1);
-            if (cache_ok(u, ids_next[2 * rh + (k & 1)], r)) vmask |= 1u << (4 * rh + k);
-          }
-        }
-        if (it + 1 < n_cache) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) ids_next[q] = cache_id(p, u, c0 + it + 1, 8 * (8 * (q >> 1) + 2 * bsel + (q & 1)));
-        }
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[RAW_FULL + stage], (it / kRawStages) & 1, abort_flag, p.hdr, 2))) break;
-        const uint8_t* raw = smem + kRawOff + stage * kRawStage;
-        for (int unit = 0; unit < 8; ++unit) {
-          const int ch = unit >> 1, rh = unit & 1;
-          // the unit's raw words first: one load latency per unit instead of one per item
-          uint32_t cw[8], sb[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int bl = 2 * bsel + (k & 1), sl = 2 * wl + ((k >> 1) & 1), pnl = 2 * ch + (k >> 2);
-            const uint8_t* src = raw + (8 * rh + bl) * kRawBlk;
-            cw[k] = *reinterpret_cast<const uint32_t*>(src + sl * 256 + pnl * 32 + c * 4);
-            sb[k] = src[2048 + sl * 32 + pnl * 4 + (c >> 1)];
-          }
-          const uint32_t slot = u_k % kRing, n = u_k / kRing;
-          if (n > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[RING_EMPTY + slot], (n - 1) & 1u, abort_flag, p.hdr, 3))) {
-            stop = true;
-            break;
-          }
-          uint8_t* dst = smem + kRingOff + slot * kUnitBytes;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int bl = 2 * bsel + (k & 1), sl = 2 * wl + ((k >> 1) & 1), ph = k >> 2;
-            const uint32_t sc = (vmask >> (4 * rh + (k & 3))) & 1u ? e4m3_to_f16x2_bcast(sb[k]) : 0u;
-            uint32_t hh[4];
-            e2m1x8_to_f16x8(cw[k], hh);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) hh[e] = hmul2_u32(hh[e], sc);
-            const int rl = 8 * bl + sl;
-            *reinterpret_cast<uint4*>(dst + ph * (kUnitBytes / 2) + rl * 128 + ((c ^ sl) << 4)) =
-                make_uint4(hh[0], hh[1], hh[2], hh[3]);
-          }
-          tc::fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[RING_FULL + slot]);
-          ++u_k;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[RAW_EMPTY + stage]);
-      }
-    }
-    const int dt = tid - kGrpA0 * 32;          // 0..255 over both groups
-    for (int tw = 0; tw < nw && !stop; ++tw) {
-      if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], tw & 1, abort_flag, p.hdr, 10))) break;
-      // in place: bf16 -> fp16, rows that are not attended -> 0; this thread's rows are (k & 3) * 32 + dt / 8
-      bool vr[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
+    for (int it = 0; it < n_tiles && !stop; ++it) {
+      const bool win = it < nw;
+      const int k = it - nw;                       // cache tile index within this CTA
+      bool vr = v_cur;
+      if (win) {
         bool oob;
-        vr[k] = window_row(p, u, tw, k * 32 + (dt >> 3), &oob);
-        if (oob && (dt & 7) == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
+        vr = window_row(p, u, it, row, &oob);
+        if (oob && hp == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], it & 1, abort_flag, p.hdr, 10))) break;
       }
-#pragma unroll 4
-      for (int k = 0; k < 32; ++k) {
-        const int q = k * 256 + dt;
-        const int pp = q >> 10, row = (q & 1023) >> 3, cc = q & 7;
-        uint4* a = reinterpret_cast<uint4*>(smem + kWinOff + pp * kPanelBytes + row * 128 + ((cc ^ (row & 7)) << 4));
-        const uint4 x = *a;
-        const bool v = vr[k & 3];
-        *a = v ? make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w)) : make_uint4(0, 0, 0, 0);
+      const bool v_next = !win && k + 1 < n_cache && cache_ok(u, id_nxt, row);
+#pragma unroll 1
+      for (int c = 0; c < kChunks; ++c) {
+        const int pnl = 2 * c + hp;
+        uint8_t* vrow = smem + kVOff + c * kChunkBytes + hp * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
+        uint32_t h[32];
+        if (win) {
+          // bf16 -> fp16 of this row's 64 columns, in place; rows that are not attended become zero
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vrow + ((j ^ (row & 7)) << 4));
+            h[4 * j] = vr ? bf2_to_h2(x.x) : 0u; h[4 * j + 1] = vr ? bf2_to_h2(x.y) : 0u;
+            h[4 * j + 2] = vr ? bf2_to_h2(x.z) : 0u; h[4 * j + 3] = vr ? bf2_to_h2(x.w) : 0u;
+          }
+        } else {
+          dequant_panel(qa0, qb0, qs0, h);
+          // shift the queue; the panel two steps ahead enters at the back
+          qa0 = qa1; qb0 = qb1; qs0 = qs1;
+          qa1 = make_uint4(0, 0, 0, 0); qb1 = qa1; qs1 = 0u;
+          const bool same = c + 2 < kChunks;
+          if (same ? vr : v_next) {
+            const int64_t id2 = same ? id_cur : id_nxt;
+            const int pnl2 = same ? pnl + 4 : pnl - 4;
+            const uint8_t* e = seq + id2 * kLatBlk + (row & 7) * 256 + pnl2 * 32;
+            qa1 = __ldg(reinterpret_cast<const uint4*>(e));
+            qb1 = __ldg(reinterpret_cast<const uint4*>(e + 16));
+            qs1 = __ldg(reinterpret_cast<const uint32_t*>(seq + id2 * kLatBlk + 2048 + (row & 7) * 32 + pnl2 * 4));
+          }
+        }
+        // logits operand: panel pnl of tile it goes to ring slot pnl & 3 (use 2 it + c / 2 of that slot)
+        const uint32_t slot = pnl & 3, use = 2u * it + (c >> 1);
+        if (use > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (use - 1) & 1u, abort_flag, p.hdr, 3))) {
+          stop = true;
+          break;
+        }
+        tc::fence_after();
+        tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
+        // values operand while the tensor-memory store completes: the chunk must have been consumed by the
+        // previous tile's value products (a window tile's chunks were, before its copy was issued)
+        bool freed = win || it == 0 || __all_sync(0xffffffffu, wait_bar(&bars[V_EMPTY + c], (it - 1) & 1, abort_flag, p.hdr, 6));
+        if (freed) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(vrow + ((j ^ (row & 7)) << 4)) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        }
+        tc::wait_st();          // no tensor-memory store may be in flight past this point, even when giving up
+        tc::fence_before();
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (!freed) {
+          stop = true;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive(&bars[TRING_FULL + slot]);
+          mbar_arrive(&bars[V_FULL + c]);
+        }
       }
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[WIN_CVT]);
+      if (!win) {
+        id_cur = id_nxt;
+        v_cur = v_next;
+        id_nxt = k + 2 < n_cache ? cache_id(p, u, c0 + k + 2, row) : -1;
+      }
     }
   } else if (warp == kLogitsWarp) {
     // ---------------- logits MMA issue: S^T(t) = C . Q^T into S buffer t & 1 ----------------
-    if (lane == 0) {
-      const uint32_t q_addr = s_base + kQOff, win_addr = s_base + kWinOff;
-      uint32_t t_k = 0;
-      bool ok = true;
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        const int sb = it & 1;
-        const bool cache = it < n_cache;
-        if (it >= 2 && !wait_bar(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4)) { ok = false; break; }
-        if (!cache && !wait_bar(&bars[WIN_CVT], (it - n_cache) & 1, abort_flag, p.hdr, 11)) { ok = false; break; }
-        const uint32_t d = tbase + kColS + 64 * sb;
-        for (int pp = 0; pp < kPanels; ++pp) {
-          uint32_t slot = 0;
-          if (cache) {
-            slot = t_k % kTRing;
-            if (!wait_bar(&bars[TRING_FULL + slot], (t_k / kTRing) & 1u, abort_flag, p.hdr, 4)) { ok = false; break; }
-          }
-          tc::fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bq = tc::smem_desc(q_addr + pp * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
-            if (cache) {
-              tc::mma_f16_ts(d, tbase + kColA + 32 * slot + 8 * ks, bq, kIdescS, (pp | ks) != 0);
-            } else {
-              const uint64_t a = tc::smem_desc(win_addr + pp * kPanelBytes + ks * 32, 16, 1024, tc::kSwizzle128B);
-              tc::mma_f16(d, a, bq, kIdescS, (pp | ks) != 0);
-            }
-          }
-          if (cache) { tc::commit(&bars[TRING_EMPTY + slot]); ++t_k; }
-        }
-        if (ok) tc::commit(&bars[S_FULL + sb]);
-      }
-      // every MMA issued must be complete before the tensor memory is released
-      tc::commit(&bars[FIN_L]);
-      drain_bar(&bars[FIN_L], 0);
-    }
-  } else if (warp == kValuesWarp) {
-    // ---------------- values MMA issue: O^T += C^T . P^T and l += ones . P^T ----------------
-    if (lane == 0) {
-      const uint32_t ring_addr = s_base + kRingOff, win_addr = s_base + kWinOff;
-      uint32_t u_k = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int pb = it & 1;
-        const bool cache = it < n_cache;
-        const uint32_t p_addr = s_base + kPOff;
-        if (!wait_bar(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 5)) break;
+    const uint32_t q_addr = s_base + kQOff;
+    bool ok = true;
+    for (int it = 0; it < n_tiles && ok; ++it) {
+      const int sb = it & 1;
+      if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4)) break;
+      const uint32_t d = tbase + kColS + 64 * sb;
+      for (int pnl = 0; pnl < kPanels; ++pnl) {
+        const uint32_t slot = pnl & 3, use = 2u * it + (pnl >> 2);
+        if (!wait_bar_warp(&bars[TRING_FULL + slot], use & 1u, abort_flag, p.hdr, 4)) { ok = false; break; }
         tc::fence_after();
-        bool ok = true;
-        if (cache) {
-          for (int unit = 0; unit < 8; ++unit) {
-            const int ch = unit >> 1, rh = unit & 1;
-            const uint32_t slot = u_k % kRing;
-            if (!wait_bar(&bars[RING_FULL + slot], (u_k / kRing) & 1u, abort_flag, p.hdr, 6)) { ok = false; break; }
-            tc::fence_after();
-            const uint32_t c_addr = ring_addr + slot * kUnitBytes;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t a = tc::smem_desc(c_addr + j * 2048, kUnitBytes / 2, 1024, tc::kSwizzle128B);
-              const uint64_t bp = tc::smem_desc(p_addr + rh * (kPBytes / 2) + j * 2048, 8192, 1024, tc::kSwizzle128B);
-              tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || rh > 0 || j > 0) ? 1u : 0u);
-            }
-            tc::commit(&bars[RING_EMPTY + slot]);
-            ++u_k;
-          }
-        } else {
-          for (int ch = 0; ch < 4; ++ch) {
-            const uint32_t c_addr = win_addr + 2 * ch * kPanelBytes;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint64_t a = tc::smem_desc(c_addr + j * 2048, kPanelBytes, 1024, tc::kSwizzle128B);
-              const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
-              tc::mma_f16(tbase + kColO + 64 * ch, a, bp, kIdescPV, (it > 0 || j > 0) ? 1u : 0u);
-            }
-          }
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bq = tc::smem_desc(q_addr + pnl * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
+          tc::mma_f16_ts_warp(d, tbase + kColA + 32 * slot + 8 * ks, bq, kIdescS, (pnl | ks) != 0);
         }
-        if (!ok) break;
-        tc::commit(&bars[PV_DONE + pb]);
-        // the window panels overlay the raw and ring buffers: free them after the last cache tile and
-        // after every window tile
-        if ((cache && it == n_cache - 1 && nw > 0) || !cache) tc::commit(&bars[WIN_EMPTY]);
+        tc::commit_warp(&bars[TRING_EMPTY + slot]);
       }
-      tc::commit(&bars[FIN_V]);
-      drain_bar(&bars[FIN_V], 0);
+      if (ok) tc::commit_warp(&bars[S_FULL + sb]);
     }
+    // every MMA issued must be complete before the tensor memory is released
+    tc::commit_warp(&bars[FIN_L]);
+    drain_bar(&bars[FIN_L], 0);
+    __syncwarp();
+  } else if (warp == kValuesWarp) {
+    // ---------------- values MMA issue: O^T += C^T . P^T, chunk by chunk ----------------
+    const uint32_t v_addr = s_base + kVOff;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int pb = it & 1;
+      const uint32_t p_addr = s_base + kPOff + pb * kPBytes;
+      if (!wait_bar_warp(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 5)) break;
+      tc::fence_after();
+      bool ok = true;
+      for (int c = 0; c < kChunks; ++c) {
+        if (!wait_bar_warp(&bars[V_FULL + c], it & 1, abort_flag, p.hdr, 6)) { ok = false; break; }
+        tc::fence_after();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint64_t a = tc::smem_desc(v_addr + c * kChunkBytes + j * 2048, kHalfBytes, 1024, tc::kSwizzle128B);
+          const uint64_t bp = tc::smem_desc(p_addr + j * 2048, 8192, 1024, tc::kSwizzle128B);
+          tc::mma_f16_warp(tbase + kColO + 64 * c, a, bp, kIdescPV, (it > 0 || j > 0) ? 1u : 0u);
+        }
+        tc::commit_warp(&bars[V_EMPTY + c]);
+      }
+      if (!ok) break;
+      tc::commit_warp(&bars[P_EMPTY + pb]);
+    }
+    tc::commit_warp(&bars[FIN_V]);
+    drain_bar(&bars[FIN_V], 0);
+    __syncwarp();
   } else if (warp == kSumWarp) {
     // ---------------- row sums: l += sum over the tile's rows of P (lane = heads 2 lane, 2 lane + 1) ----
     float l0 = 0.0f, l1 = 0.0f;
     const int h0 = 2 * lane;
-    bool ok = true;
-    for (int it = 0; it < n_tiles && ok; ++it) {
+    for (int it = 0; it < n_tiles; ++it) {
       const int pb = it & 1;
-      if (!__all_sync(0xffffffffu, wait_bar(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 13))) { ok = false; break; }
+      if (!wait_bar_warp(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 13)) break;
       if (flag[pb]) {
         // the softmax raised the reference maxima for this tile: rescale like O
         l0 *= alpha[64 * pb + h0];
         l1 *= alpha[64 * pb + h0 + 1];
       }
-      const uint8_t* pbuf = smem + kPOff + (lane & 3) * 4;
+      const uint8_t* pbuf = smem + kPOff + pb * kPBytes + (lane & 3) * 4;
       float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
 #pragma unroll 8
       for (int r = 0; r < kRows; r += 2) {
@@ -716,77 +572,96 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       l0 += a0 + b0;
       l1 += a1 + b1;
       if (it == n_tiles - 1) {
-        float* lsum = reinterpret_cast<float*>(smem + kLsumOff);
-        lsum[h0] = l0;
-        lsum[h0 + 1] = l1;
+        lsh[h0] = l0;
+        lsh[h0 + 1] = l1;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[PV_DONE + pb]);
+      if (lane == 0) mbar_arrive(&bars[P_EMPTY + pb]);
     }
   } else {
     // ---------------- softmax (warps 0-3, thread = tile row) ----------------
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     bool ok = true;
-    int id_next = n_cache > 0 ? cache_id(p, u, c0, lane_row(tid)) : -1;
+    int64_t sid_nxt = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
     for (int it = 0; it < n_tiles; ++it) {
       const int sb = it & 1;
-      // tensor-memory lane tid holds row lane_row(tid) of a cache tile (row tid of a window tile)
-      const int row = it < n_cache ? lane_row(tid) : tid;
       bool valid;
-      if (it < n_cache) {
-        valid = cache_ok(u, id_next, row);
-        if (it + 1 < n_cache) id_next = cache_id(p, u, c0 + it + 1, row);
-      } else {
+      if (it < nw) {
         bool oob;
-        valid = window_row(p, u, it - n_cache, row, &oob);
+        valid = window_row(p, u, it, row, &oob);
+      } else {
+        valid = cache_ok(u, sid_nxt, row);
+        sid_nxt = it - nw + 1 < n_cache ? cache_id(p, u, c0 + it - nw + 1, row) : -1;
       }
-      const uint32_t s_col = kColS + 64 * sb;
       if (!all_softmax(wait_bar(&bars[S_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
-      // alpha[sb] and flag[sb] were last read by the row sums of tile it - 2
-      if (it >= 2) {
-        if (!all_softmax(wait_bar(&bars[PV_DONE + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) { ok = false; break; }
-      }
       tc::fence_after();
+      // P buffer sb, alpha[sb] and flag[sb] were last read by the value products and row sums of tile it - 2
+      if (it >= 2 && !all_softmax(wait_bar(&bars[P_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) {
+        ok = false;
+        break;
+      }
       float* al = alpha + 64 * sb;
-      // Fast path: probabilities against the current reference maxima; the full path runs only when a
-      // probability would exceed 2^8 (a maximum moved by more than the slack, or none was set yet).
-      uint32_t w[32];
+      const uint32_t s_col = tbase + lane_base + kColS + 64 * sb;
+      uint8_t* prow = smem + kPOff + sb * kPBytes + row * 128;
+      // Fast path: probabilities against the current reference maxima, 32 heads at a time, written to row
+      // `row` of P (fp16, MN-major: 64 heads contiguous, 128-byte swizzle); the full path runs, and rewrites
+      // the row, only when a probability would exceed 2^8 (a maximum moved by more than the slack, or none
+      // was set yet).
       bool over = false;
-      {
-        uint32_t sr[64];
-        tc::ld_32x64(tbase + lane_base + s_col, sr);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t sr[32];
+        tc::ld_32x32(s_col + 32 * half, sr);
         tc::wait_ld();
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 ma = *reinterpret_cast<const float4*>(msh + 8 * c);
-          const float4 mb = *reinterpret_cast<const float4*>(msh + 8 * c + 4);
+        for (int c = 0; c < 4; ++c) {
+          const float4 ma = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c);
+          const float4 mb = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c + 4);
           const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+          uint32_t w[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int h = 8 * c + 2 * k;
             const float p0 = valid ? ex2(__uint_as_float(sr[h]) * p.scale_log2 - mm[2 * k]) : 0.0f;
             const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * p.scale_log2 - mm[2 * k + 1]) : 0.0f;
             over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
-            w[4 * c + k] = f2_to_h2(p0, p1);
+            w[k] = f2_to_h2(p0, p1);
           }
+          const int pc = 4 * half + c;
+          *reinterpret_cast<uint4*>(prow + ((pc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       const bool full = any_softmax(over);
+      if (!full) {
+        // S buffer sb has been read for the last time: the logits of tile it + 2 may overwrite it
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
+      }
       if (tid == 0) flag[sb] = 0;
       if (full) {
+        // per-head maximum over the warp's 32 rows, 32 heads at a time, by a transposing reduction: at
+        // the step with offset o a lane keeps the half of its values selected by (lane & o) and takes the
+        // maximum with its partner's copy of that half, so after five steps lane l holds head 32 half + l
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-          // per-head maximum over the warp's 32 rows (one warp reduction per head)
           uint32_t sr[32];
-          tc::ld_32x32(tbase + lane_base + s_col + 32 * half, sr);
+          tc::ld_32x32(s_col + 32 * half, sr);
           tc::wait_ld();
+          float v[32];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const float v = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
-            float mx;
-            asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx) : "f"(v));
-            red[warp * 64 + 32 * half + h] = mx;
+          for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+#pragma unroll
+          for (int n = 16, o = 16; n >= 1; n >>= 1, o >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+              const float keep = up ? v[n + i] : v[i];
+              const float give = up ? v[i] : v[n + i];
+              v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, o));
+            }
           }
+          red[warp * 64 + 32 * half + lane] = v[0];
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (tid < 64) {
@@ -800,10 +675,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (flag[sb]) {
-          // the previous tile's value products must be complete before O is rescaled (the ones before it
-          // completed earlier: the values are issued in tile order); the row-sum warp rescales l itself
+          // every value product before this tile must be complete before O is rescaled (the ones of tile
+          // it - 1 complete last: the values are issued in tile order); the row-sum warp rescales l itself
           if (it > 0) {
-            if (!all_softmax(wait_bar(&bars[PV_DONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 12))) {
+            if (!all_softmax(wait_bar(&bars[P_EMPTY + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 12))) {
               ok = false;
               break;
             }
@@ -822,36 +697,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           }
           tc::wait_st();
         }
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t sr[32];
-          tc::ld_32x32(tbase + lane_base + s_col + 32 * half, sr);
+          tc::ld_32x32(s_col + 32 * half, sr);
           tc::wait_ld();
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float m0 = msh[32 * half + 2 * k], m1 = msh[32 * half + 2 * k + 1];
-            const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[2 * k]) * p.scale_log2 - m0);
-            const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[2 * k + 1]) * p.scale_log2 - m1);
-            w[16 * half + k] = f2_to_h2(p0, p1);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int h = 8 * c + 2 * k;
+              const float m0 = msh[32 * half + h], m1 = msh[32 * half + h + 1];
+              const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h]) * p.scale_log2 - m0);
+              const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h + 1]) * p.scale_log2 - m1);
+              w[k] = f2_to_h2(p0, p1);
+            }
+            const int pc = 4 * half + c;
+            *reinterpret_cast<uint4*>(prow + ((pc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+        // the S buffer is released after its last read
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
       }
-      // S buffer sb has been read for the last time: the logits of tile it + 2 may overwrite it
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
-      // P was read by the values and the row sums of tile it - 1
-      if (it >= 1) {
-        if (!all_softmax(wait_bar(&bars[PV_DONE + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 14))) {
-          ok = false;
-          break;
-        }
-      }
-      // probabilities, fp16, row `row` of P (MN-major: 64 heads contiguous, 128-byte swizzle)
-      uint8_t* prow = smem + kPOff + row * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
       tc::fence_proxy_async();
       tc::fence_before();
       __syncwarp();
@@ -860,63 +730,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     // ---------------- epilogue ----------------
     const int last = n_tiles - 1;
     const bool have = all_softmax(ok && n_tiles > 0 &&
-                                  wait_bar(&bars[PV_DONE + (last & 1)], (last >> 1) & 1, abort_flag, p.hdr, 8));
+                                  wait_bar(&bars[P_EMPTY + (last & 1)], (last >> 1) & 1, abort_flag, p.hdr, 8));
     tc::fence_after();
-    // the row sums, one per head, written by the row-sum warp before its last arrival on PV_DONE
-    float* lsh = reinterpret_cast<float*>(smem + kLsumOff);
+    // the row sums, one per head, written by the row-sum warp before its last arrival on P_EMPTY
     if (!have && tid < 64) lsh[tid] = 0.0f;
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const int64_t prow_base = (u.unit * p.splits + split) * H;
-    if (p.cluster) {
-      // o is staged by every warp after the roles end; m and l are already in shared memory
-      if (tid == 0) flag[3] = have ? 1 : 0;
-      if (!have && tid < 64) msh[tid] = -INFINITY;
-    }
+    if (tid == 0) flag[3] = have ? 1 : 0;
+    if (p.splits == 1) {
+      // 1 / l per head, over red (whose last use was the last tile's softmax)
+      if (tid < 64) red[tid] = lsh[tid] > 0.0f ? 1.0f / lsh[tid] : 0.0f;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
 #pragma unroll 1
-    for (int k = 0; k < 8 && !p.cluster; ++k) {
-      uint32_t o[32];
-      if (have) {
-        tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
-        tc::wait_ld();
-      } else {
+      for (int k = 0; k < 8; ++k) {
+        uint32_t o[32];
+        if (have) {
+          tc::ld_32x32(tbase + lane_base + kColO + 32 * k, o);
+          tc::wait_ld();
+        } else {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) o[h] = 0u;
-      }
-      const int d = 128 * (k >> 1) + tid;
+          for (int h = 0; h < 32; ++h) o[h] = 0u;
+        }
+        const int d = 128 * (k >> 1) + tid;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int h = 32 * (k & 1) + j;
-        if (h >= H) break;
-        const float l = lsh[h];
-        const float x = __uint_as_float(o[j]);
-        if (p.splits == 1) p.out[(u.unit * H + h) * (int64_t)kLatent + d] = l > 0.0f ? x / l : 0.0f;
-        else p.part_o[(prow_base + h) * kLatent + d] = x;
+        for (int j = 0; j < 32; ++j) {
+          const int h = 32 * (k & 1) + j;
+          if (h >= H) break;
+          p.out[(u.unit * H + h) * (int64_t)kLatent + d] = __uint_as_float(o[j]) * red[h];
+        }
       }
-    }
-    if (tid < H && !p.cluster) {
-      const float l = lsh[tid];
-      const float m = have ? msh[tid] : -INFINITY;
-      if (p.splits == 1) {
-        if (p.out_lse != nullptr) p.out_lse[u.unit * H + tid] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      } else {
-        *reinterpret_cast<float2*>(p.part_ml + (prow_base + tid) * 2) = make_float2(m, l);
+      if (tid < H && p.out_lse != nullptr) {
+        const float l = lsh[tid];
+        p.out_lse[u.unit * H + tid] = l > 0.0f ? (msh[tid] + log2f(l)) * kLn2 : -INFINITY;
       }
+    } else if (tid < H) {
+      *reinterpret_cast<float2*>(p.part_ml + (prow_base + tid) * 2) = make_float2(have ? msh[tid] : -INFINITY, lsh[tid]);
     }
     tc::fence_before();
   }
 
-  if (p.cluster) {
-    // ---------------- staging of o: [head][512] fp32 over the operand area ----------------
+  if (p.splits > 1) {
+    // ---------------- this split's unnormalised o, written by all warps ----------------
     // Every product has completed (the softmax saw the last values finish). Warp w reads tensor-memory
-    // subpartition w % 4 (latent columns 32 (w % 4) .. of each 128-column chunk), 32-column pieces
+    // subpartition w % 4 (latent column 32 (w % 4) + lane of each 128-column chunk), 32-column pieces
     // 2 (w / 4) and 2 (w / 4) + 1.
     __syncwarp();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    const bool had = flag[3] != 0;
+    const int64_t prow_base = (u.unit * p.splits + split) * H;
     {
-      const bool had = flag[3] != 0;
-      float* stage = reinterpret_cast<float*>(smem + kRawOff);
       const uint32_t sp_base = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll 1
       for (int k = 2 * (warp >> 2); k < 2 * (warp >> 2) + 2; ++k) {
@@ -924,58 +788,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         if (had) {
           tc::ld_32x32(tbase + sp_base + kColO + 32 * k, o);
           tc::wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
         }
         const int d = 128 * (k >> 1) + 32 * (warp & 3) + lane;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) stage[(32 * (k & 1) + j) * kLatent + d] = had ? __uint_as_float(o[j]) : 0.0f;
-      }
-    }
-    // ---------------- merge of the cluster's splits ----------------
-    // Thread = (head tid / 8, every eighth float4 column of this CTA's slice); the weights of the splits
-    // for its head are computed once: w_s = 2^(m_s - M) / sum_s 2^(m_s - M) l_s over splits with l_s > 0.
-    cluster_sync();
-    const int S = p.splits;
-    const int h = tid >> 3, t8 = tid & 7;
-    const int c_lo = split * (kLatent / 4) / S, c_hi = (split + 1) * (kLatent / 4) / S;
-    const float* stage = reinterpret_cast<const float*>(smem + kRawOff);
-    const float* lsum = reinterpret_cast<const float*>(smem + kLsumOff);
-    if (h < H) {
-      float ms[8], ls[8];
-      float M = -INFINITY;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        ms[s] = -INFINITY;
-        ls[s] = 0.0f;
-        if (s < S) {
-          ms[s] = ld_cluster_f32(cluster_addr(msh + h, s));
-          ls[s] = ld_cluster_f32(cluster_addr(lsum + h, s));
-          if (ls[s] > 0.0f) M = fmaxf(M, ms[s]);
+        for (int j = 0; j < 32; ++j) {
+          const int h = 32 * (k & 1) + j;
+          if (h < H) p.part_o[(prow_base + h) * kLatent + d] = __uint_as_float(o[j]);
         }
       }
-      float L = 0.0f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        ms[s] = (s < S && ls[s] > 0.0f) ? exp2f(ms[s] - M) : 0.0f;     // the split's weight
-        L += ms[s] * ls[s];
-      }
-      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-      for (int c = c_lo + t8; c < c_hi; c += 8) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          if (s < S && ms[s] > 0.0f) {
-            const float4 v = ld_cluster_v4(cluster_addr(stage + h * kLatent + 4 * c, s));
-            acc.x += ms[s] * v.x; acc.y += ms[s] * v.y; acc.z += ms[s] * v.z; acc.w += ms[s] * v.w;
-          }
-        }
-        *reinterpret_cast<float4*>(p.out + (u.unit * H + h) * (int64_t)kLatent + 4 * c) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-      }
-      if (split == 0 && t8 == 0 && p.out_lse != nullptr)
-        p.out_lse[u.unit * H + h] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
-    // no CTA may leave while another still reads its shared memory
-    cluster_sync();
   }
   __syncthreads();
   tc::fence_after();
@@ -983,35 +807,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 }
 
 // out[u][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, splits in order; lse = (M + log2 L) ln 2.
+// One block per (unit, head), thread = 4 latent columns; the splits are read eight at a time with every
+// load of a batch issued before the first use.
 __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
+  constexpr int kBatch = 8;
   const int64_t row = blockIdx.x;                 // unit * H + h
   const int64_t unit = row / p.heads;
   const int h = (int)(row % p.heads);
-  const int d = threadIdx.x * 4;
+  const int S = p.splits, H = p.heads;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + unit * S * H + h;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) + (unit * S * H + h) * (int64_t)(kLatent / 4) + threadIdx.x;
   float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit * p.splits + s) * p.heads + h) * 2);
-    if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+  for (int s0 = 0; s0 < S; s0 += kBatch) {
+    float2 x[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) x[i] = s0 + i < S ? ml[(s0 + i) * H] : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (x[i].y > 0.0f) M = fmaxf(M, x[i].x);
   }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.0f;
   if (M != -INFINITY) {
-    for (int s = 0; s < p.splits; ++s) {
-      const int64_t pr = (unit * p.splits + s) * p.heads + h;
-      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + pr * 2);
-      if (!(ml.y > 0.0f)) continue;
-      const float w = exp2f(ml.x - M);
-      const float4 v = *reinterpret_cast<const float4*>(p.part_o + pr * kLatent + d);
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-      L += w * ml.y;
+    for (int s0 = 0; s0 < S; s0 += kBatch) {
+      float2 x[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        x[i] = make_float2(-INFINITY, 0.0f);
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 + i < S) {
+          x[i] = ml[(s0 + i) * H];
+          v[i] = po[(int64_t)(s0 + i) * H * (kLatent / 4)];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        if (!(x[i].y > 0.0f)) continue;
+        const float w = exp2f(x[i].x - M);
+        acc.x += w * v[i].x; acc.y += w * v[i].y; acc.z += w * v[i].z; acc.w += w * v[i].w;
+        L += w * x[i].y;
+      }
     }
   }
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  *reinterpret_cast<float4*>(p.out + row * kLatent + d) =
+  reinterpret_cast<float4*>(p.out)[row * (kLatent / 4) + threadIdx.x] =
       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   if (threadIdx.x == 0 && p.out_lse != nullptr) p.out_lse[row] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
-
 
 }  // namespace
 
@@ -1037,60 +880,12 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   clear_stale_error();
   cudaError_t e = ensure_smem_limit(attn_tc_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.splits, (unsigned)p.units);
-  if (!p.cluster) {
-    attn_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, map);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel, p, map);
-}
-
-int attn_max_clusters(int size) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  static std::mutex mu;
-  static std::map<std::pair<int, int>, int> known;
-  std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(dev, size);
-  auto it = known.find(key);
-  if (it != known.end()) return it->second;
-  int n = 0;
-  if (ensure_smem_limit(attn_tc_kernel, kSmemBytes) == cudaSuccess) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)size, 1, 1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)size;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, attn_tc_kernel, &cfg) != cudaSuccess) n = 0;
-  }
-  cudaGetLastError();
-  known[key] = n;
-  return n;
+  attn_tc_kernel<<<dim3((unsigned)p.splits, (unsigned)p.units), kThreads, kSmemBytes, s>>>(p, map);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
-  if (p.units == 0 || p.splits == 1 || p.cluster) return cudaSuccess;
+  if (p.units == 0 || p.splits == 1) return cudaSuccess;
   ProfScope prof("attn_combine", s);
   clear_stale_error();
   combine_kernel<<<(unsigned)(p.units * p.heads), 128, 0, s>>>(p);

@@ -73,7 +73,7 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 // ---------------------------------------------------------------------------------------------
 struct AttnLayout {
   int64_t units;
-  int n_ct, n_wt, splits, cache_splits, win_split, cluster, last_ct;
+  int n_ct, n_wt, splits, cache_splits, win_split, last_ct;
   size_t o_off, ml_off, total;
 };
 
@@ -99,11 +99,9 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
     if (last > L.n_ct - (L.cache_splits - 1)) last = L.n_ct - (L.cache_splits - 1);
     L.last_ct = last;
   }
-  // the splits of a unit merge in shared memory when they fit a portable cluster and every unit's
-  // cluster can be resident at once; otherwise through partials in the workspace and a combine kernel
-  L.cluster = (L.splits >= 2 && L.splits <= 8 && L.units <= attn_max_clusters(L.splits)) ? 1 : 0;
+  // every split writes its partial (o, m, l) to the workspace and a combine kernel merges them
   L.o_off = CSA_WS_HEADER_BYTES;
-  const size_t parts = (L.splits > 1 && !L.cluster) ? (size_t)L.units * L.splits * a->heads : 0;
+  const size_t parts = L.splits > 1 ? (size_t)L.units * L.splits * a->heads : 0;
   L.ml_off = round_up(L.o_off + parts * kLatent * 4, 256);
   L.total = round_up(L.ml_off + parts * 2 * 4, 256);
   return L;
@@ -468,7 +466,6 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.swa = static_cast<const __nv_bfloat16*>(a->swa); p.swa_stride_b = a->swa_stride_b; p.swa_rows = a->swa_rows;
   p.swa_len = a->swa_len; p.swa_first_pos = a->swa_first_pos;
   p.splits = L.splits; p.cache_splits = L.cache_splits; p.win_split = L.win_split; p.n_ct = L.n_ct; p.n_wt = L.n_wt;
-  p.cluster = L.cluster;
   p.last_ct = L.last_ct;
   p.part_o = reinterpret_cast<float*>(w + L.o_off);
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);

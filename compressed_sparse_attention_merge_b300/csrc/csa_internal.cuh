@@ -137,6 +137,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
+// Non-blocking check of the phase with the given parity: true if it has completed (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(done) : "r"(bar_addr), "r"(parity) : "memory");
+  return done != 0;
+}
+
 // Polls the phase with the given parity; true once it has completed, false after kSpinLimit polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_addr(bar);
@@ -246,9 +254,6 @@ struct AttnParams {
   // last_ct >= 0: the last cache split, which then also takes the window tiles, gets cache tiles
   // [n_ct - last_ct, n_ct) and the others share the rest evenly; -1: every cache split gets an even share.
   int last_ct;
-  // cluster = 1: the splits of a unit form one thread-block cluster and are merged through distributed
-  // shared memory by the attention kernel itself (no partials, no combine launch).
-  int cluster;
   float* part_o;               // [units][splits][heads][512]
   float* part_ml;              // [units][splits][heads][2]
   float* out;                  // used when splits == 1
@@ -266,8 +271,6 @@ cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s
 cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
-// Clusters of `size` attention CTAs that can be resident at once on the current device (0 if none).
-int attn_max_clusters(int size);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
 
 // Clears an error that an earlier runtime call of another component left in this thread's last-error

@@ -336,11 +336,10 @@ typedef struct csa_attn_args {
 } csa_attn_args;
 
 /* Workspace bytes for one call with these arguments on the current device. A query's rows are cut into
- * 128-row tiles shared by several CTAs (splits). When a query's splits fit one thread-block cluster of at
- * most 8 CTAs, and every query's cluster can be resident at once, the splits merge through distributed
- * shared memory. The workspace is then only the status header. Otherwise it also holds every split's
- * partial (o, m, l), merged by a second kernel. The answer depends on the device's SM count and cluster
- * occupancy, so query it with the device current that will run the call. */
+ * 128-row tiles shared by several CTAs (splits), as many as fill the device's SMs. With more than one split
+ * the workspace holds every split's partial (o, m, l), which a second kernel merges; with one split it is only
+ * the status header. The answer depends on the device's SM count, so query it with the device current that
+ * will run the call. */
 size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* args);
 csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
                                   cudaStream_t stream);
