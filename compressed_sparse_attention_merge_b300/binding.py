@@ -104,6 +104,8 @@ def lib():
             f = getattr(L, name)
             f.restype = I32
             f.argtypes = [I64, ctypes.POINTER(AttnArgs), P, SZ, P]
+        L.csa_debug_set_fault.restype = I32
+        L.csa_debug_set_fault.argtypes = [I32, ctypes.c_uint32]
         L.csa_profile_begin.restype = I32
         L.csa_profile_begin.argtypes = [I32]
         L.csa_profile_end.restype = I32
@@ -357,6 +359,15 @@ def sparse_attn_prefill(q, cache, n_entries, idx, out, *, q_pos, max_entries, wi
 # ------------------------------------------------------------------------------------------------
 # Kernel timing
 # ------------------------------------------------------------------------------------------------
+
+FAULT_NONE, FAULT_WITHHOLD_ARRIVAL = 0, 1
+
+
+def debug_set_fault(fault, spin_limit=0):
+    """csa_debug_set_fault (test-only): make later attention launches withhold one internal arrival so
+    that a bounded wait gives up after spin_limit polls; FAULT_NONE restores normal launches."""
+    _check(lib().csa_debug_set_fault(int(fault), int(spin_limit)), "csa_debug_set_fault")
+
 
 def profile_begin(max_launches=4096):
     _check(lib().csa_profile_begin(max_launches), "csa_profile_begin")

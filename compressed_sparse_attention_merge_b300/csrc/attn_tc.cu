@@ -100,10 +100,10 @@ constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T M
 
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         uint32_t* hdr, uint32_t detail) {
+                                         uint32_t* hdr, uint32_t detail, uint32_t limit) {
   const uint32_t a = smem_addr(bar);
   if (mbar_test_wait(a, parity)) return true;      // the common case: the phase completed already
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if ((i & 7u) == 7u && *abort_flag) return false;
   }
@@ -114,8 +114,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 
 // The same wait taken by a whole warp; the result is the same on every lane.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* hdr, uint32_t detail) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, hdr, detail));
+                                              uint32_t* hdr, uint32_t detail, uint32_t limit) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, hdr, detail, limit));
 }
 
 // Bounded wait that ignores the abort flag (draining copies that must land before the CTA exits).
@@ -383,21 +383,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     }
     if (qt < 64) msh[qt] = -INFINITY;
     tc::fence_proxy_async();
-    asm volatile("bar.sync 2, %0;" :: "n"(kQThreads) : "memory");
+    asm volatile("bar.sync 2, %0;" :: "n"(kThreads) : "memory");
+  } else {
+    // the gather warp starts its L2 prefetches once the queries have arrived, so that the queries and the
+    // first tile's bytes (loaded by the converters) are not queued behind the later tiles
+    asm volatile("bar.sync 2, %0;" :: "n"(kThreads) : "memory");
   }
 
   if (warp == kGatherWarp) {
     // ---------------- gather: block-id checks, L2 prefetch, later window tiles ----------------
-    // the blocks of cache tile k go to L2 when the converters start tile k - 2 (the first three at once), so
-    // that the early tiles are not queued behind the later ones; lanes 0-15 take one block each
+    // the blocks of cache tile k go to L2 when the converters start tile k - 2 (tiles 1 and 2 at once; the
+    // converters load tile 0 themselves, so its ids are only checked); lanes 0-15 take one block each
     for (int k = 0; k < n_cache; ++k) {
       const int t = nw + k - 3;           // the tile whose first values chunk paces this prefetch
-      if (t >= 0 && !wait_bar_warp(&bars[V_FULL], t & 1, abort_flag, p.hdr, 16)) break;
+      if (t >= 0 && !wait_bar_warp(&bars[V_FULL], t & 1, abort_flag, p.hdr, 16, p.spin_limit)) break;
       const int slot = (c0 + k) * kTileBlocks + lane;
       if (lane < kTileBlocks && slot < p.top_k) {
         const int64_t id = __ldg(p.idx + u.unit * p.top_k + slot);
         if (id < -1 || id >= u.nb_cap) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
-        if (id >= 0 && id < u.n_b) prefetch_l2(seq + id * kLatBlk, kLatBlk);
+        if (k > 0 && id >= 0 && id < u.n_b) prefetch_l2(seq + id * kLatBlk, kLatBlk);
       }
     }
     if (lane == 0) {
@@ -410,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       for (int tw = 1; tw < nw; ++tw) {
         // the values buffer holds the previous tile until its value products are done
         bool ok = true;
-        for (int c = 0; c < kChunks && ok; ++c) ok = wait_bar(&bars[V_EMPTY + c], (tw - 1) & 1, abort_flag, p.hdr, 9);
+        for (int c = 0; c < kChunks && ok; ++c) ok = wait_bar(&bars[V_EMPTY + c], (tw - 1) & 1, abort_flag, p.hdr, 9, p.spin_limit);
         if (!ok) break;
         copy_window_tile(p, u, tw, smem, &swa_map, &bars[WIN_FULL]);
         ++copied;
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         bool oob;
         vr = window_row(p, u, it, row, &oob);
         if (oob && hp == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
-        if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], it & 1, abort_flag, p.hdr, 10))) break;
+        if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], it & 1, abort_flag, p.hdr, 10, p.spin_limit))) break;
       }
       const bool v_next = !win && k + 1 < n_cache && cache_ok(u, id_nxt, row);
 #pragma unroll 1
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
         // logits operand: panel pnl of tile it goes to ring slot pnl & 3 (use 2 it + c / 2 of that slot)
         const uint32_t slot = pnl & 3, use = 2u * it + (c >> 1);
-        if (use > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (use - 1) & 1u, abort_flag, p.hdr, 3))) {
+        if (use > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (use - 1) & 1u, abort_flag, p.hdr, 3, p.spin_limit))) {
           stop = true;
           break;
         }
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
         // values operand while the tensor-memory store completes: the chunk must have been consumed by the
         // previous tile's value products (a window tile's chunks were, before its copy was issued)
-        bool freed = win || it == 0 || __all_sync(0xffffffffu, wait_bar(&bars[V_EMPTY + c], (it - 1) & 1, abort_flag, p.hdr, 6));
+        bool freed = win || it == 0 || __all_sync(0xffffffffu, wait_bar(&bars[V_EMPTY + c], (it - 1) & 1, abort_flag, p.hdr, 6, p.spin_limit));
         if (freed) {
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -502,11 +506,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     bool ok = true;
     for (int it = 0; it < n_tiles && ok; ++it) {
       const int sb = it & 1;
-      if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4)) break;
+      if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4, p.spin_limit)) break;
       const uint32_t d = tbase + kColS + 64 * sb;
       for (int pnl = 0; pnl < kPanels; ++pnl) {
         const uint32_t slot = pnl & 3, use = 2u * it + (pnl >> 2);
-        if (!wait_bar_warp(&bars[TRING_FULL + slot], use & 1u, abort_flag, p.hdr, 4)) { ok = false; break; }
+        if (!wait_bar_warp(&bars[TRING_FULL + slot], use & 1u, abort_flag, p.hdr, 4, p.spin_limit)) { ok = false; break; }
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -527,11 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     for (int it = 0; it < n_tiles; ++it) {
       const int pb = it & 1;
       const uint32_t p_addr = s_base + kPOff + pb * kPBytes;
-      if (!wait_bar_warp(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 5)) break;
+      if (!wait_bar_warp(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 5, p.spin_limit)) break;
       tc::fence_after();
       bool ok = true;
       for (int c = 0; c < kChunks; ++c) {
-        if (!wait_bar_warp(&bars[V_FULL + c], it & 1, abort_flag, p.hdr, 6)) { ok = false; break; }
+        if (!wait_bar_warp(&bars[V_FULL + c], it & 1, abort_flag, p.hdr, 6, p.spin_limit)) { ok = false; break; }
         tc::fence_after();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -542,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         tc::commit_warp(&bars[V_EMPTY + c]);
       }
       if (!ok) break;
-      tc::commit_warp(&bars[P_EMPTY + pb]);
+      if (!(p.fault == CSA_FAULT_WITHHOLD_ARRIVAL && it == 0)) tc::commit_warp(&bars[P_EMPTY + pb]);
     }
     tc::commit_warp(&bars[FIN_V]);
     drain_bar(&bars[FIN_V], 0);
@@ -553,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const int h0 = 2 * lane;
     for (int it = 0; it < n_tiles; ++it) {
       const int pb = it & 1;
-      if (!wait_bar_warp(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 13)) break;
+      if (!wait_bar_warp(&bars[P_FULL + pb], (it >> 1) & 1, abort_flag, p.hdr, 13, p.spin_limit)) break;
       if (flag[pb]) {
         // the softmax raised the reference maxima for this tile: rescale like O
         l0 *= alpha[64 * pb + h0];
@@ -593,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         valid = cache_ok(u, sid_nxt, row);
         sid_nxt = it - nw + 1 < n_cache ? cache_id(p, u, c0 + it - nw + 1, row) : -1;
       }
-      if (!all_softmax(wait_bar(&bars[S_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 7))) { ok = false; break; }
+      if (!all_softmax(wait_bar(&bars[S_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 7, p.spin_limit))) { ok = false; break; }
       tc::fence_after();
       // P buffer sb, alpha[sb] and flag[sb] were last read by the value products and row sums of tile it - 2
-      if (it >= 2 && !all_softmax(wait_bar(&bars[P_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12))) {
+      if (it >= 2 && !all_softmax(wait_bar(&bars[P_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 12, p.spin_limit))) {
         ok = false;
         break;
       }
@@ -678,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           // every value product before this tile must be complete before O is rescaled (the ones of tile
           // it - 1 complete last: the values are issued in tile order); the row-sum warp rescales l itself
           if (it > 0) {
-            if (!all_softmax(wait_bar(&bars[P_EMPTY + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 12))) {
+            if (!all_softmax(wait_bar(&bars[P_EMPTY + ((it - 1) & 1)], ((it - 1) >> 1) & 1, abort_flag, p.hdr, 12, p.spin_limit))) {
               ok = false;
               break;
             }
@@ -730,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     // ---------------- epilogue ----------------
     const int last = n_tiles - 1;
     const bool have = all_softmax(ok && n_tiles > 0 &&
-                                  wait_bar(&bars[P_EMPTY + (last & 1)], (last >> 1) & 1, abort_flag, p.hdr, 8));
+                                  wait_bar(&bars[P_EMPTY + (last & 1)], (last >> 1) & 1, abort_flag, p.hdr, 8, p.spin_limit));
     tc::fence_after();
     // the row sums, one per head, written by the row-sum warp before its last arrival on P_EMPTY
     if (!have && tid < 64) lsh[tid] = 0.0f;

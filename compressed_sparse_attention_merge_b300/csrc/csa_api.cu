@@ -195,6 +195,14 @@ EncodeTiledFn encode_tiled_fn() {
 
 thread_local char g_last_error[256] = "";
 
+int g_fault = CSA_FAULT_NONE;
+uint32_t g_fault_spin = kSpinLimit;
+
+void debug_fault(int* fault, uint32_t* spin_limit) {
+  *fault = g_fault;
+  *spin_limit = g_fault == CSA_FAULT_NONE ? kSpinLimit : g_fault_spin;
+}
+
 csa_status cuda_fail(cudaError_t e, const char* where) {
   std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
   return CSA_ERR_CUDA;
@@ -330,7 +338,10 @@ csa_status csa_pack_fp4_multi(int n_jobs, const int64_t* batch, const csa_pack_a
 }
 
 // ------------------------------------------------------------------------------------------------
-static csa_status validate_index(int64_t batch, const csa_index_args* a) {
+}  // extern "C"
+
+namespace csa {
+csa_status validate_index_args(int64_t batch, const csa_index_args* a) {
   if (a == nullptr || batch < 0) return CSA_ERR_INVALID_ARG;
   if (a->n_query < 1 || a->max_entries < 0) return CSA_ERR_INVALID_ARG;
   if (a->heads != 1 && a->heads != 2 && a->heads != 4 && a->heads != 8) return CSA_ERR_INVALID_ARG;
@@ -353,6 +364,9 @@ static csa_status validate_index(int64_t batch, const csa_index_args* a) {
     return CSA_ERR_INVALID_ARG;
   return CSA_OK;
 }
+}  // namespace csa
+
+extern "C" {
 
 size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* a) {
   if (a == nullptr || batch < 0) return 0;
@@ -360,7 +374,7 @@ size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* a) {
 }
 
 csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
-  csa_status st = validate_index(batch, a);
+  csa_status st = validate_index_args(batch, a);
   if (st != CSA_OK) return st;
   int num_sms = 0;
   st = current_device(&num_sms);
@@ -471,6 +485,7 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
   p.out = a->out; p.out_lse = a->out_lse;
   p.hdr = reinterpret_cast<uint32_t*>(w);
+  debug_fault(&p.fault, &p.spin_limit);
   if (cudaError_t e = launch_attn(p, stream)) return cuda_fail(e, "attn");
   if (cudaError_t e = launch_combine(p, stream)) return cuda_fail(e, "combine");
   return CSA_OK;
@@ -484,6 +499,15 @@ csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* a, void* w
 csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
                                    cudaStream_t stream) {
   return sparse_attn(batch, a, ws, ws_bytes, stream, true);
+}
+
+// ------------------------------------------------------------------------------------------------
+csa_status csa_debug_set_fault(int fault, uint32_t spin_limit) {
+  if (fault != CSA_FAULT_NONE && fault != CSA_FAULT_WITHHOLD_ARRIVAL) return CSA_ERR_INVALID_ARG;
+  if (fault != CSA_FAULT_NONE && spin_limit == 0) return CSA_ERR_INVALID_ARG;
+  csa::g_fault = fault;
+  csa::g_fault_spin = spin_limit;
+  return CSA_OK;
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -259,7 +259,14 @@ struct AttnParams {
   float* out;                  // used when splits == 1
   float* out_lse;
   uint32_t* hdr;
+  // Bounded waits give up after this many polls (kSpinLimit unless a test lowered it), and a nonzero
+  // fault makes the kernel withhold one arrival (csa_debug_set_fault).
+  uint32_t spin_limit;
+  int fault;
 };
+
+// The fault and poll limit that csa_debug_set_fault set for later attention launches of this process.
+void debug_fault(int* fault, uint32_t* spin_limit);
 
 // ------------------------------------------------------------------------------------------------
 // Launchers (one per kernel file). Each returns the launch error, if any.
@@ -294,6 +301,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
+
+// Host-side checks of csa_index_topk's arguments (shapes, flags, pointers, alignment); CSA_OK when the call
+// may proceed. Touches no device state.
+csa_status validate_index_args(int64_t batch, const csa_index_args* a);
 
 // Records the text of a CUDA runtime failure for csa_last_error() and returns CSA_ERR_CUDA.
 csa_status cuda_fail(cudaError_t e, const char* where);

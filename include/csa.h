@@ -250,7 +250,9 @@ csa_status csa_index_topk(int64_t batch, const csa_index_args* args, void* ws, s
  *     is larger is rejected with CSA_ERR_WORKSPACE_TOO_SMALL before anything is launched, and
  *     csa_last_error() gives both sizes. Every GPU that loads the library holds the array until exit.
  *   - The first call on a device (with that device current) looks up the array's device address; make
- *     that first call before capturing any stream on that device.
+ *     that first call before capturing any stream on that device. A lookup that fails is retried by the
+ *     next call. Invalid arguments are rejected (CSA_ERR_INVALID_ARG, CSA_ERR_ALIGNMENT) before the size
+ *     check and before anything is queued.
  *   - Every call on a device shares the one array, and it keeps the previous call's contents; each call
  *     clears the status word itself. Calls whose work overlaps on the GPU (different streams, or
  *     different host threads, without ordering between them) race on the array and give undefined
@@ -345,6 +347,21 @@ csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* args, void
                                   cudaStream_t stream);
 csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
                                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * csa_debug_set_fault -- test-only fault injection for the device-side failure path.
+ *
+ * Every wait inside the library's kernels is bounded: after a fixed number of polls it gives up, records
+ * CSA_ERR_TIMEOUT in the workspace status word (read by csa_get_device_status) and the kernel's other
+ * roles stop too, so the kernel returns and the CUDA context stays usable. This call lets a test make such
+ * a wait run out without any GPU fault: with fault = CSA_FAULT_WITHHOLD_ARRIVAL, later attention launches
+ * of this process withhold one internal arrival (the value products of a CTA's first tile never report
+ * completion), so a wait behind it gives up after spin_limit polls (each poll suspends for at most about
+ * 20 microseconds). fault = CSA_FAULT_NONE restores normal launches (spin_limit is then ignored and the
+ * library's own limit applies). Process-wide, not thread-safe; not for production use.
+ * ------------------------------------------------------------------------------------------------ */
+enum { CSA_FAULT_NONE = 0, CSA_FAULT_WITHHOLD_ARRIVAL = 1 };
+csa_status csa_debug_set_fault(int fault, uint32_t spin_limit);
 
 /* ------------------------------------------------------------------------------------------------
  * Kernel timing (opt-in, not thread-safe). Between csa_profile_begin and csa_profile_end every kernel

@@ -129,7 +129,7 @@ def test_misaligned_pointers_rejected_before_any_device_call(lib):
 
 
 def test_attention_workspace_size_is_host_only(lib):
-    # without a device the size is the partials layout (no cluster merge), 148 SMs assumed: 4 queries of
+    # without a device the size is the partials layout, 148 SMs assumed: 4 queries of
     # 16 cache tiles take 16 cache splits and a window split each, so 17 partials of (o, m, l) per head
     from compressed_sparse_attention_merge_b300 import binding as b
     aa = b.AttnArgs()
@@ -142,3 +142,21 @@ def test_attention_workspace_size_is_host_only(lib):
     assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) >= 256 + 2 * 64 * (512 * 4 + 2 * 4)
     aa.swa_rows, aa.window = 0, 0
     assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) == 256
+
+
+def test_static_index_validates_before_sizing(lib):
+    # csa_index_topk_static checks its arguments first: a malformed call is CSA_ERR_INVALID_ARG (not a
+    # workspace-size answer) and nothing is queued; without a device none of this needs one
+    from compressed_sparse_attention_merge_b300 import binding as b
+    ia = b.IndexArgs()
+    ia.n_query, ia.heads, ia.dim, ia.top_k, ia.flags, ia.max_entries = -3, 4, 128, 8, b.IDX_RELU, 64
+    assert lib.csa_index_topk_static(1, ctypes.byref(ia), None, None) == b.ERR_INVALID_ARG
+    ia.n_query, ia.max_entries = 1, -5
+    assert lib.csa_index_topk_static(1, ctypes.byref(ia), None, None) == b.ERR_INVALID_ARG
+    # a call whose scratch would exceed the array but whose arguments are malformed (3 heads): invalid first
+    ia.heads, ia.max_entries, ia.n_query = 3, 8 << 20, 64
+    assert lib.csa_index_topk_static(4, ctypes.byref(ia), None, None) == b.ERR_INVALID_ARG
+    # a well-formed call with misaligned queries: alignment, still before the size check
+    ia.heads, ia.n_query, ia.max_entries = 4, 1, 64
+    ia.q_idx, ia.keys, ia.n_entries, ia.out_idx, ia.keys_stride_b = 0x10008, 0x10000, 0x10000, 0x10000, 8 * 576
+    assert lib.csa_index_topk_static(1, ctypes.byref(ia), None, None) == b.ERR_ALIGNMENT

@@ -284,3 +284,36 @@ def test_prefill_matches_oracle(csa):
                                                 int(pos[j]), W, SCALE)
         assert_attn_close(out[0, j], ref, f"position {pos[j]}")
         assert_lse_close(lse[0, j], ref_lse, f"position {pos[j]}")
+
+
+def test_bounded_wait_gives_up_and_the_context_survives(csa):
+    # Failure path without a GPU fault: the test-only injection makes the attention withhold one internal
+    # arrival, so the epilogue's wait (one cache tile per query, no window: one tile per CTA) gives up after
+    # 64 polls, records CSA_ERR_TIMEOUT and the kernel returns. The same call then runs normally on the same
+    # context and matches the oracle.
+    g = torch.Generator(device=DEV).manual_seed(61)
+    B, T, H, K = 2, 2 * 300, 64, 16
+    E = T // 2
+    x = _latents(g, B, T)
+    q = torch.randn(B, 1, H, 512, generator=g, device=DEV).to(torch.bfloat16)
+    ws0 = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T] * B, E, 512, 2, csa.SCALE_AMAX, ws0)
+    n_entries = torch.full((B,), E, dtype=torch.int32, device=DEV)
+    idx = torch.arange(K, dtype=torch.int32, device=DEV).view(1, 1, K).repeat(B, 1, 1).contiguous()
+    out = torch.full((B, 1, H, 512), float("nan"), device=DEV)
+    args = csa.attn_args(q, cache, n_entries, idx, out, max_entries=E, window=0, scale=SCALE)
+    ws = csa.workspace(csa.sparse_attn_workspace_size(B, args), DEV)
+    csa.debug_set_fault(csa.FAULT_WITHHOLD_ARRIVAL, 64)
+    try:
+        csa.sparse_attn_decode(q, cache, n_entries, idx, out, max_entries=E, window=0, scale=SCALE, ws=ws)
+        status = csa.device_status(ws)
+    finally:
+        csa.debug_set_fault(csa.FAULT_NONE)
+    assert status == csa.ERR_TIMEOUT
+    csa.sparse_attn_decode(q, cache, n_entries, idx, out, max_entries=E, window=0, scale=SCALE, ws=ws)
+    assert csa.device_status(ws) == csa.OK
+    xf, qf, o = to_np(x), to_np(q), out.cpu().numpy()
+    for b in range(B):
+        entries = o_fp4.dequantize(o_fp4.pack(xf[b], 2, "amax", n_blocks=-(-E // 8)), 512, E)
+        ref, _ = o_attn.decode_attention(qf[b, 0].astype(np.float64), entries, E, np.arange(K), np.zeros((0, 512)), SCALE)
+        assert_attn_close(o[b, 0], ref, f"seq {b} after the timeout")

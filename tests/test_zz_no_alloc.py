@@ -10,6 +10,9 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import fp4 as o_fp4
+from oracle import indexer as o_idx
+
 from _pipeline import gpu_index, gpu_pack_sequences
 
 pytestmark = pytest.mark.gpu
@@ -60,3 +63,52 @@ def test_static_scratch_rejects_too_large_a_call(csa):
     assert "static array" in str(err.value)
     torch.cuda.synchronize()
     assert torch.all(out == -7)
+
+
+def test_static_scratch_matches_the_oracle_flat_and_hierarchical(csa):
+    # the static entry point against the CPU oracle directly: a flat call, then a hierarchical call that uses
+    # the coarse-score and kept-super-block regions of the array, then the flat call again
+    g = torch.Generator(device=DEV).manual_seed(73)
+    lengths, dim, heads, top_k, keep = [3 * 512 + 77, 512 * 5], 128, 4, 48, 128
+    B, E = len(lengths), max(lengths)
+    keys = torch.randint(-4, 5, (B, E, dim), generator=g, device=DEV).float()
+    q_idx = torch.randint(-4, 5, (B, 1, heads, dim), generator=g, device=DEV).float()
+    ws = csa.workspace(256, DEV)
+    coarse = csa.empty_coarse(B, E, dim, DEV)
+    kc = gpu_pack_sequences(csa, keys, lengths, E, dim, 1, csa.SCALE_POW2, ws, coarse=coarse)
+    n_entries = torch.tensor(lengths, dtype=torch.int32, device=DEV)
+    kf, qi = keys.cpu().numpy(), q_idx.cpu().numpy()
+    for hier in (False, True, False):
+        got = torch.full((B, 1, top_k), -7, dtype=torch.int32, device=DEV)
+        status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+        extra = dict(coarse_sum=coarse, keep_blocks=keep) if hier else {}
+        csa.index_topk_static(q_idx, kc, n_entries, got, max_entries=E, top_k=top_k, status_out=status, **extra)
+        torch.cuda.synchronize()
+        assert int(status.item()) == csa.OK
+        for b in range(B):
+            n = lengths[b]
+            deq = o_fp4.dequantize(o_fp4.pack(kf[b, :n], 1, "pow2", n_blocks=-(-E // 8)), dim, E)
+            if hier:
+                ref, _ = o_idx.hierarchical_topk(qi[b], deq, n, top_k, keep)
+            else:
+                ref, _ = o_idx.flat_topk(qi[b], deq, n, top_k)
+            np.testing.assert_array_equal(got[b].cpu().numpy(), ref, err_msg=f"hier={hier} seq {b}")
+
+
+def test_static_scratch_reports_a_device_check_then_recovers(csa):
+    # an entry count beyond max_entries is clamped by the kernels and reported through status_out; the
+    # next call starts from a cleared status word and reports 0
+    q_idx, kc, n_entries, E = _case(csa, 74, [900, 640], 64, 2, 1)
+    top_k = 16
+    bad = n_entries.clone()
+    bad[1] = E + 100
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    out = torch.empty(2, 1, top_k, dtype=torch.int32, device=DEV)
+    csa.index_topk_static(q_idx, kc, bad, out, max_entries=E, top_k=top_k, status_out=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == csa.ERR_DEVICE_CHECK
+    csa.index_topk_static(q_idx, kc, n_entries, out, max_entries=E, top_k=top_k, status_out=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == csa.OK
+    ref, _ = gpu_index(csa, q_idx, kc, n_entries, E, top_k)
+    np.testing.assert_array_equal(out.cpu().numpy(), ref.cpu().numpy())
