@@ -69,7 +69,9 @@ constexpr int kMOff = kFlagOff + 16;                       // float m[64]
 constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[2][64]: per P buffer
 constexpr int kRedOff = kAlphaOff + 2 * 64 * 4;            // float red[4][64]
 constexpr int kLsumOff = kRedOff + 4 * 64 * 4;             // float lsum[64]: final row sums
-constexpr int kSmemBytes = kLsumOff + 64 * 4;
+constexpr int kQScaleOff = kLsumOff + 64 * 4;              // float qscale[64]: per-head log2 softmax scale
+constexpr int kQMaxOff = kQScaleOff + 64 * 4;              // uint qmax[64]: bits of each head's largest |q|
+constexpr int kSmemBytes = kQMaxOff + 64 * 4;
 static_assert(kVOff % 1024 == 0 && kPOff % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -320,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     mbar_init(&bars[FIN_V], 1);
     fence_mbar_init();
     flag[0] = 0; flag[1] = 0; *abort_flag = 0; flag[3] = 0;
+    for (int h = 0; h < 64; ++h) reinterpret_cast<uint32_t*>(smem + kQMaxOff)[h] = 0u;
   }
   tc::fence_before();
   __syncthreads();
@@ -357,13 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   }
 
   if (warp != kGatherWarp) {
-    // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero. Every load of a
-    // thread is issued before the first conversion.
+    // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero. Each head is first
+    // scaled by a power of two 2^-k_h that puts its largest magnitude in [2^14, 2^15), so that every
+    // finite bf16 query converts to fp16 exactly (bf16 carries 8 significant bits, fp16 11); the factor
+    // 2^k_h goes into that head's softmax scale. Every load of a thread is issued before the first use.
     constexpr int kQThreads = kThreads - 32;
     constexpr int kQItems = kHeadsPad * 64;
     constexpr int kQPer = (kQItems + kQThreads - 1) / kQThreads;
     const int qt = tid < kGatherWarp * 32 ? tid : tid - 32;
     const __nv_bfloat16* qg = p.q + u.unit * (int64_t)H * kLatent;
+    uint32_t* qmax = reinterpret_cast<uint32_t*>(smem + kQMaxOff);
+    float* qscale = reinterpret_cast<float*>(smem + kQScaleOff);
     uint4 v[kQPer];
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
@@ -376,10 +383,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     for (int k = 0; k < kQPer; ++k) {
       const int i = qt + k * kQThreads;
       if (i < kQItems) {
-        const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
-        const uint4 w = make_uint4(bf2_to_h2(v[k].x), bf2_to_h2(v[k].y), bf2_to_h2(v[k].z), bf2_to_h2(v[k].w));
-        *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = w;
+        // magnitudes compare as integers: the bits of |x| with the sign cleared
+        uint32_t m = 0u;
+        const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
+        atomicMax(qmax + (i >> 6), m);
       }
+    }
+    asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = qt + k * kQThreads;
+      if (i < kQItems) {
+        const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
+        const uint32_t mb = qmax[h];
+        int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;    // exponent of the largest |q|, - 14
+        sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+        const float f = __int_as_float((127 - sh) << 23);                  // 2^-sh, exact
+        const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = f2_to_h2(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+        *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    if (qt < 64) {
+      const uint32_t mb = qmax[qt];
+      int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;
+      sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+      qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);      // scale_log2 * 2^sh
     }
     if (qt < 64) msh[qt] = -INFINITY;
     tc::fence_proxy_async();
@@ -443,13 +477,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         uint8_t* vrow = smem + kVOff + c * kChunkBytes + hp * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
         uint32_t h[32];
         if (win) {
-          // bf16 -> fp16 of this row's 64 columns, in place; rows that are not attended become zero
+          // bf16 -> fp16 of this row's 64 columns, in place; rows that are not attended become zero. A value
+          // beyond the fp16 range (|x| > 65504, outside the call's contract) becomes infinite: reported.
+          uint32_t inf = 0u;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint4 x = *reinterpret_cast<const uint4*>(vrow + ((j ^ (row & 7)) << 4));
             h[4 * j] = vr ? bf2_to_h2(x.x) : 0u; h[4 * j + 1] = vr ? bf2_to_h2(x.y) : 0u;
             h[4 * j + 2] = vr ? bf2_to_h2(x.z) : 0u; h[4 * j + 3] = vr ? bf2_to_h2(x.w) : 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              inf |= ((h[4 * j + e] & 0x7C00u) == 0x7C00u) | ((h[4 * j + e] & 0x7C000000u) == 0x7C000000u);
           }
+          if (inf) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
         } else {
           dequant_panel(qa0, qb0, qs0, h);
           // shift the queue; the panel two steps ahead enters at the back
@@ -585,6 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   } else {
     // ---------------- softmax (warps 0-3, thread = tile row) ----------------
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float* qsc = reinterpret_cast<const float*>(smem + kQScaleOff);
     bool ok = true;
     int64_t sid_nxt = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
     for (int it = 0; it < n_tiles; ++it) {
@@ -622,12 +663,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           const float4 ma = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c);
           const float4 mb = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c + 4);
           const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+          const float4 sa = *reinterpret_cast<const float4*>(qsc + 32 * half + 8 * c);
+          const float4 sbb = *reinterpret_cast<const float4*>(qsc + 32 * half + 8 * c + 4);
+          const float ss[8] = {sa.x, sa.y, sa.z, sa.w, sbb.x, sbb.y, sbb.z, sbb.w};
           uint32_t w[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int h = 8 * c + 2 * k;
-            const float p0 = valid ? ex2(__uint_as_float(sr[h]) * p.scale_log2 - mm[2 * k]) : 0.0f;
-            const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * p.scale_log2 - mm[2 * k + 1]) : 0.0f;
+            const float p0 = valid ? ex2(__uint_as_float(sr[h]) * ss[2 * k] - mm[2 * k]) : 0.0f;
+            const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * ss[2 * k + 1] - mm[2 * k + 1]) : 0.0f;
             over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
             w[k] = f2_to_h2(p0, p1);
           }
@@ -654,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           tc::wait_ld();
           float v[32];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+          for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(sr[h]) * qsc[32 * half + h] : -INFINITY;
 #pragma unroll
           for (int n = 16, o = 16; n >= 1; n >>= 1, o >>= 1) {
             const bool up = (lane & o) != 0;
@@ -713,8 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
             for (int k = 0; k < 4; ++k) {
               const int h = 8 * c + 2 * k;
               const float m0 = msh[32 * half + h], m1 = msh[32 * half + h + 1];
-              const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h]) * p.scale_log2 - m0);
-              const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h + 1]) * p.scale_log2 - m1);
+              const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h]) * qsc[32 * half + h] - m0);
+              const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h + 1]) * qsc[32 * half + h + 1] - m1);
               w[k] = f2_to_h2(p0, p1);
             }
             const int pc = 4 * half + c;

@@ -285,10 +285,14 @@ csa_status csa_index_topk_static(int64_t batch, const csa_index_args* args, int3
  * Duplicates between the cache and the window are not removed. A query with no rows gets out = 0 and
  * lse = -inf.
  *
- * Precision (library choice): cache rows are dequantized exactly (E2M1 x E4M3 products fit fp16); q and
- * window rows are converted from bf16 to fp16 (exact for 2^-14 <= |x| <= 65504; smaller magnitudes lose
- * at most 2^-25 absolute; larger ones overflow, so |q|, |window| must stay below 65504); products are
- * accumulated in fp32, probabilities are rounded to fp16 for the value product, sums are fp32.
+ * Precision (library choice): cache rows are dequantized exactly (E2M1 x E4M3 products fit fp16). Each
+ * head of q is scaled by the power of two that puts its largest magnitude in [2^14, 2^15) and converted
+ * to fp16, exactly for any finite bf16 query (elements more than 2^28 below the head's largest lose bits),
+ * the factor going into that head's softmax scale. Window rows are converted from bf16 to fp16 (exact for
+ * 2^-14 <= |x| <= 65504; smaller magnitudes lose at most 2^-25 absolute); a window value beyond 65504
+ * is outside the contract and is reported as CSA_ERR_DEVICE_CHECK (the outputs of that query are then
+ * undefined). Products are accumulated in fp32, probabilities are rounded to fp16 for the value product,
+ * sums are fp32.
  *
  * Causal and independent queries. csa_sparse_attn_prefill is the causal multi-query call: query j of
  * sequence b sits at token q_pos[b][j] and sees only what exists at that position. It serves prefill

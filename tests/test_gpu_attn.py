@@ -317,3 +317,43 @@ def test_bounded_wait_gives_up_and_the_context_survives(csa):
         entries = o_fp4.dequantize(o_fp4.pack(xf[b], 2, "amax", n_blocks=-(-E // 8)), 512, E)
         ref, _ = o_attn.decode_attention(qf[b, 0].astype(np.float64), entries, E, np.arange(K), np.zeros((0, 512)), SCALE)
         assert_attn_close(o[b, 0], ref, f"seq {b} after the timeout")
+
+
+def test_queries_beyond_fp16_range_and_window_overflow(csa):
+    # Queries of any finite bf16 magnitude: heads 0-15 up to ~1e5 (beyond fp16), heads 16-31 around 1e-6
+    # (fp16 subnormals), the rest N(0, 1); every head matches the fp64 oracle. A window value beyond the
+    # fp16 range is outside the call's contract and is reported as a device check.
+    g = torch.Generator(device=DEV).manual_seed(62)
+    B, T, H, K, W = 2, 2 * 700, 64, 32, 128
+    E = T // 2
+    x = _latents(g, B, T)
+    q = torch.randn(B, 1, H, 512, generator=g, device=DEV)
+    q[:, :, :16] *= 3.0e4
+    q[:, :, 16:32] *= 1.0e-6
+    q = q.to(torch.bfloat16)
+    swa = torch.randn(B, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa_len = torch.tensor([W, 90], dtype=torch.int32, device=DEV)
+    ws0 = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T] * B, E, 512, 2, csa.SCALE_AMAX, ws0)
+    n_entries = torch.full((B,), E, dtype=torch.int32, device=DEV)
+    rng = np.random.default_rng(62)
+    idx_np = np.stack([rng.choice(-(-E // 8), K, replace=False) for _ in range(B)]).astype(np.int32)[:, None, :]
+    idx = torch.from_numpy(idx_np).to(DEV)
+    out, lse = gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, E, W)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    xf, qf, sf = to_np(x), to_np(q), to_np(swa)
+    assert np.abs(qf[:, :, :16]).max() > 65504
+    for b in range(B):
+        entries = o_fp4.dequantize(o_fp4.pack(xf[b], 2, "amax", n_blocks=-(-E // 8)), 512, E)
+        ref, ref_lse = o_attn.decode_attention(qf[b, 0].astype(np.float64), entries, E, idx_np[b, 0],
+                                               sf[b, :int(swa_len[b])], SCALE)
+        assert_attn_close(out[b, 0], ref, f"seq {b}")
+        # lse grows with |q|: compare it relative to its size for the large heads
+        np.testing.assert_allclose(lse[b, 0], ref_lse, rtol=1e-5, atol=2e-3)
+    swa[1, 5, 100] = 1.0e5
+    bad = torch.empty(B, 1, H, 512, device=DEV)
+    args = csa.attn_args(q, cache, n_entries, idx, bad, max_entries=E, window=W, scale=SCALE, swa=swa, swa_len=swa_len)
+    ws = csa.workspace(csa.sparse_attn_workspace_size(B, args), DEV)
+    csa.sparse_attn_decode(q, cache, n_entries, idx, bad, max_entries=E, window=W, scale=SCALE, ws=ws, swa=swa,
+                           swa_len=swa_len)
+    assert csa.device_status(ws) == csa.ERR_DEVICE_CHECK
