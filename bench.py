@@ -123,6 +123,10 @@ class DecodeWorkload:
         ia = csa.index_args(self.q_idx[0], kcache, self.n_entries, self.idx[0], max_entries=E, top_k=K,
                             coarse_sum=coarse, keep_blocks=case.hier_keep, q_pos=self.q_pos)
         self.ws_index = csa.workspace(csa.index_topk_workspace_size(B, ia), device)
+        # one pair of templates per cache replica (their pointers are the only per-replica fields)
+        self.index_tmpl = [csa.index_args(self.q_idx[0], self.kcaches[r], self.n_entries, self.idx[0], max_entries=E,
+                                          top_k=K, coarse_sum=self.coarses[r], keep_blocks=case.hier_keep,
+                                          q_pos=self.q_pos) for r in range(replicas)]
         if self.causal:
             aa = csa.attn_args(self.q[0], cache, self.n_entries, self.idx[0], self.out, max_entries=E,
                                window=case.window, scale=SCALE, swa=self.swa[0], swa_first_pos=self.swa_first_pos,
@@ -131,6 +135,15 @@ class DecodeWorkload:
             aa = csa.attn_args(self.q[0], cache, self.n_entries, self.idx[0], self.out, max_entries=E,
                                window=case.window, scale=SCALE, swa=self.swa[0], swa_len=self.swa_len)
         self.ws_attn = csa.workspace(csa.sparse_attn_workspace_size(B, aa), device)
+        if self.causal:
+            self.attn_tmpl = [csa.attn_args(self.q[0], self.caches[r], self.n_entries, self.idx[0], self.out,
+                                            max_entries=E, window=case.window, scale=SCALE, swa=self.swa[0],
+                                            swa_first_pos=self.swa_first_pos, q_pos=self.q_pos)
+                              for r in range(replicas)]
+        else:
+            self.attn_tmpl = [csa.attn_args(self.q[0], self.caches[r], self.n_entries, self.idx[0], self.out,
+                                            max_entries=E, window=case.window, scale=SCALE, swa=self.swa[0],
+                                            swa_len=self.swa_len) for r in range(replicas)]
         self.ws_pack = ws
         self.queries_per_step = B * case.n_query
 
@@ -149,24 +162,18 @@ class DecodeWorkload:
             (new_tokens, cache, dict(merge=2, scale_rule=csa.SCALE_AMAX, max_entries=self.E, first_entry=self.first)),
             (new_keys, kcache, dict(merge=1, scale_rule=csa.SCALE_POW2, max_entries=self.E, first_entry=self.first,
                                     coarse_sum=coarse))], ws=self.ws_pack)
-        src, n_idx = 0, 0
+        # every layer (indexer for Full / Reindex, attention) through the library's multi-layer entry point
+        layers, n_idx = [], 0
         for layer, mode in enumerate(self.modes):
+            ent = {"mode": mode, "q": q[layer], "swa": self.swa[layer],
+                   "out": out if layer_outs is None else layer_outs[layer]}
             if mode != "reuse":
-                src = n_idx
-                csa.index_topk(q_idx[n_idx % q_idx.shape[0]], kcache, self.n_entries, self.idx[src],
-                               max_entries=self.E, top_k=c.top_k, ws=self.ws_index, coarse_sum=coarse,
-                               keep_blocks=c.hier_keep, q_pos=self.q_pos)
+                ent["q_idx"] = q_idx[n_idx % q_idx.shape[0]]
+                ent["idx"] = self.idx[n_idx]
                 n_idx += 1
-            o = out if layer_outs is None else layer_outs[layer]
-            if self.causal:
-                # draft positions: each sees the entries and window rows at or before its own token
-                csa.sparse_attn_prefill(q[layer], cache, self.n_entries, self.idx[src], o, q_pos=self.q_pos,
-                                        max_entries=self.E, window=c.window, scale=SCALE, ws=self.ws_attn,
-                                        swa=self.swa[layer], swa_first_pos=self.swa_first_pos)
-            else:
-                csa.sparse_attn_decode(q[layer], cache, self.n_entries, self.idx[src], o, max_entries=self.E,
-                                       window=c.window, scale=SCALE, ws=self.ws_attn, swa=self.swa[layer],
-                                       swa_len=self.swa_len)
+            layers.append(ent)
+        csa.decode_layers(layers, index_tmpl=self.index_tmpl[r], attn_tmpl=self.attn_tmpl[r], ws_index=self.ws_index,
+                          ws_attn=self.ws_attn)
         return out
 
     def algorithmic_bytes(self):

@@ -62,6 +62,12 @@ class AttnArgs(ctypes.Structure):
                 ("out_lse", ctypes.c_void_p)]
 
 
+class LayerArgs(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("q_idx", ctypes.c_void_p),
+                ("idx", ctypes.c_void_p), ("q", ctypes.c_void_p), ("swa", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("out_lse", ctypes.c_void_p)]
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
@@ -104,6 +110,9 @@ def lib():
             f = getattr(L, name)
             f.restype = I32
             f.argtypes = [I64, ctypes.POINTER(AttnArgs), P, SZ, P]
+        L.csa_decode_layers.restype = I32
+        L.csa_decode_layers.argtypes = [I64, I32, ctypes.POINTER(LayerArgs), ctypes.POINTER(IndexArgs),
+                                        ctypes.POINTER(AttnArgs), P, SZ, P, SZ, P]
         L.csa_debug_set_fault.restype = I32
         L.csa_debug_set_fault.argtypes = [I32, ctypes.c_uint32]
         L.csa_profile_begin.restype = I32
@@ -354,6 +363,33 @@ def sparse_attn_prefill(q, cache, n_entries, idx, out, *, q_pos, max_entries, wi
                   swa_first_pos=swa_first_pos, q_pos=q_pos, out_lse=out_lse)
     _check(lib().csa_sparse_attn_prefill(q.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)),
            "csa_sparse_attn_prefill")
+
+
+LAYER_FULL, LAYER_REINDEX, LAYER_REUSE = 0, 1, 2
+_LAYER_MODES = {"full": LAYER_FULL, "reindex": LAYER_REINDEX, "reuse": LAYER_REUSE}
+
+
+def decode_layers(layers, *, index_tmpl, attn_tmpl, ws_index, ws_attn, stream=None):
+    """csa_decode_layers: a step of several layers over one cache. layers: list of dicts with keys mode
+    ("full" | "reindex" | "reuse"), q_idx and idx (Full / Reindex), q, swa (or None), out, out_lse (or
+    None). index_tmpl / attn_tmpl: IndexArgs / AttnArgs (from index_args / attn_args) holding the shared
+    fields; a set q_pos in attn_tmpl makes the attention causal. The batch is taken from the first layer's q."""
+    n = len(layers)
+    arr = (LayerArgs * n)()
+    for i, layer in enumerate(layers):
+        arr[i].mode = _LAYER_MODES[layer["mode"]]
+        if layer["mode"] != "reuse":
+            arr[i].q_idx = _need(layer["q_idx"], "q_idx", torch.float32).data_ptr()
+            arr[i].idx = _need(layer["idx"], "idx", torch.int32).data_ptr()
+        arr[i].q = _need(layer["q"], "q", torch.bfloat16).data_ptr()
+        arr[i].swa = None if layer.get("swa") is None else _need(layer["swa"], "swa", torch.bfloat16).data_ptr()
+        arr[i].out = _need(layer["out"], "out", torch.float32).data_ptr()
+        arr[i].out_lse = None if layer.get("out_lse") is None else _need(layer["out_lse"], "out_lse",
+                                                                         torch.float32).data_ptr()
+    batch = layers[0]["q"].shape[0]
+    _check(lib().csa_decode_layers(batch, n, arr, ctypes.byref(index_tmpl), ctypes.byref(attn_tmpl), _ptr(ws_index),
+                                   ws_index.numel(), _ptr(ws_attn), ws_attn.numel(), _stream(stream)),
+           "csa_decode_layers")
 
 
 # ------------------------------------------------------------------------------------------------

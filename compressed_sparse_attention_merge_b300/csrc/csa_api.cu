@@ -502,6 +502,66 @@ csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* a, void* 
 }
 
 // ------------------------------------------------------------------------------------------------
+csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* layers,
+                             const csa_index_args* index_tmpl, const csa_attn_args* attn_tmpl, void* ws_index,
+                             size_t ws_index_bytes, void* ws_attn, size_t ws_attn_bytes, cudaStream_t stream) {
+  if (n_layers < 1 || layers == nullptr || index_tmpl == nullptr || attn_tmpl == nullptr || batch < 0)
+    return CSA_ERR_INVALID_ARG;
+  const bool causal = attn_tmpl->q_pos != nullptr;
+  // every layer's calls are validated before the first launch
+  int32_t* src = nullptr;
+  for (int l = 0; l < n_layers; ++l) {
+    const csa_layer_args& L = layers[l];
+    if (L.mode != CSA_LAYER_FULL && L.mode != CSA_LAYER_REINDEX && L.mode != CSA_LAYER_REUSE) return CSA_ERR_INVALID_ARG;
+    if (L.mode == CSA_LAYER_REUSE && src == nullptr) return CSA_ERR_INVALID_ARG;
+    if (L.mode != CSA_LAYER_REUSE) {
+      csa_index_args ia = *index_tmpl;
+      ia.q_idx = L.q_idx;
+      ia.out_idx = L.idx;
+      ia.out_block_scores = nullptr;
+      csa_status st = validate_index_args(batch, &ia);
+      if (st != CSA_OK) return st;
+      if (batch > 0) {
+        st = check_ws(ws_index, ws_index_bytes, index_layout(batch, &ia).total);
+        if (st != CSA_OK) return st;
+      }
+      src = L.idx;
+    }
+    csa_attn_args aa = *attn_tmpl;
+    aa.q = L.q;
+    aa.idx = src;
+    aa.swa = L.swa;
+    aa.out = L.out;
+    aa.out_lse = L.out_lse;
+    csa_status st = validate_attn(batch, &aa, causal);
+    if (st != CSA_OK) return st;
+  }
+  src = nullptr;
+  for (int l = 0; l < n_layers; ++l) {
+    const csa_layer_args& L = layers[l];
+    if (L.mode != CSA_LAYER_REUSE) {
+      csa_index_args ia = *index_tmpl;
+      ia.q_idx = L.q_idx;
+      ia.out_idx = L.idx;
+      ia.out_block_scores = nullptr;
+      const csa_status st = csa_index_topk(batch, &ia, ws_index, ws_index_bytes, stream);
+      if (st != CSA_OK) return st;
+      src = L.idx;
+    }
+    csa_attn_args aa = *attn_tmpl;
+    aa.q = L.q;
+    aa.idx = src;
+    aa.swa = L.swa;
+    aa.out = L.out;
+    aa.out_lse = L.out_lse;
+    const csa_status st = causal ? csa_sparse_attn_prefill(batch, &aa, ws_attn, ws_attn_bytes, stream)
+                                 : csa_sparse_attn_decode(batch, &aa, ws_attn, ws_attn_bytes, stream);
+    if (st != CSA_OK) return st;
+  }
+  return CSA_OK;
+}
+
+// ------------------------------------------------------------------------------------------------
 csa_status csa_debug_set_fault(int fault, uint32_t spin_limit) {
   if (fault != CSA_FAULT_NONE && fault != CSA_FAULT_WITHHOLD_ARRIVAL) return CSA_ERR_INVALID_ARG;
   if (fault != CSA_FAULT_NONE && spin_limit == 0) return CSA_ERR_INVALID_ARG;

@@ -353,6 +353,43 @@ csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* args, voi
                                    cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * csa_decode_layers -- a step of several layers over one shared cache: for every layer in order, the
+ * indexer (Full and Reindex layers) and the sparse attention.
+ *
+ * Follows [card] Key ideas, "CSA2 with three static layer modes": a Full layer makes the global KV and
+ * the index, a Reindex layer reuses the KV but rescores with its own indexer query, a Reuse layer reuses
+ * both the KV and the Top-K indices; "Every layer keeps its own query and sliding-window KV".
+ *
+ * index_tmpl and attn_tmpl hold everything the layers share (keys, entry counts, Top-K size, flags,
+ * hierarchical keys, cache, window lengths, scale, heads, and q_pos for causal positions); their per-layer
+ * pointers (q_idx, out_idx; q, idx, swa, out, out_lse) are ignored and taken from layers[l]:
+ *   CSA_LAYER_FULL / CSA_LAYER_REINDEX: csa_index_topk with q_idx into idx, then attention over idx;
+ *   CSA_LAYER_REUSE: attention over the idx of the most recent Full or Reindex layer (layers[l].q_idx and
+ *                    layers[l].idx are ignored).
+ * Attention runs as csa_sparse_attn_prefill when attn_tmpl->q_pos is set (causal positions, e.g. the
+ * draft tokens of a multi-token decode step) and as csa_sparse_attn_decode otherwise.
+ * ws_index and ws_attn are sized by csa_index_topk_workspace_size / csa_sparse_attn_workspace_size for the
+ * templates; they are reused by every layer, in order, on `stream`. Every layer is validated before
+ * anything is launched; the first layer may not be a Reuse layer.
+ * ------------------------------------------------------------------------------------------------ */
+enum { CSA_LAYER_FULL = 0, CSA_LAYER_REINDEX = 1, CSA_LAYER_REUSE = 2 };
+
+typedef struct csa_layer_args {
+  int32_t mode;
+  int32_t reserved0;
+  const float* q_idx;   /* indexer queries [batch][n_query][heads][dim] (Full / Reindex) */
+  int32_t* idx;         /* Top-K output [batch][n_query][top_k] (Full / Reindex) */
+  const void* q;        /* attention queries, bf16 [batch][n_query][heads][512] */
+  const void* swa;      /* this layer's window rows (layout of csa_attn_args.swa), or NULL if window = 0 */
+  float* out;           /* [batch][n_query][heads][512] */
+  float* out_lse;       /* [batch][n_query][heads] or NULL */
+} csa_layer_args;
+
+csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* layers,
+                             const csa_index_args* index_tmpl, const csa_attn_args* attn_tmpl, void* ws_index,
+                             size_t ws_index_bytes, void* ws_attn, size_t ws_attn_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
  * csa_debug_set_fault -- test-only fault injection for the device-side failure path.
  *
  * Every wait inside the library's kernels is bounded: after a fixed number of polls it gives up, records

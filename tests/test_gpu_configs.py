@@ -178,3 +178,51 @@ def test_prefill_2048_at_128k():
         win = o_attn.prefill_window(swa, first, p, c.window)
         want, _ = o_attn.attend(to_np(d["q"][0, j]).astype(np.float64), np.concatenate([rows, win]), SCALE)
         assert_attn_close(out[j], want, f"prefill position {p}")
+
+
+def test_chain_step_as_one_graph_replays_the_eager_step():
+    # the 20-layer chain through the library's multi-layer entry point (csa_decode_layers) at a smaller size
+    # (4 sequences of 8K tokens): captured once as a CUDA graph and replayed, it reproduces the eager step bit
+    # for bit, and sampled layers match the oracle (Reuse layers with their source layer's indices)
+    import dataclasses
+    from compressed_sparse_attention_merge_b300 import synth
+    case = dataclasses.replace(synth.CHAIN_128K_B64, name="chain20_8k_b4", tokens=[8192] * 4, seed=20299)
+    w = bench.DecodeWorkload(case, torch.device(DEV), replicas=1, keep_inputs=True)
+    L = len(w.modes)
+    eager = [torch.empty_like(w.out) for _ in range(L)]
+    graphed = [torch.full_like(w.out, float("nan")) for _ in range(L)]
+    w.step(0, layer_outs=eager)
+    torch.cuda.synchronize()
+    idx_eager = [t.clone() for t in w.idx]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        w.step(0, layer_outs=graphed)
+    for t in w.idx:
+        t.fill_(-9)
+    g.replay()
+    torch.cuda.synchronize()
+    assert w.csa.device_status(w.ws_attn) == w.csa.OK and w.csa.device_status(w.ws_index) == w.csa.OK
+    for layer in range(L):
+        assert torch.equal(graphed[layer], eager[layer]), f"layer {layer}"
+    for a, b in zip(w.idx, idx_eager):
+        assert torch.equal(a, b)
+    d = w.inputs
+    E, b = w.E, 1
+    tok = d["tokens"][b]
+    keys = d["keys"][b].cpu().numpy().astype(np.float64)
+    n_idx, src, ref_idx = 0, 0, {}
+    sources = []
+    for layer, mode in enumerate(w.modes):
+        if mode != "reuse":
+            src = n_idx
+            ref, _ = o_idx.flat_topk(d["q_idx"][n_idx % d["q_idx"].shape[0], b].cpu().numpy(), keys, E, case.top_k)
+            np.testing.assert_array_equal(w.idx[src][b].cpu().numpy(), ref, err_msg=f"layer {layer}")
+            ref_idx[src] = ref
+            n_idx += 1
+        sources.append(src)
+    for layer in (0, 1, 4, 5, 19):
+        ref = ref_idx[sources[layer]]
+        rows = _oracle_rows(tok, ref[0], lambda e: e < E)
+        swa = to_np(d["swa"][layer, b])[:int(d["swa_len"][b])].astype(np.float64)
+        want, _ = o_attn.attend(to_np(d["q"][layer, b, 0]).astype(np.float64), np.concatenate([rows, swa]), SCALE)
+        assert_attn_close(graphed[layer][b, 0].cpu().numpy(), want, f"layer {layer} ({w.modes[layer]})")
