@@ -14,9 +14,10 @@
 // S and O accumulate in tensor memory; the row sums l are added up by one warp from the fp16
 // probabilities in shared memory (the same values the tensor core multiplies).
 //   Every tile is dequantised once. Eight converter warps (thread = tensor-memory lane = tile row) read
-//   their row's FP4 codes and scales straight from global memory (the gather warp prefetches the CTA's
-//   blocks into L2 at the start, and each converter loads the next tile's bytes into registers while it
-//   works on the current one), convert a 64-column panel to fp16 and write it twice: into the logits
+//   their row's FP4 codes and scales straight from global memory (the gather warp prefetches each cache
+//   tile's blocks into L2 three tiles ahead; a converter keeps the codes of its next two panels in flight in
+//   registers, one 32-byte load each, and loads a tile's scale bytes once), convert a 64-column panel to
+//   fp16 and write it twice: into the logits
 //   operand ring in tensor memory, and into the values buffer in shared memory, a whole tile of C^T in the
 //   128-byte-swizzled MN-major layout, recycled per 128-latent chunk as the value products finish with it.
 //   Window tiles come first: their bf16 rows are copied by tensor map straight into the values buffer and
@@ -64,8 +65,8 @@ constexpr int kPOff = kVOff + kChunks * kChunkBytes;       // 196,608: two P^T b
 constexpr int kBarOff = kPOff + 2 * kPBytes;               // 229,376
 constexpr int kNumBars = 32;
 constexpr int kTmemPtrOff = kBarOff + kNumBars * 8;
-constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], int abort, int have
-constexpr int kMOff = kFlagOff + 16;                       // float m[64]
+constexpr int kFlagOff = kTmemPtrOff + 16;                 // int flag[2], abort, have, progress
+constexpr int kMOff = kFlagOff + 32;                       // float m[64]
 constexpr int kAlphaOff = kMOff + 64 * 4;                  // float alpha[2][64]: per P buffer
 constexpr int kRedOff = kAlphaOff + 2 * 64 * 4;            // float red[4][64]
 constexpr int kLsumOff = kRedOff + 4 * 64 * 4;             // float lsum[64]: final row sums
@@ -236,19 +237,44 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t* h) {
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
 }
 
-// One 64-column panel of a cache row: 32 code bytes (a, b) and 4 scale bytes (sc) -> 32 f16x2, exact.
+// One 64-column panel of a cache row: 32 code bytes (w) and 4 scale bytes (sc) -> 32 f16x2, exact.
 // Zero codes and a zero scale (rows that are not attended) give exact zeros.
-__device__ __forceinline__ void dequant_panel(const uint4& a, const uint4& b, uint32_t sc, uint32_t* h) {
-  e2m1x8_to_f16x8(a.x, h);      e2m1x8_to_f16x8(a.y, h + 4);
-  e2m1x8_to_f16x8(a.z, h + 8);  e2m1x8_to_f16x8(a.w, h + 12);
-  e2m1x8_to_f16x8(b.x, h + 16); e2m1x8_to_f16x8(b.y, h + 20);
-  e2m1x8_to_f16x8(b.z, h + 24); e2m1x8_to_f16x8(b.w, h + 28);
+__device__ __forceinline__ void dequant_panel(const uint32_t* w, uint32_t sc, uint32_t* h) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e2m1x8_to_f16x8(w[i], h + 4 * i);
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const uint32_t s2 = e4m3_to_f16x2_bcast((sc >> (8 * g)) & 0xFFu);
 #pragma unroll
     for (int k = 0; k < 8; ++k) h[8 * g + k] = hmul2_u32(h[8 * g + k], s2);
   }
+}
+
+// 32 bytes (one sector) of read-only global memory in one 256-bit load; p must be 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const void* ptr, uint32_t* r) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "l"(ptr));
+}
+
+// 16 bytes of read-only global memory (a volatile load: issued where written and never repeated).
+__device__ __forceinline__ uint4 ld_nc_v4(const void* ptr) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(ptr));
+  return r;
+}
+
+// The scale words of the four panels of parity hp (panels hp, hp + 2, hp + 4, hp + 6) of one cache row:
+// one 256-bit load of the row's 32 scale bytes; zeros for a row that is not attended.
+__device__ __forceinline__ void load_scales(const uint8_t* seq, int id, bool ok, int row, int hp, uint32_t* sc) {
+  uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  if (ok) ld_nc_v8(seq + (int64_t)id * kLatBlk + 2048 + (row & 7) * 32, w);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sc[c] = hp ? w[2 * c + 1] : w[2 * c];
+}
+
+__device__ __forceinline__ uint32_t pick4(const uint32_t* v, int i) {
+  return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p,
@@ -321,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     mbar_init(&bars[FIN_L], 1);
     mbar_init(&bars[FIN_V], 1);
     fence_mbar_init();
-    flag[0] = 0; flag[1] = 0; *abort_flag = 0; flag[3] = 0;
+    flag[0] = 0; flag[1] = 0; *abort_flag = 0; flag[3] = 0; flag[4] = -1;
     for (int h = 0; h < 64; ++h) reinterpret_cast<uint32_t*>(smem + kQMaxOff)[h] = 0u;
   }
   tc::fence_before();
@@ -333,30 +359,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   // The first window tile lands in the values buffer while the queries are loaded.
   if (warp == kGatherWarp && lane == 0 && nw > 0) copy_window_tile(p, u, 0, smem, &swa_map, &bars[WIN_FULL]);
 
-  // Converters: their rows' block ids of the first two cache tiles and the raw bytes of the first two panels,
-  // so that these loads are in flight during the query load. The raw bytes of the next two panels a
-  // converter handles form a queue in registers (q0 is the next panel to convert): each step converts q0,
-  // shifts the queue and loads the panel two steps ahead into q1 (the same tile's chunk c + 2, or the next
-  // cache tile's chunk c - 2).
+  // Converters: their rows' block ids of the first three cache tiles, the scales of the first two and the
+  // codes of the first two panels, so that these loads are in flight during the query load. The codes of the
+  // next two panels a converter handles form a queue in registers (q0 is the next to convert): each
+  // conversion shifts the queue and loads the panel two places further on (the same tile's chunk c + 2, or
+  // the next cache tile's chunk c - 2).
   const bool is_conv = warp >= kConv0 && warp < kConv0 + kConvWarps;
   const int sp = warp & 3;                         // tensor-memory subpartition of this warp
   const int hp = (warp - kConv0) >> 2;             // converters: panel parity
   const int row = sp * 32 + lane;                  // converters and softmax: tile row = tensor-memory lane
-  uint4 qa0 = make_uint4(0, 0, 0, 0), qa1 = qa0, qb0 = qa0, qb1 = qa0;
-  uint32_t qs0 = 0, qs1 = 0;
-  int64_t id_cur = -1, id_nxt = -1;
-  bool v_cur = false;
+  uint32_t q0[8], q1[8], qs0 = 0u, qs1 = 0u;
+  uint32_t sc_c[4] = {0u, 0u, 0u, 0u}, sc_n[4] = {0u, 0u, 0u, 0u};   // scale words of cache tiles 0 and 1
+  int id_c = -1, id_n = -1, id_nn = -1;            // block ids of cache tiles 0, 1 and 2 for this row
+#pragma unroll
+  for (int i = 0; i < 8; ++i) { q0[i] = 0u; q1[i] = 0u; }
   if (is_conv) {
-    id_cur = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
-    id_nxt = n_cache > 1 ? cache_id(p, u, c0 + 1, row) : -1;
-    v_cur = n_cache > 0 && cache_ok(u, id_cur, row);
-    if (v_cur) {
-      const uint8_t* e = seq + id_cur * kLatBlk + (row & 7) * 256 + hp * 32;
-      const uint32_t* sc = reinterpret_cast<const uint32_t*>(seq + id_cur * kLatBlk + 2048 + (row & 7) * 32 + hp * 4);
-      qa0 = __ldg(reinterpret_cast<const uint4*>(e));       qb0 = __ldg(reinterpret_cast<const uint4*>(e + 16));
-      qa1 = __ldg(reinterpret_cast<const uint4*>(e + 64));  qb1 = __ldg(reinterpret_cast<const uint4*>(e + 80));
-      qs0 = __ldg(sc); qs1 = __ldg(sc + 2);
+    id_c = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
+    id_n = n_cache > 1 ? cache_id(p, u, c0 + 1, row) : -1;
+    id_nn = n_cache > 2 ? cache_id(p, u, c0 + 2, row) : -1;
+    const bool ok0 = n_cache > 0 && cache_ok(u, id_c, row);
+    if (ok0) {
+      const uint8_t* e = seq + (int64_t)id_c * kLatBlk + (row & 7) * 256 + hp * 32;
+      ld_nc_v8(e, q0);
+      ld_nc_v8(e + 64, q1);
     }
+    load_scales(seq, id_c, ok0, row, hp, sc_c);
+    load_scales(seq, id_n, n_cache > 1 && cache_ok(u, id_n, row), row, hp, sc_n);
+    qs0 = sc_c[0];
+    qs1 = sc_c[1];
   }
 
   if (warp != kGatherWarp) {
@@ -367,6 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     constexpr int kQThreads = kThreads - 32;
     constexpr int kQItems = kHeadsPad * 64;
     constexpr int kQPer = (kQItems + kQThreads - 1) / kQThreads;
+    static_assert(kQThreads % 32 == 0 && kQItems % 32 == 0, "one head per warp and item batch");
     const int qt = tid < kGatherWarp * 32 ? tid : tid - 32;
     const __nv_bfloat16* qg = p.q + u.unit * (int64_t)H * kLatent;
     uint32_t* qmax = reinterpret_cast<uint32_t*>(smem + kQMaxOff);
@@ -377,18 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       const int i = qt + k * kQThreads;
       const int h = i >> 6, ch = i & 63;
       v[k] = make_uint4(0, 0, 0, 0);
-      if (i < kQItems && h < H) v[k] = __ldg(reinterpret_cast<const uint4*>(qg + (int64_t)h * kLatent + ch * 8));
+      if (i < kQItems && h < H) v[k] = ld_nc_v4(qg + (int64_t)h * kLatent + ch * 8);
     }
 #pragma unroll
     for (int k = 0; k < kQPer; ++k) {
       const int i = qt + k * kQThreads;
       if (i < kQItems) {
         // magnitudes compare as integers: the bits of |x| with the sign cleared
+        // (the 32 lanes of a warp hold 32 consecutive items starting at a multiple of 32, so all lie in one
+        // head's 64 and the warp reduces them before one atomic; the branch is uniform per warp, since
+        // kQItems and kQThreads are multiples of 32)
         uint32_t m = 0u;
         const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
-        atomicMax(qmax + (i >> 6), m);
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) atomicMax(qmax + (i >> 6), m);
       }
     }
     asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
@@ -426,11 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 
   if (warp == kGatherWarp) {
     // ---------------- gather: block-id checks, L2 prefetch, later window tiles ----------------
-    // the blocks of cache tile k go to L2 when the converters start tile k - 2 (tiles 1 and 2 at once; the
-    // converters load tile 0 themselves, so its ids are only checked); lanes 0-15 take one block each
+    // the blocks of cache tile k go to L2 when the converters start tile k - 3 (tiles 1 and 2 at once; the
+    // converters load tile 0 themselves, so its ids are only checked); lanes 0-15 take one block each.
+    // The pacing is a hint: a wait that runs out (or a CTA that gives up) just prefetches at once.
+    volatile int* progress = flag + 4;
     for (int k = 0; k < n_cache; ++k) {
-      const int t = nw + k - 3;           // the tile whose first values chunk paces this prefetch
-      if (t >= 0 && !wait_bar_warp(&bars[V_FULL], t & 1, abort_flag, p.hdr, 16, p.spin_limit)) break;
+      const int target = nw + k - 3;
+      for (uint32_t i = 0; k >= 3 && i < p.spin_limit && *progress < target && !*abort_flag; ++i) __nanosleep(64);
       const int slot = (c0 + k) * kTileBlocks + lane;
       if (lane < kTileBlocks && slot < p.top_k) {
         const int64_t id = __ldg(p.idx + u.unit * p.top_k + slot);
@@ -459,18 +496,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   } else if (is_conv) {
     // ---------------- converters: one 64-column panel of every chunk of every tile ----------------
     const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
+    volatile int* progress = flag + 4;
     bool stop = false;
     for (int it = 0; it < n_tiles && !stop; ++it) {
+      if (warp == kConv0 && lane == 0) *progress = it;
       const bool win = it < nw;
       const int k = it - nw;                       // cache tile index within this CTA
-      bool vr = v_cur;
+      bool vr = false;
       if (win) {
         bool oob;
         vr = window_row(p, u, it, row, &oob);
         if (oob && hp == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
         if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], it & 1, abort_flag, p.hdr, 10, p.spin_limit))) break;
       }
-      const bool v_next = !win && k + 1 < n_cache && cache_ok(u, id_nxt, row);
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
         const int pnl = 2 * c + hp;
@@ -491,53 +529,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           }
           if (inf) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
         } else {
-          dequant_panel(qa0, qb0, qs0, h);
-          // shift the queue; the panel two steps ahead enters at the back
-          qa0 = qa1; qb0 = qb1; qs0 = qs1;
-          qa1 = make_uint4(0, 0, 0, 0); qb1 = qa1; qs1 = 0u;
+          dequant_panel(q0, qs0, h);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) { q0[i] = q1[i]; q1[i] = 0u; }
+          qs0 = qs1;
+          qs1 = 0u;
+          // the panel two places further on enters at the back of the queue
           const bool same = c + 2 < kChunks;
-          if (same ? vr : v_next) {
-            const int64_t id2 = same ? id_cur : id_nxt;
-            const int pnl2 = same ? pnl + 4 : pnl - 4;
-            const uint8_t* e = seq + id2 * kLatBlk + (row & 7) * 256 + pnl2 * 32;
-            qa1 = __ldg(reinterpret_cast<const uint4*>(e));
-            qb1 = __ldg(reinterpret_cast<const uint4*>(e + 16));
-            qs1 = __ldg(reinterpret_cast<const uint32_t*>(seq + id2 * kLatBlk + 2048 + (row & 7) * 32 + pnl2 * 4));
+          const int id2 = same ? id_c : id_n;
+          if (cache_ok(u, id2, row)) {
+            ld_nc_v8(seq + (int64_t)id2 * kLatBlk + (row & 7) * 256 + (same ? pnl + 4 : pnl - 4) * 32, q1);
+            qs1 = same ? pick4(sc_c, c + 2) : pick4(sc_n, c - 2);
           }
         }
-        // logits operand: panel pnl of tile it goes to ring slot pnl & 3 (use 2 it + c / 2 of that slot)
+        // values operand: the chunk must have been consumed by the previous tile's value products (a window
+        // tile's chunks were, before its copy was issued)
+        if (!win && it > 0 &&
+            !__all_sync(0xffffffffu, wait_bar(&bars[V_EMPTY + c], (it - 1) & 1, abort_flag, p.hdr, 6, p.spin_limit))) {
+          stop = true;
+          break;
+        }
+        // logits operand: panel pnl of tile it goes to ring slot pnl & 3, use 2 it + c / 2 of that slot. A slot
+        // written for chunks 0 and 1 was last read by tile it - 1's logits products, which are complete once
+        // that tile's values have freed a chunk (or its window copy has landed): only chunks 2 and 3 wait for
+        // the ring.
         const uint32_t slot = pnl & 3, use = 2u * it + (c >> 1);
-        if (use > 0 && !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (use - 1) & 1u, abort_flag, p.hdr, 3, p.spin_limit))) {
+        if (c >= 2 &&
+            !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (use - 1) & 1u, abort_flag, p.hdr, 3, p.spin_limit))) {
           stop = true;
           break;
         }
         tc::fence_after();
         tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
-        // values operand while the tensor-memory store completes: the chunk must have been consumed by the
-        // previous tile's value products (a window tile's chunks were, before its copy was issued)
-        bool freed = win || it == 0 || __all_sync(0xffffffffu, wait_bar(&bars[V_EMPTY + c], (it - 1) & 1, abort_flag, p.hdr, 6, p.spin_limit));
-        if (freed) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(vrow + ((j ^ (row & 7)) << 4)) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        }
-        tc::wait_st();          // no tensor-memory store may be in flight past this point, even when giving up
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(vrow + ((j ^ (row & 7)) << 4)) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        tc::wait_st();          // no tensor-memory store may be in flight past this point
         tc::fence_before();
         tc::fence_proxy_async();
         __syncwarp();
-        if (!freed) {
-          stop = true;
-          break;
-        }
         if (lane == 0) {
           mbar_arrive(&bars[TRING_FULL + slot]);
           mbar_arrive(&bars[V_FULL + c]);
         }
       }
       if (!win) {
-        id_cur = id_nxt;
-        v_cur = v_next;
-        id_nxt = k + 2 < n_cache ? cache_id(p, u, c0 + k + 2, row) : -1;
+        // the scales of tile k + 2 are loaded a tile before the queue reaches it, its id one more tile earlier
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sc_c[i] = sc_n[i];
+        load_scales(seq, id_nn, k + 2 < n_cache && cache_ok(u, id_nn, row), row, hp, sc_n);
+        id_c = id_n;
+        id_n = id_nn;
+        id_nn = k + 3 < n_cache ? cache_id(p, u, c0 + k + 3, row) : -1;
       }
     }
   } else if (warp == kLogitsWarp) {
@@ -648,46 +691,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       float* al = alpha + 64 * sb;
       const uint32_t s_col = tbase + lane_base + kColS + 64 * sb;
       uint8_t* prow = smem + kPOff + sb * kPBytes + row * 128;
-      // Fast path: probabilities against the current reference maxima, 32 heads at a time, written to row
-      // `row` of P (fp16, MN-major: 64 heads contiguous, 128-byte swizzle); the full path runs, and rewrites
-      // the row, only when a probability would exceed 2^8 (a maximum moved by more than the slack, or none
-      // was set yet).
-      bool over = false;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32];
-        tc::ld_32x32(s_col + 32 * half, sr);
-        tc::wait_ld();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float4 ma = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c);
-          const float4 mb = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c + 4);
-          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-          const float4 sa = *reinterpret_cast<const float4*>(qsc + 32 * half + 8 * c);
-          const float4 sbb = *reinterpret_cast<const float4*>(qsc + 32 * half + 8 * c + 4);
-          const float ss[8] = {sa.x, sa.y, sa.z, sa.w, sbb.x, sbb.y, sbb.z, sbb.w};
-          uint32_t w[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int h = 8 * c + 2 * k;
-            const float p0 = valid ? ex2(__uint_as_float(sr[h]) * ss[2 * k] - mm[2 * k]) : 0.0f;
-            const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * ss[2 * k + 1] - mm[2 * k + 1]) : 0.0f;
-            over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
-            w[k] = f2_to_h2(p0, p1);
-          }
-          const int pc = 4 * half + c;
-          *reinterpret_cast<uint4*>(prow + ((pc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      const bool full = any_softmax(over);
-      if (!full) {
-        // S buffer sb has been read for the last time: the logits of tile it + 2 may overwrite it
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
-      }
+      // Probabilities against the current reference maxima, 32 heads at a time, written to row `row` of P
+      // (fp16, MN-major: 64 heads contiguous, 128-byte swizzle). When a probability would exceed 2^8 (a
+      // maximum moved by more than the slack, or none was set yet), the maxima are raised and the same loop
+      // runs once more; after a raise every probability is at most 2^8, so there is no third pass.
       if (tid == 0) flag[sb] = 0;
-      if (full) {
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        bool over = false;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sr[32];
+          tc::ld_32x32(s_col + 32 * half, sr);
+          tc::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 ma = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c);
+            const float4 mb = *reinterpret_cast<const float4*>(msh + 32 * half + 8 * c + 4);
+            const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+            const float4 sa = *reinterpret_cast<const float4*>(qsc + 32 * half + 8 * c);
+            const float4 sbb = *reinterpret_cast<const float4*>(qsc + 32 * half + 8 * c + 4);
+            const float ss[8] = {sa.x, sa.y, sa.z, sa.w, sbb.x, sbb.y, sbb.z, sbb.w};
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int h = 8 * c + 2 * k;
+              const float p0 = valid ? ex2(__uint_as_float(sr[h]) * ss[2 * k] - mm[2 * k]) : 0.0f;
+              const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * ss[2 * k + 1] - mm[2 * k + 1]) : 0.0f;
+              over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
+              w[k] = f2_to_h2(p0, p1);
+            }
+            const int pc = 4 * half + c;
+            *reinterpret_cast<uint4*>(prow + ((pc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        if (pass == 1 || !any_softmax(over)) break;
         // per-head maximum over the warp's 32 rows, 32 heads at a time, by a transposing reduction: at
         // the step with offset o a lane keeps the half of its values selected by (lane & o) and takes the
         // maximum with its partner's copy of that half, so after five steps lane l holds head 32 half + l
@@ -745,31 +783,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           }
           tc::wait_st();
         }
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sr[32];
-          tc::ld_32x32(s_col + 32 * half, sr);
-          tc::wait_ld();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int h = 8 * c + 2 * k;
-              const float m0 = msh[32 * half + h], m1 = msh[32 * half + h + 1];
-              const float p0 = (!valid || m0 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h]) * qsc[32 * half + h] - m0);
-              const float p1 = (!valid || m1 == -INFINITY) ? 0.0f : ex2(__uint_as_float(sr[h + 1]) * qsc[32 * half + h + 1] - m1);
-              w[k] = f2_to_h2(p0, p1);
-            }
-            const int pc = 4 * half + c;
-            *reinterpret_cast<uint4*>(prow + ((pc ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
-        // the S buffer is released after its last read
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
       }
+      if (!ok) break;
+      // S buffer sb has been read for the last time: the logits of tile it + 2 may overwrite it
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[S_EMPTY + sb]);
       tc::fence_proxy_async();
       tc::fence_before();
       __syncwarp();
@@ -855,8 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 }
 
 // out[u][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, splits in order; lse = (M + log2 L) ln 2.
-// One block per (unit, head), thread = 4 latent columns; the splits are read eight at a time with every
-// load of a batch issued before the first use.
+// One block per (unit, head), thread = 4 latent columns. The splits are read eight at a time, the (m, l)
+// pairs and the o slices of a batch all issued before the first use; a later batch with a larger maximum
+// rescales what the earlier batches added up (at most eight splits need no rescale).
 __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
   constexpr int kBatch = 8;
   const int64_t row = blockIdx.x;                 // unit * H + h
@@ -865,37 +885,37 @@ __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
   const int S = p.splits, H = p.heads;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + unit * S * H + h;
   const float4* po = reinterpret_cast<const float4*>(p.part_o) + (unit * S * H + h) * (int64_t)(kLatent / 4) + threadIdx.x;
-  float M = -INFINITY;
+  float M = -INFINITY, L = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < S; s0 += kBatch) {
     float2 x[kBatch];
+    float4 v[kBatch];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) x[i] = s0 + i < S ? ml[(s0 + i) * H] : make_float2(-INFINITY, 0.0f);
+    for (int i = 0; i < kBatch; ++i) {
+      x[i] = make_float2(-INFINITY, 0.0f);
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + i < S) {
+        x[i] = ml[(s0 + i) * H];
+        v[i] = po[(int64_t)(s0 + i) * H * (kLatent / 4)];
+      }
+    }
+    float Mb = M;
 #pragma unroll
     for (int i = 0; i < kBatch; ++i)
-      if (x[i].y > 0.0f) M = fmaxf(M, x[i].x);
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.0f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < S; s0 += kBatch) {
-      float2 x[kBatch];
-      float4 v[kBatch];
+      if (x[i].y > 0.0f) Mb = fmaxf(Mb, x[i].x);
+    if (Mb == -INFINITY) continue;
+    if (Mb != M && M != -INFINITY) {
+      const float r = exp2f(M - Mb);
+      acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+      L *= r;
+    }
+    M = Mb;
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        x[i] = make_float2(-INFINITY, 0.0f);
-        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s0 + i < S) {
-          x[i] = ml[(s0 + i) * H];
-          v[i] = po[(int64_t)(s0 + i) * H * (kLatent / 4)];
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (!(x[i].y > 0.0f)) continue;
-        const float w = exp2f(x[i].x - M);
-        acc.x += w * v[i].x; acc.y += w * v[i].y; acc.z += w * v[i].z; acc.w += w * v[i].w;
-        L += w * x[i].y;
-      }
+    for (int i = 0; i < kBatch; ++i) {
+      if (!(x[i].y > 0.0f)) continue;
+      const float w = exp2f(x[i].x - M);
+      acc.x += w * v[i].x; acc.y += w * v[i].y; acc.z += w * v[i].z; acc.w += w * v[i].w;
+      L += w * x[i].y;
     }
   }
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;

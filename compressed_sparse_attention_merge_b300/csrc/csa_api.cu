@@ -437,7 +437,7 @@ static csa_status validate_attn(int64_t batch, const csa_attn_args* a, bool pref
   if (batch == 0) return CSA_OK;
   if (a->q == nullptr || a->cache == nullptr || a->n_entries == nullptr || a->idx == nullptr || a->out == nullptr)
     return CSA_ERR_INVALID_ARG;
-  if (!aligned(a->q, 16) || !aligned(a->cache, 16) || a->cache_stride_b % 16 != 0 || !aligned(a->out, 16))
+  if (!aligned(a->q, 16) || !aligned(a->cache, 32) || a->cache_stride_b % 32 != 0 || !aligned(a->out, 16))
     return CSA_ERR_ALIGNMENT;
   if (batch > 1 && a->cache_stride_b < ceil_div(a->max_entries, kBlockEntries) * block_bytes(kLatent))
     return CSA_ERR_INVALID_ARG;

@@ -307,8 +307,8 @@ csa_status csa_index_topk_static(int64_t batch, const csa_index_args* args, int3
  *   n_query   queries per sequence (decode: independent queries over the whole prefix; prefill: causal).
  *   heads     16, 32, 48 or 64.   scale: softmax scale (1/sqrt(512) for the pages' latent).
  *   q         device bf16 [batch][n_query][heads][512], contiguous, 16-byte aligned.
- *   cache     device packed latent cache (csa_pack_fp4, dim 512), 16-byte aligned; stride in bytes,
- *             a multiple of 16.
+ *   cache     device packed latent cache (csa_pack_fp4, dim 512), 32-byte aligned (the kernel reads
+ *             it in 32-byte sectors); stride in bytes, a multiple of 32.
  *   n_entries device int32 [batch]; max_entries bounds it and the block ids.
  *   idx       device int32 [batch][n_query][top_k] block ids (ascending not required; -1 = empty slot).
  *   window    sliding-window length in rows, 0..1024 (the pages use 128).

@@ -121,6 +121,11 @@ def test_misaligned_pointers_rejected_before_any_device_call(lib):
     assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_ALIGNMENT
     aa.out, aa.window, aa.swa, aa.swa_len, aa.swa_rows = good, 128, bad, good, 128
     assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_ALIGNMENT
+    aa.swa, aa.cache = good, good + 16                   # 16-byte aligned is not enough for the latent cache
+    assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_ALIGNMENT
+    aa.cache, aa.cache_stride_b = good, 2304 * 8 + 16    # nor a stride that is not a multiple of 32
+    assert lib.csa_sparse_attn_decode(2, ctypes.byref(aa), None, 0, None) == b.ERR_ALIGNMENT
+    aa.cache_stride_b = 0
     # and the argument checks that come first
     aa.swa, aa.window = good, 2048                       # window above 1,024 rows
     assert lib.csa_sparse_attn_decode(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
