@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   if (warp == kGatherWarp && lane == 0 && nw > 0) copy_window_tile(p, u, 0, smem, &swa_map, &bars[WIN_FULL]);
 
   // Converters: their rows' block ids of the first three cache tiles, the scales of the first two and the
-  // codes of the first two panels, so that these loads are in flight during the query load. The codes of the
+  // codes of the first two panels, loaded as soon as the queries are in shared memory. The codes of the
   // next two panels a converter handles form a queue in registers (q0 is the next to convert): each
   // conversion shifts the queue and loads the panel two places further on (the same tile's chunk c + 2, or
   // the next cache tile's chunk c - 2).
@@ -373,22 +373,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   int id_c = -1, id_n = -1, id_nn = -1;            // block ids of cache tiles 0, 1 and 2 for this row
 #pragma unroll
   for (int i = 0; i < 8; ++i) { q0[i] = 0u; q1[i] = 0u; }
-  if (is_conv) {
-    id_c = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
-    id_n = n_cache > 1 ? cache_id(p, u, c0 + 1, row) : -1;
-    id_nn = n_cache > 2 ? cache_id(p, u, c0 + 2, row) : -1;
-    const bool ok0 = n_cache > 0 && cache_ok(u, id_c, row);
-    if (ok0) {
-      const uint8_t* e = seq + (int64_t)id_c * kLatBlk + (row & 7) * 256 + hp * 32;
-      ld_nc_v8(e, q0);
-      ld_nc_v8(e + 64, q1);
-    }
-    load_scales(seq, id_c, ok0, row, hp, sc_c);
-    load_scales(seq, id_n, n_cache > 1 && cache_ok(u, id_n, row), row, hp, sc_n);
-    qs0 = sc_c[0];
-    qs1 = sc_c[1];
-  }
-
   if (warp != kGatherWarp) {
     // queries: bf16 -> fp16, K-major 128-byte-swizzled panels; heads beyond H are zero. Each head is first
     // scaled by a power of two 2^-k_h that puts its largest magnitude in [2^14, 2^15), so that every
@@ -453,6 +437,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     if (qt < 64) msh[qt] = -INFINITY;
     tc::fence_proxy_async();
     asm volatile("bar.sync 2, %0;" :: "n"(kThreads) : "memory");
+    if (is_conv) {
+      griddep_wait();                                // the index list comes from the kernel before
+      id_c = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
+      id_n = n_cache > 1 ? cache_id(p, u, c0 + 1, row) : -1;
+      id_nn = n_cache > 2 ? cache_id(p, u, c0 + 2, row) : -1;
+      const bool ok0 = n_cache > 0 && cache_ok(u, id_c, row);
+      if (ok0) {
+        const uint8_t* e = seq + (int64_t)id_c * kLatBlk + (row & 7) * 256 + hp * 32;
+        ld_nc_v8(e, q0);
+        ld_nc_v8(e + 64, q1);
+      }
+      load_scales(seq, id_c, ok0, row, hp, sc_c);
+      load_scales(seq, id_n, n_cache > 1 && cache_ok(u, id_n, row), row, hp, sc_n);
+      qs0 = sc_c[0];
+      qs1 = sc_c[1];
+    }
   } else {
     // the gather warp starts its L2 prefetches once the queries have arrived, so that the queries and the
     // first tile's bytes (loaded by the converters) are not queued behind the later tiles
@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 
   if (warp == kGatherWarp) {
     // ---------------- gather: block-id checks, L2 prefetch, later window tiles ----------------
+    griddep_wait();
     // the blocks of cache tile k go to L2 when the converters start tile k - 3 (tiles 1 and 2 at once; the
     // converters load tile 0 themselves, so its ids are only checked); lanes 0-15 take one block each.
     // The pacing is a hint: a wait that runs out (or a CTA that gives up) just prefetches at once.
@@ -670,6 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float* qsc = reinterpret_cast<const float*>(smem + kQScaleOff);
     bool ok = true;
+    griddep_wait();
+    griddep_launch();
     int64_t sid_nxt = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
     for (int it = 0; it < n_tiles; ++it) {
       const int sb = it & 1;
@@ -879,6 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 // rescales what the earlier batches added up (at most eight splits need no rescale).
 __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
   constexpr int kBatch = 8;
+  griddep_wait();                                  // the partials come from the kernel before
+  griddep_launch();
   const int64_t row = blockIdx.x;                 // unit * H + h
   const int64_t unit = row / p.heads;
   const int h = (int)(row % p.heads);
@@ -926,7 +931,7 @@ __global__ void __launch_bounds__(128) combine_kernel(AttnParams p) {
 
 }  // namespace
 
-cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
   if (p.units == 0) return cudaSuccess;
   // window rows as a [batch][swa_rows][512] bf16 tensor, copied in [1 x 128 x 64] boxes with the
   // 128-byte swizzle of the kernel's panels; rows outside the tensor read as zero
@@ -948,16 +953,15 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s) {
   clear_stale_error();
   cudaError_t e = ensure_smem_limit(attn_tc_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<dim3((unsigned)p.splits, (unsigned)p.units), kThreads, kSmemBytes, s>>>(p, map);
-  return cudaGetLastError();
+  return launch_ex(attn_tc_kernel, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads), (size_t)kSmemBytes, s,
+                   pdl, p, map);
 }
 
-cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s, bool pdl) {
   if (p.units == 0 || p.splits == 1) return cudaSuccess;
   ProfScope prof("attn_combine", s);
   clear_stale_error();
-  combine_kernel<<<(unsigned)(p.units * p.heads), 128, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_ex(combine_kernel, dim3((unsigned)(p.units * p.heads)), dim3(128), 0, s, pdl, p);
 }
 
 }  // namespace csa

@@ -174,6 +174,9 @@ cudaError_t ensure_smem_limit_fn(const void* kernel, int bytes) {
   for (const Entry& x : table)
     if (x.fn == kernel && x.dev == dev && x.bytes >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // prefer the largest shared-memory carveout, so that as many CTAs stay resident as the bytes allow
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) table.push_back(Entry{kernel, dev, bytes});
   return e;
 }
@@ -373,7 +376,11 @@ size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* a) {
   return index_layout(batch, a).total;
 }
 
-csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes, cudaStream_t stream) {
+namespace csa {
+// csa_index_topk's launches; `early` makes the first of them a programmatic dependent of the kernel before
+// it in the stream (only for a kernel of the same call of the C ABI, whose outputs these launches wait for).
+static csa_status index_topk_run(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream, bool early) {
   csa_status st = validate_index_args(batch, a);
   if (st != CSA_OK) return st;
   int num_sms = 0;
@@ -396,11 +403,11 @@ csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size
     cp.relu = relu; cp.coarse = a->coarse_sum; cp.coarse_stride_b = a->coarse_stride_b;
     cp.n_entries = a->n_entries; cp.n_super = L.n_super;
     cp.scores = reinterpret_cast<float*>(w + L.coarse_off); cp.batch = batch;
-    if (cudaError_t e = launch_coarse_score(cp, stream)) return cuda_fail(e, "coarse_score");
+    if (cudaError_t e = launch_coarse_score(cp, stream, early)) return cuda_fail(e, "coarse_score");
     TopkParams tk{};
     tk.scores = cp.scores; tk.score_stride = L.n_super; tk.n = L.n_super; tk.k = (int)L.keep_super;
     tk.out = kept; tk.out_stride = L.keep_super; tk.units = L.units; tk.hdr = hdr;
-    if (cudaError_t e = launch_topk(tk, stream)) return cuda_fail(e, "topk");
+    if (cudaError_t e = launch_topk(tk, stream, true)) return cuda_fail(e, "topk");
   }
 
   ScoreParams sp{};
@@ -409,13 +416,13 @@ csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size
   sp.max_entries = a->max_entries; sp.q_pos = a->q_pos;
   sp.kept = hier ? kept : nullptr; sp.keep_super = (int)L.keep_super;
   sp.scores = scores; sp.score_stride = L.n_slots; sp.n_slots = L.n_slots; sp.batch = batch; sp.hdr = hdr;
-  if (cudaError_t e = launch_index_score(sp, num_sms, stream)) return cuda_fail(e, "index_score");
+  if (cudaError_t e = launch_index_score(sp, num_sms, stream, hier || early)) return cuda_fail(e, "index_score");
 
   TopkParams tk{};
   tk.scores = scores; tk.score_stride = L.n_slots; tk.n = L.n_slots; tk.k = a->top_k;
   tk.out = a->out_idx; tk.out_stride = a->top_k; tk.units = L.units; tk.hdr = hdr;
   if (hier) { tk.map_super = kept; tk.map_stride = (int)L.keep_super; }
-  if (cudaError_t e = launch_topk(tk, stream)) return cuda_fail(e, "topk");
+  if (cudaError_t e = launch_topk(tk, stream, true)) return cuda_fail(e, "topk");
 
   if (a->out_block_scores != nullptr && !hier) {
     if (cudaError_t e = cudaMemcpyAsync(a->out_block_scores, scores, (size_t)L.units * L.n_slots * 4,
@@ -423,6 +430,12 @@ csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size
       return cuda_fail(e, "block score copy");
   }
   return CSA_OK;
+}
+}  // namespace csa
+
+extern "C" csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+  return index_topk_run(batch, a, ws, ws_bytes, stream, false);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -458,8 +471,9 @@ size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* a) {
   return attn_layout(batch, a, num_sms).total;
 }
 
+// The attention's launches; `early` as for index_topk_run.
 static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream,
-                              bool prefill) {
+                              bool prefill, bool early) {
   csa_status st = validate_attn(batch, a, prefill);
   if (st != CSA_OK) return st;
   int num_sms = 0;
@@ -486,19 +500,19 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.out = a->out; p.out_lse = a->out_lse;
   p.hdr = reinterpret_cast<uint32_t*>(w);
   debug_fault(&p.fault, &p.spin_limit);
-  if (cudaError_t e = launch_attn(p, stream)) return cuda_fail(e, "attn");
-  if (cudaError_t e = launch_combine(p, stream)) return cuda_fail(e, "combine");
+  if (cudaError_t e = launch_attn(p, stream, early)) return cuda_fail(e, "attn");
+  if (cudaError_t e = launch_combine(p, stream, true)) return cuda_fail(e, "combine");
   return CSA_OK;
 }
 
 csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
                                   cudaStream_t stream) {
-  return sparse_attn(batch, a, ws, ws_bytes, stream, false);
+  return sparse_attn(batch, a, ws, ws_bytes, stream, false, false);
 }
 
 csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
                                    cudaStream_t stream) {
-  return sparse_attn(batch, a, ws, ws_bytes, stream, true);
+  return sparse_attn(batch, a, ws, ws_bytes, stream, true, false);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -544,7 +558,8 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
       ia.q_idx = L.q_idx;
       ia.out_idx = L.idx;
       ia.out_block_scores = nullptr;
-      const csa_status st = csa_index_topk(batch, &ia, ws_index, ws_index_bytes, stream);
+      // every launch after the call's first is a programmatic dependent of the one before it
+      const csa_status st = index_topk_run(batch, &ia, ws_index, ws_index_bytes, stream, l > 0);
       if (st != CSA_OK) return st;
       src = L.idx;
     }
@@ -554,8 +569,7 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
     aa.swa = L.swa;
     aa.out = L.out;
     aa.out_lse = L.out_lse;
-    const csa_status st = causal ? csa_sparse_attn_prefill(batch, &aa, ws_attn, ws_attn_bytes, stream)
-                                 : csa_sparse_attn_decode(batch, &aa, ws_attn, ws_attn_bytes, stream);
+    const csa_status st = sparse_attn(batch, &aa, ws_attn, ws_attn_bytes, stream, causal, true);
     if (st != CSA_OK) return st;
   }
   return CSA_OK;

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -269,16 +270,46 @@ struct AttnParams {
 void debug_fault(int* fault, uint32_t* spin_limit);
 
 // ------------------------------------------------------------------------------------------------
-// Launchers (one per kernel file). Each returns the launch error, if any.
+// Programmatic dependent launch. Within one call of the C ABI, every kernel after the first is launched as
+// a programmatic dependent of the kernel before it: it may start (and run its prologue: tensor-memory
+// allocation, barrier setup, loads of the call's inputs) once every CTA of that kernel has passed
+// griddep_launch(). Each kernel calls griddep_wait() before it reads anything the kernel before it
+// writes, and before it exits; the wait returns once that kernel has completed and its writes are
+// visible. A kernel signals griddep_launch() only after its own wait, so at most two kernels of a call
+// overlap and every earlier one has completed. The first kernel of a call is launched normally: whatever
+// ran before the call has completed when it starts.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launchers (one per kernel file). Each returns the launch error, if any; `pdl` launches the kernel as a
+// programmatic dependent of the kernel before it in the stream (see above).
 // ------------------------------------------------------------------------------------------------
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
 cudaError_t launch_pack_multi(const PackParams* jobs, int n, cudaStream_t s);
 cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s);
-cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s);
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t s);
-cudaError_t launch_attn(const AttnParams& p, cudaStream_t s);
-cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s, bool pdl);
+cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s, bool pdl);
 
 // Clears an error that an earlier runtime call of another component left in this thread's last-error
 // slot without checking it, so that the check after a launch reports that launch alone. A sticky error

@@ -30,7 +30,6 @@ namespace {
 
 constexpr int kStageBlocks = 16;
 constexpr int kStageRows = kStageBlocks * kBlockEntries;     // 128 = M of the product
-constexpr int kStages = 6;
 constexpr int kThreads = 192;                                 // warp 0 copies, 1 MMA, 2-5 scales + epilogue
 
 template <int DI, int N>
@@ -44,6 +43,8 @@ struct Cfg {
   static constexpr int kSwzShift = DI == 64 ? 2 : (DI == 128 ? 1 : 0);
   static constexpr int kSwzMask = DI == 64 ? 1 : (DI == 128 ? 3 : 7);
   static constexpr uint32_t kSbo = 8 * kRowCodes;
+  // copy stages in flight: five at dim 128 (9,216 B each), so that four CTAs fit in one SM's shared memory
+  static constexpr int kStages = DI == 128 ? 5 : 6;
   // shared memory (bytes)
   static constexpr int kCodesOff = 0;
   static constexpr int kScalesOff = kCodesOff + kStages * kCodesStage;
@@ -156,15 +157,17 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
   constexpr uint32_t kIdesc = idesc_mxf4(kStageRows, N);
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* sfr = empty + kStages;
-  uint64_t* dfull = sfr + kStages;              // [kND]
+  uint64_t* empty = full + C::kStages;
+  uint64_t* sfr = empty + C::kStages;
+  uint64_t* dfull = sfr + C::kStages;              // [kND]
   uint64_t* dempty = dfull + 4;                 // [kND]
   uint64_t* fin = dempty + 4;                   // [1]
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(fin + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_ptr + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();                                  // (hierarchical) the kept super-blocks come from the kernel before
+  griddep_launch();
   const bool hier = p.kept != nullptr;
   const int64_t unit = blockIdx.y;
   IdxUnit u;
@@ -190,7 +193,7 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
   // prepare the unit's FP4 queries ----------------
   if (warp == 1) tc::alloc(tmem_ptr, C::kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); mbar_init(&sfr[i], 4); }
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); mbar_init(&sfr[i], 4); }
     for (int i = 0; i < C::kND; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4); }
     mbar_init(fin, 1);
     fence_mbar_init();
@@ -206,8 +209,8 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
     if (lane == 0) {
       int issued = 0;
       for (int k = 0; k < n; ++k) {
-        const int slot = k % kStages;
-        if (k >= kStages && !wait_or_abort(&empty[slot], ((k / kStages) - 1) & 1, abort_flag, p.hdr)) break;
+        const int slot = k % C::kStages;
+        if (k >= C::kStages && !wait_or_abort(&empty[slot], ((k / C::kStages) - 1) & 1, abort_flag, p.hdr)) break;
         const int64_t st = k0 + k;
         int64_t id0 = st * kStageBlocks;
         if (hier) {
@@ -223,8 +226,8 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
         }
         ++issued;
       }
-      for (int k = issued - kStages < 0 ? 0 : issued - kStages; k < issued; ++k)
-        drain(&full[k % kStages], (k / kStages) & 1);
+      for (int k = issued - C::kStages < 0 ? 0 : issued - C::kStages; k < issued; ++k)
+        drain(&full[k % C::kStages], (k / C::kStages) & 1);
     }
   } else {
   constexpr int kSetupThreads = kThreads - 32;
@@ -277,8 +280,8 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
     // ---------------- products ----------------
     if (lane == 0) {
       for (int k = 0; k < n; ++k) {
-        const int slot = k % kStages, db = k % C::kND, sb = k % C::kNSF;
-        if (!wait_or_abort(&sfr[slot], (k / kStages) & 1, abort_flag, p.hdr)) break;
+        const int slot = k % C::kStages, db = k % C::kND, sb = k % C::kNSF;
+        if (!wait_or_abort(&sfr[slot], (k / C::kStages) & 1, abort_flag, p.hdr)) break;
         if (k >= C::kND && !wait_or_abort(&dempty[db], ((k / C::kND) - 1) & 1, abort_flag, p.hdr)) break;
         tc::fence_after();
         const uint32_t a0 = s_base + C::kCodesOff + slot * C::kCodesStage;
@@ -306,8 +309,8 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
     for (int h = 0; h < HI; ++h) w[h] = p.head_w ? __ldg(p.head_w + h) : 1.0f;
     // key scale factors of stage k into scale buffer k % kNSF (lane m, column base + 4 s + m / 32)
     auto write_scales = [&](int k) -> bool {
-      const int slot = k % kStages;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&full[slot], (k / kStages) & 1, abort_flag, p.hdr))) return false;
+      const int slot = k % C::kStages;
+      if (!__all_sync(0xffffffffu, wait_or_abort(&full[slot], (k / C::kStages) & 1, abort_flag, p.hdr))) return false;
       const uint8_t* sc = smem + C::kScalesOff + slot * C::kScalesStage + (m >> 3) * (8 * C::kRowScales) +
                           (m & 7) * C::kRowScales;
 #pragma unroll
@@ -389,6 +392,8 @@ constexpr int kCoarsePerCta = 8 * kCoarsePerWarp;
 __global__ void __launch_bounds__(256) coarse_score_kernel(CoarseScoreParams p) {
   extern __shared__ float xq_sh[];                 // [heads][dim]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  griddep_wait();
+  griddep_launch();
   const int64_t unit = blockIdx.y;
   const int64_t b = unit / p.n_query;
   const int64_t n_e = p.n_entries[b];
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(256) coarse_score_kernel(CoarseScoreParams p) 
 }
 
 template <int DI, int HI, int N>
-cudaError_t launch_tc(const ScoreParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_tc(const ScoreParams& p, int num_sms, cudaStream_t s, bool pdl) {
   using C = Cfg<DI, N>;
   constexpr int NQ = N / HI;
   EncodeTiledFn enc = encode_tiled_fn();
@@ -481,62 +486,66 @@ cudaError_t launch_tc(const ScoreParams& p, int num_sms, cudaStream_t s) {
   const int groups_per_seq = hier ? 1 : (int)((p.n_query + NQ - 1) / NQ);
   const int64_t units = hier ? p.batch * p.n_query : p.batch * groups_per_seq;
   const int64_t spu = (p.n_slots + kStageBlocks - 1) / kStageBlocks;
-  // a few CTAs per SM in total (as many as tensor memory allows), each with a contiguous range of one
-  // unit's stages
-  const int per_sm = (int)(512 / C::kTmemCols) < 4 ? (int)(512 / C::kTmemCols) : 4;
-  int64_t splits = (int64_t)num_sms * per_sm / units;
-  if (splits > spu) splits = spu;
-  if (splits < 1) splits = 1;
+  // one wave: as many CTAs per SM as shared memory, registers and tensor memory let stay resident (at most 4),
+  // each with a contiguous range of one unit's stages
   if (units > 65535) return cudaErrorInvalidValue;
   cudaError_t e = ensure_smem_limit(index_tc_kernel<DI, HI, N>, C::kSmem);
   if (e != cudaSuccess) return e;
+  int dev = 0, smem_sm = 0, reserved = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  const int by_smem = smem_sm / (C::kSmem + reserved);
+  int per_sm = (int)(512 / C::kTmemCols) < 4 ? (int)(512 / C::kTmemCols) : 4;
+  if (by_smem < per_sm) per_sm = by_smem < 1 ? 1 : by_smem;
+  int64_t splits = (int64_t)num_sms * per_sm / units;
+  if (splits > spu) splits = spu;
+  if (splits < 1) splits = 1;
   clear_stale_error();
-  dim3 grid((unsigned)splits, (unsigned)units);
-  index_tc_kernel<DI, HI, N><<<grid, kThreads, C::kSmem, s>>>(p, spu, (int)splits, groups_per_seq, codes_map,
-                                                              scales_map);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)splits, (unsigned)units);
+  return launch_ex(index_tc_kernel<DI, HI, N>, grid, dim3(kThreads), (size_t)C::kSmem, s, pdl, p, spu, (int)splits,
+                   groups_per_seq, codes_map, scales_map);
 }
 
 template <int DI, int HI>
-cudaError_t launch_h(const ScoreParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_h(const ScoreParams& p, int num_sms, cudaStream_t s, bool pdl) {
   // one unit per query group that fits 16 columns (decode), else 64 columns (64 / HI query positions)
-  if (p.kept != nullptr || p.n_query * HI <= 16) return launch_tc<DI, HI, 16>(p, num_sms, s);
-  return launch_tc<DI, HI, 64>(p, num_sms, s);
+  if (p.kept != nullptr || p.n_query * HI <= 16) return launch_tc<DI, HI, 16>(p, num_sms, s, pdl);
+  return launch_tc<DI, HI, 64>(p, num_sms, s, pdl);
 }
 
 template <int DI>
-cudaError_t launch_d(const ScoreParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_d(const ScoreParams& p, int num_sms, cudaStream_t s, bool pdl) {
   switch (p.heads) {
-    case 1: return launch_h<DI, 1>(p, num_sms, s);
-    case 2: return launch_h<DI, 2>(p, num_sms, s);
-    case 4: return launch_h<DI, 4>(p, num_sms, s);
-    case 8: return launch_h<DI, 8>(p, num_sms, s);
+    case 1: return launch_h<DI, 1>(p, num_sms, s, pdl);
+    case 2: return launch_h<DI, 2>(p, num_sms, s, pdl);
+    case 4: return launch_h<DI, 4>(p, num_sms, s, pdl);
+    case 8: return launch_h<DI, 8>(p, num_sms, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s, bool pdl) {
   if (p.n_slots == 0) return cudaSuccess;
   ProfScope prof(p.kept ? "index_score_hier" : "index_score", s);
   switch (p.dim) {
-    case 64: return launch_d<64>(p, num_sms, s);
-    case 128: return launch_d<128>(p, num_sms, s);
-    case 256: return launch_d<256>(p, num_sms, s);
+    case 64: return launch_d<64>(p, num_sms, s, pdl);
+    case 128: return launch_d<128>(p, num_sms, s, pdl);
+    case 256: return launch_d<256>(p, num_sms, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s) {
+cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s, bool pdl) {
   const int64_t units = p.batch * p.n_query;
   if (units == 0 || p.n_super == 0) return cudaSuccess;
   if (units > 65535 || p.dim > 256) return cudaErrorInvalidValue;
   ProfScope prof("coarse_score", s);
   clear_stale_error();
-  dim3 grid((unsigned)((p.n_super + kCoarsePerCta - 1) / kCoarsePerCta), (unsigned)units);
-  coarse_score_kernel<<<grid, 256, (size_t)p.heads * p.dim * sizeof(float), s>>>(p);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)((p.n_super + kCoarsePerCta - 1) / kCoarsePerCta), (unsigned)units);
+  return launch_ex(coarse_score_kernel, grid, dim3(256), (size_t)p.heads * p.dim * sizeof(float), s, pdl, p);
 }
 
 }  // namespace csa

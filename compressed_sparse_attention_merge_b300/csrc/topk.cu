@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkParams p) {
   __shared__ uint32_t hist[256];
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_prefix, s_krem, s_ncand;
+  griddep_wait();                                  // the scores come from the kernel before
+  griddep_launch();
 
   const int64_t unit = blockIdx.x;
   const float* sc = p.scores + unit * p.score_stride;
@@ -151,6 +153,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(TopkParams p)
   __shared__ uint32_t hist[2][256];
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_prefix, s_krem, s_ncand;
+  griddep_wait();                                  // the scores come from the kernel before
+  griddep_launch();
   const int64_t unit = blockIdx.x;
   const float* sc = p.scores + unit * p.score_stride;
   int32_t* out = p.out + unit * p.out_stride;
@@ -281,15 +285,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(TopkParams p)
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkParams& p, cudaStream_t s) {
+cudaError_t launch_topk(const TopkParams& p, cudaStream_t s, bool pdl) {
   if (p.units == 0) return cudaSuccess;
   ProfScope prof("topk", s);
   clear_stale_error();
-  if (p.n <= 4 * kTopkThreads) topk_reg_kernel<4><<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
-  else if (p.n <= 8 * kTopkThreads) topk_reg_kernel<8><<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
-  else if (p.n <= 16 * kTopkThreads) topk_reg_kernel<16><<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
-  else topk_kernel<<<(unsigned)p.units, kTopkThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)p.units), block(kTopkThreads);
+  if (p.n <= 4 * kTopkThreads) return launch_ex(topk_reg_kernel<4>, grid, block, 0, s, pdl, p);
+  if (p.n <= 8 * kTopkThreads) return launch_ex(topk_reg_kernel<8>, grid, block, 0, s, pdl, p);
+  if (p.n <= 16 * kTopkThreads) return launch_ex(topk_reg_kernel<16>, grid, block, 0, s, pdl, p);
+  return launch_ex(topk_kernel, grid, block, 0, s, pdl, p);
 }
 
 }  // namespace csa
