@@ -377,10 +377,11 @@ size_t csa_index_topk_workspace_size(int64_t batch, const csa_index_args* a) {
 }
 
 namespace csa {
-// csa_index_topk's launches; `early` makes the first of them a programmatic dependent of the kernel before
-// it in the stream (only for a kernel of the same call of the C ABI, whose outputs these launches wait for).
+// csa_index_topk's launches, all programmatic dependents: each of its kernels waits for the kernel before it
+// ahead of its first memory access.
 static csa_status index_topk_run(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream, bool early) {
+                                 cudaStream_t stream) {
+  const bool early = true;
   csa_status st = validate_index_args(batch, a);
   if (st != CSA_OK) return st;
   int num_sms = 0;
@@ -435,7 +436,7 @@ static csa_status index_topk_run(int64_t batch, const csa_index_args* a, void* w
 
 extern "C" csa_status csa_index_topk(int64_t batch, const csa_index_args* a, void* ws, size_t ws_bytes,
                                      cudaStream_t stream) {
-  return index_topk_run(batch, a, ws, ws_bytes, stream, false);
+  return index_topk_run(batch, a, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -471,7 +472,9 @@ size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* a) {
   return attn_layout(batch, a, num_sms).total;
 }
 
-// The attention's launches; `early` as for index_topk_run.
+// The attention's launches; `early` makes the attention kernel a programmatic dependent of the kernel before
+// it, which is only right when that kernel belongs to the same call (the attention loads the call's queries
+// and window rows before it waits).
 static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream,
                               bool prefill, bool early) {
   csa_status st = validate_attn(batch, a, prefill);
@@ -558,8 +561,7 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
       ia.q_idx = L.q_idx;
       ia.out_idx = L.idx;
       ia.out_block_scores = nullptr;
-      // every launch after the call's first is a programmatic dependent of the one before it
-      const csa_status st = index_topk_run(batch, &ia, ws_index, ws_index_bytes, stream, l > 0);
+      const csa_status st = index_topk_run(batch, &ia, ws_index, ws_index_bytes, stream);
       if (st != CSA_OK) return st;
       src = L.idx;
     }

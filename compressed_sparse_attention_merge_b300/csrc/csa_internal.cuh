@@ -275,9 +275,10 @@ void debug_fault(int* fault, uint32_t* spin_limit);
 // allocation, barrier setup, loads of the call's inputs) once every CTA of that kernel has passed
 // griddep_launch(). Each kernel calls griddep_wait() before it reads anything the kernel before it
 // writes, and before it exits; the wait returns once that kernel has completed and its writes are
-// visible. A kernel signals griddep_launch() only after its own wait, so at most two kernels of a call
-// overlap and every earlier one has completed. The first kernel of a call is launched normally: whatever
-// ran before the call has completed when it starts.
+// visible. A kernel signals griddep_launch() only after its own wait, so at most two kernels overlap and
+// every earlier one has completed. A kernel whose first action is the wait (pack, coarse sums, indexer,
+// Top-K, combine) is launched as a dependent even as the first kernel of a call; the attention kernel reads
+// the call's inputs before its wait, so it is a dependent only after a kernel of the same call.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -117,12 +117,16 @@ __device__ __forceinline__ void pack_thread(const PackParams& p, int64_t t) {
 
 template <int TPG>
 __global__ void __launch_bounds__(256) pack_fp4_kernel(PackParams p) {
+  griddep_wait();                                  // before any access: the cache may still be read before
+  griddep_launch();
   pack_thread<TPG>(p, (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
 }
 
 // Several jobs in one launch; each CTA belongs to one job (its CTA range in m.cta_begin).
 template <int TPG>
 __global__ void __launch_bounds__(256) pack_fp4_multi_kernel(const __grid_constant__ PackMulti m) {
+  griddep_wait();                                  // before any access: the caches may still be read before
+  griddep_launch();
   int j = 0;
   while (j + 1 < m.n && (int64_t)blockIdx.x >= m.cta_begin[j + 1]) ++j;
   pack_thread<TPG>(m.job[j], ((int64_t)blockIdx.x - m.cta_begin[j]) * blockDim.x + threadIdx.x);
@@ -138,6 +142,8 @@ constexpr int kCoarseStage = 36864;
 __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touched) {
   __shared__ __align__(16) uint8_t stage[kCoarseStage];
   __shared__ __align__(8) uint64_t bar;
+  griddep_wait();                                // before any access: the packed entries come from the kernel before
+  griddep_launch();
   const int d = threadIdx.x;                     // blockDim.x == dim
   const int gl = blockIdx.x;
   const int64_t b = blockIdx.y;
@@ -203,12 +209,11 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t s) {
   clear_stale_error();
   // a quad per group while the call is smaller than eight 256-thread CTAs on each of 148 SMs (the modes
   // write the same bytes; the choice only trades per-thread latency against load width)
-  if (groups * 4 <= (int64_t)8 * threads * 148) {
-    pack_fp4_kernel<4><<<(unsigned)((groups * 4 + threads - 1) / threads), threads, 0, s>>>(p);
-  } else {
-    pack_fp4_kernel<1><<<(unsigned)((groups + threads - 1) / threads), threads, 0, s>>>(p);
-  }
-  return cudaGetLastError();
+  // (a programmatic dependent: the kernel waits before its first access)
+  if (groups * 4 <= (int64_t)8 * threads * 148)
+    return launch_ex(pack_fp4_kernel<4>, dim3((unsigned)((groups * 4 + threads - 1) / threads)), dim3(threads), 0, s,
+                     true, p);
+  return launch_ex(pack_fp4_kernel<1>, dim3((unsigned)((groups + threads - 1) / threads)), dim3(threads), 0, s, true, p);
 }
 
 cudaError_t launch_pack_multi(const PackParams* jobs, int n, cudaStream_t s) {
@@ -231,9 +236,8 @@ cudaError_t launch_pack_multi(const PackParams* jobs, int n, cudaStream_t s) {
   m.cta_begin[m.n] = ctas;
   ProfScope prof("pack_fp4", s);
   clear_stale_error();
-  if (tpg == 4) pack_fp4_multi_kernel<4><<<(unsigned)ctas, threads, 0, s>>>(m);
-  else pack_fp4_multi_kernel<1><<<(unsigned)ctas, threads, 0, s>>>(m);
-  return cudaGetLastError();
+  if (tpg == 4) return launch_ex(pack_fp4_multi_kernel<4>, dim3((unsigned)ctas), dim3(threads), 0, s, true, m);
+  return launch_ex(pack_fp4_multi_kernel<1>, dim3((unsigned)ctas), dim3(threads), 0, s, true, m);
 }
 
 cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s) {
@@ -243,8 +247,7 @@ cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s) {
   dim3 grid((unsigned)touched, (unsigned)p.batch);
   ProfScope prof("coarse_sum", s);
   clear_stale_error();
-  coarse_sum_kernel<<<grid, p.dim, 0, s>>>(p, touched);
-  return cudaGetLastError();
+  return launch_ex(coarse_sum_kernel, grid, dim3((unsigned)p.dim), 0, s, true, p, touched);
 }
 
 }  // namespace csa
