@@ -10,6 +10,7 @@ Modules
   attention  sparse attention over selected entries plus the sliding window (fp64), and the dense
              attention used by the "Top-K covering everything" invariant.
   chain      the Full / Reindex / Reuse layer pattern.
+  projection the cache write path: latent projection of hidden rows, then pair-merge and pack.
 
 Sources the definitions follow (web pages about the DeepSeek-V4.1-Flash technical report):
   [digest]   "DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression" (paper-digest.app),
