@@ -53,6 +53,7 @@ def _cases():
         "chain20_128k_b64_h64": synth.CHAIN_128K_B64,
         "prefill_2048_at_128k_h64": synth.PREFILL_2K_AT_128K,
         "decode_64k_b32_h64_q4": synth.DECODE_64K_B32_Q4,
+        "project_pack_128k_h4096": synth.PROJECT_128K_H4096,
     }
 
 
@@ -290,6 +291,48 @@ class PrefillWorkload:
         return {"q": self.q, "q_idx": self.q_idx, "new_tokens": self.chunk, "new_keys": self.chunk_keys}
 
 
+class ProjectWorkload:
+    """The cache write path: each step projects every hidden row of the batch to the latent and pair-merges
+    and FP4-packs the result into the cache (csa_project_pack, one kernel)."""
+
+    metric = "cache-write tokens/s (latent projection + pair-merge + FP4 pack)"
+    unit = "tokens/s"
+    dtype = "bf16 mma f32 accumulate, fp4-e2m1/e4m3 cache"
+
+    def __init__(self, case, device, replicas, keep_inputs=False):
+        from compressed_sparse_attention_merge_b300 import binding as csa
+        from compressed_sparse_attention_merge_b300 import synth
+        self.csa, self.case, self.device = csa, case, device
+        d = synth.make_project(case, device)
+        self.h, self.w = d["h"], d["w"]
+        self.E = case.tokens // 2
+        self.caches = [csa.empty_cache(case.batch, self.E, 512, device) for _ in range(replicas)]
+        self.out = self.caches[0]
+        self.ws_pack = csa.workspace(256, device)
+        self.queries_per_step = case.batch * case.tokens
+        self.modes = ["project"]
+
+    def step(self, r, new_tokens=None, out=None, **_):
+        h = self.h if new_tokens is None else new_tokens
+        cache = self.caches[r] if out is None else out
+        self.csa.project_pack(h, self.w, cache, scale_rule=self.csa.SCALE_AMAX, max_entries=self.E, ws=self.ws_pack)
+        return cache
+
+    def flops(self):
+        c = self.case
+        return {"project_pack": 2 * c.batch * c.tokens * c.hidden * 512}
+
+    def algorithmic_bytes(self):
+        c = self.case
+        return {"project_pack": c.batch * c.tokens * c.hidden * 2 + 512 * c.hidden * 2 + c.batch * self.E * 288}
+
+    def step_bytes(self):
+        return sum(self.algorithmic_bytes().values())
+
+    def h2d_inputs(self):
+        return {"new_tokens": self.h}
+
+
 def shard_case(name, shard):
     """The workload's case for one rank: rank r draws its own sequences (seed offset by 1000 r), so that N
     ranks hold N different shards of one global batch."""
@@ -300,6 +343,8 @@ def shard_case(name, shard):
 
 def make_workload(name, device, replicas, keep_inputs=False, shard=0):
     case = shard_case(name, shard)
+    if name.startswith("project"):
+        return ProjectWorkload(case, device, replicas, keep_inputs)
     if name.startswith("prefill"):
         return PrefillWorkload(case, device, replicas, keep_inputs)
     return DecodeWorkload(case, device, replicas, keep_inputs)
@@ -482,8 +527,7 @@ def run_ours(args):
     def e2e_step(r):
         for k in host_in:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        out = w.step(r, q=dev_in["q"], q_idx=dev_in["q_idx"], new_tokens=dev_in["new_tokens"],
-                     new_keys=dev_in["new_keys"])
+        out = w.step(r, **dev_in)
         host_out.copy_(out, non_blocking=True)
 
     def timed(fn):
@@ -512,7 +556,7 @@ def run_ours(args):
     del e2e_graphs, graphs
     e2e_ms = e2e_pipelined(w, host_in, args, world, device, stream)
     # a device check or a bounded wait that gave up in any run above voids the measurement
-    for ws_name in ("ws_pack", "ws_index", "ws_attn"):
+    for ws_name in [n for n in ("ws_pack", "ws_index", "ws_attn") if hasattr(w, n)]:
         st = csa.device_status(getattr(w, ws_name))
         if st != csa.OK:
             raise RuntimeError(f"{ws_name}: device status {st} after the timed runs")
@@ -520,7 +564,7 @@ def run_ours(args):
     peaks = _peaks()
     kernels = {}
     alg = w.algorithmic_bytes()
-    flops = w.flops() if isinstance(w, PrefillWorkload) else {}
+    flops = w.flops() if hasattr(w, "flops") else {}
     for name, (n, tot) in kt.items():
         avg_ms = tot / n
         ent = {"launches_per_step": n / args.steps, "avg_ms": round(avg_ms, 5),
@@ -535,7 +579,7 @@ def run_ours(args):
             ent["achieved_tflops"] = round(per_launch / (avg_ms * 1e-3) / 1e12, 2)
         kernels[name] = ent
     dom = max(kt.items(), key=lambda kv: kv[1][1])[0]
-    if isinstance(w, PrefillWorkload) and dom in flops:
+    if dom in flops:
         achieved = kernels[dom]["achieved_tflops"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
@@ -550,12 +594,14 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, budget_s=args.cpu_budget)
 
+    metric, unit = getattr(w, "metric", METRIC), getattr(w, "unit", UNIT)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": round(value, 1), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "timing": {"windows": len(per_window), "steps_per_window": args.steps, "statistic": "median window",
                    "ms_per_step_min": round(min(per_window), 5), "ms_per_step_max": round(max(per_window), 5)}, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp4-e2m1/e4m3 cache, fp16 mma f32 accumulate", "data": "synthetic",
+        "vs_baseline": None, "dtype": getattr(w, "dtype", "fp4-e2m1/e4m3 cache, fp16 mma f32 accumulate"),
+        "data": "synthetic",
         "config": {"workload": args.workload, "launch": "CUDA graph per step",
                    "batch_per_gpu": w.case.batch if hasattr(w.case, "batch") else 1,
                    "queries_per_step_per_gpu": w.queries_per_step, "layers": len(w.modes),
@@ -564,7 +610,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world} (batch sharded, no collective)"},
         "alg_bytes_per_step": w.step_bytes(),
         "achieved_step_gbs": round(w.step_bytes() / (ms * 1e-3) / 1e9, 1),
-        "e2e": {"value": round(world * w.queries_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": round(world * w.queries_per_step / (e2e_ms * 1e-3), 1), "unit": unit,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "launch": "per step: inputs copied from pinned host memory on a copy stream, the "
                           "entry points on the compute stream, the output copied back on a third stream; "
@@ -617,8 +663,7 @@ def e2e_pipelined(w, host_in, args, world, device, comp):
             cap.wait_event(in_ready[b])
             if i >= 2:
                 cap.wait_event(copied[b])
-            w.step(r, q=bufs[b]["q"], q_idx=bufs[b]["q_idx"], new_tokens=bufs[b]["new_tokens"],
-                   new_keys=bufs[b]["new_keys"], out=outs[b])
+            w.step(r, out=outs[b], **bufs[b])
             done[b].record(cap)
             down.wait_event(done[b])
             with torch.cuda.stream(down):
@@ -645,9 +690,14 @@ def e2e_pipelined(w, host_in, args, world, device, comp):
 
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels, from one ncu
-# capture of the same workload: {(workload, kernel): bytes}. An entry is removed when its kernel changes;
-# the roofline then reports traffic as null.
-TRAFFIC = {}
+# capture of the same workload with one cache replica (still larger than L2):
+#   python bench.py --steps 2 --warmup 3 --no-cpu-baseline --min-seconds 0 --replicas 1
+# under ncu -k regex:<kernel> -s 2 -c 1. An entry is removed when its kernel changes; the roofline then
+# reports traffic as null.
+TRAFFIC = {
+    ("decode_64k_b32_h64", "sparse_attn"): 25_284_096 + 21_760,
+    ("decode_64k_b32_h64", "index_score"): 75_612_160 + 1_262_592,
+}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -768,16 +818,40 @@ class OraclePrefillSample:
         return outs
 
 
-def _oracle_sample(workload):
+class OracleProjectSample:
+    """A slice of the projection workload's tokens for the CPU oracle (the same value recipe, its own draw)."""
+
+    def __init__(self, case, tokens=256, seed_offset=0):
+        from compressed_sparse_attention_merge_b300 import synth
+        g = synth.generator(case.seed + 1000 + seed_offset, "cpu")
+        self.h = synth.normal_bf16(g, (tokens, case.hidden), "cpu").float().numpy()
+        w = torch.randn(512, case.hidden, generator=g) / case.hidden ** 0.5
+        self.w = w.to(torch.bfloat16).float().numpy()
+        self.tokens = tokens
+
+    def step(self):
+        from oracle import projection as o_proj
+        return o_proj.project_pack(self.h, self.w, "amax")
+
+
+def _oracle_sample(workload, seed_offset=0):
+    """(sample, units per step, what the sample is) for the CPU oracle."""
     case = _cases()[workload]
+    if workload.startswith("project"):
+        s = OracleProjectSample(case, seed_offset=seed_offset)
+        return s, s.tokens, f"{s.tokens} tokens of one sequence (projection of the hidden rows, merge and pack)"
     if workload.startswith("prefill"):
         s = OraclePrefillSample(case)
         return s, len(s.positions), f"{len(s.positions)} positions of the chunk (pack of the whole chunk, " \
                                     f"dequantisation of the cache, per-position index + Top-K and attention)"
-    s = OracleDecodeSample(case)
+    s = OracleDecodeSample(case, seed_offset=seed_offset)
     return s, case.n_query, "one sequence of the batch (re-pack of the newest entry, dequantisation of the " \
                             "cache, index + Top-K, attention" + (" through all layers" if case.layers > 1 else "") \
                             + ")"
+
+
+def _metric_unit(workload):
+    return (ProjectWorkload.metric, ProjectWorkload.unit) if workload.startswith("project") else (METRIC, UNIT)
 
 
 def _host_cpu():
@@ -803,9 +877,7 @@ def _oracle_worker(args):
         threadpoolctl.threadpool_limits(1)
     except Exception:
         pass
-    case = _cases()[workload]
-    s = OracleDecodeSample(case, seed_offset=index) if not workload.startswith("prefill") else OraclePrefillSample(case)
-    queries = case.n_query if not workload.startswith("prefill") else len(s.positions)
+    s, queries, _ = _oracle_sample(workload, seed_offset=index)
     s.step()
     n, t0 = 0, time.perf_counter()
     while True:
@@ -831,7 +903,7 @@ def cpu_baseline(workload, budget_s=20.0, parallel=True):
             break
     one = n * queries / el
     nproc, model = _host_cpu()
-    out = {"value": round(one, 4), "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+    out = {"value": round(one, 4), "unit": _metric_unit(workload)[1], "cores": _blas_threads(), "kind": "oracle",
            "sample": what + f"; {n} repetitions in {el:.1f} s", "host": {"nproc": nproc, "cpu": model}}
     if parallel and nproc > 1:
         import multiprocessing as mp
@@ -860,15 +932,16 @@ def run_reference(args):
     el = time.perf_counter() - t0
     value = args.steps * queries / el
     cores = _blas_threads()
-    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    metric, unit = _metric_unit(args.workload)
+    line = {"metric": metric, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": args.workload, "launch": "the oracle (numpy, fp64) on the host cores",
                        "sample": what},
             "impl": "reference",
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": what},
-            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 

@@ -42,6 +42,13 @@ class PackArgs(ctypes.Structure):
                 ("coarse_sum", ctypes.c_void_p), ("coarse_stride_b", ctypes.c_int64)]
 
 
+class ProjectArgs(ctypes.Structure):
+    _fields_ = [("h", ctypes.c_void_p), ("h_stride_b", ctypes.c_int64), ("h_stride_t", ctypes.c_int64),
+                ("hidden", ctypes.c_int64), ("w", ctypes.c_void_p), ("n_tokens", ctypes.c_int64),
+                ("scale_rule", ctypes.c_int32), ("reserved", ctypes.c_int32), ("first_entry", ctypes.c_void_p),
+                ("max_entries", ctypes.c_int64), ("cache", ctypes.c_void_p), ("cache_stride_b", ctypes.c_int64)]
+
+
 class IndexArgs(ctypes.Structure):
     _fields_ = [("n_query", ctypes.c_int64), ("heads", ctypes.c_int32), ("dim", ctypes.c_int32),
                 ("q_idx", ctypes.c_void_p), ("head_w", ctypes.c_void_p), ("flags", ctypes.c_int32),
@@ -97,6 +104,8 @@ def lib():
         L.csa_pack_fp4.restype = I32
         L.csa_pack_fp4.argtypes = [I64, ctypes.POINTER(PackArgs), P, SZ, P]
         L.csa_pack_fp4_multi.restype = I32
+        L.csa_project_pack.restype = I32
+        L.csa_project_pack.argtypes = [I64, ctypes.POINTER(ProjectArgs), P, SZ, P]
         L.csa_pack_fp4_multi.argtypes = [I32, ctypes.POINTER(I64), ctypes.POINTER(PackArgs), P, SZ, P]
         L.csa_index_topk_workspace_size.restype = SZ
         L.csa_index_topk_workspace_size.argtypes = [I64, ctypes.POINTER(IndexArgs)]
@@ -226,6 +235,31 @@ def pack_fp4(x, cache, *, merge, scale_rule, max_entries, ws, first_entry=None, 
     a = pack_args(x, cache, merge=merge, scale_rule=scale_rule, max_entries=max_entries,
                   first_entry=first_entry, coarse_sum=coarse_sum)
     _check(lib().csa_pack_fp4(x.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)), "csa_pack_fp4")
+
+
+def project_pack(h, w, cache, *, scale_rule, max_entries, ws, first_entry=None, stream=None):
+    """csa_project_pack: project hidden rows h [B, T, hidden] (bf16) by w [512, hidden] (bf16) and pair-merge
+    + FP4-pack the latents into cache [B, blocks, 2304] at entries first_entry[b]..."""
+    _need(h, "h", torch.bfloat16)
+    _need(w, "w", torch.bfloat16)
+    _need(cache, "cache", torch.uint8)
+    if h.dim() != 3 or h.stride(2) != 1:
+        raise ValueError("h must be [batch, n_tokens, hidden] with contiguous rows")
+    if w.dim() != 2 or w.shape[0] != 512 or w.shape[1] != h.shape[2] or not w.is_contiguous():
+        raise ValueError("w must be a contiguous [512, hidden] tensor")
+    a = ProjectArgs()
+    a.h = h.data_ptr()
+    a.h_stride_b, a.h_stride_t = h.stride(0), h.stride(1)
+    a.hidden = h.shape[2]
+    a.w = w.data_ptr()
+    a.n_tokens = h.shape[1]
+    a.scale_rule = scale_rule
+    a.first_entry = None if first_entry is None else _need(first_entry, "first_entry", torch.int32).data_ptr()
+    a.max_entries = max_entries
+    a.cache = cache.data_ptr()
+    a.cache_stride_b = cache[0].numel() if cache.dim() > 1 else cache.numel()
+    _check(lib().csa_project_pack(h.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)),
+           "csa_project_pack")
 
 
 PACK_MAX_JOBS = 4

@@ -340,6 +340,40 @@ csa_status csa_pack_fp4_multi(int n_jobs, const int64_t* batch, const csa_pack_a
   return CSA_OK;
 }
 
+csa_status csa_project_pack(int64_t batch, const csa_project_args* a, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  if (a == nullptr || batch < 0 || batch > 65535) return CSA_ERR_INVALID_ARG;
+  if (a->scale_rule != CSA_SCALE_AMAX && a->scale_rule != CSA_SCALE_POW2) return CSA_ERR_INVALID_ARG;
+  if (a->reserved != 0) return CSA_ERR_INVALID_ARG;
+  if (a->hidden < 64 || a->hidden > 16384 || a->hidden % 64 != 0) return CSA_ERR_INVALID_ARG;
+  if (a->n_tokens < 0 || a->n_tokens > (int64_t)65535 * 128 || a->max_entries < 0) return CSA_ERR_INVALID_ARG;
+  const int64_t n_pairs = a->n_tokens / 2;
+  const bool empty = batch == 0 || n_pairs == 0;
+  if (!empty) {
+    if (a->h == nullptr || a->w == nullptr || a->cache == nullptr) return CSA_ERR_INVALID_ARG;
+    if (!aligned(a->h, 16) || !aligned(a->w, 16) || !aligned(a->cache, 16)) return CSA_ERR_ALIGNMENT;
+    if (a->h_stride_t % 8 != 0 || a->h_stride_b % 8 != 0 || a->cache_stride_b % 16 != 0) return CSA_ERR_ALIGNMENT;
+    if (a->h_stride_t < a->hidden) return CSA_ERR_INVALID_ARG;
+    if (batch > 1 && a->h_stride_b < a->n_tokens * a->h_stride_t) return CSA_ERR_INVALID_ARG;
+    if (batch > 1 && a->cache_stride_b < ceil_div(a->max_entries, kBlockEntries) * block_bytes(kLatent))
+      return CSA_ERR_INVALID_ARG;
+  }
+  csa_status st = current_device(nullptr);
+  if (st != CSA_OK) return st;
+  st = check_ws(ws, ws_bytes, CSA_WS_HEADER_BYTES);
+  if (st != CSA_OK) return st;
+  if (empty) return CSA_OK;
+  ProjectParams p{};
+  p.h = static_cast<const __nv_bfloat16*>(a->h);
+  p.h_stride_b = a->h_stride_b; p.h_stride_t = a->h_stride_t; p.hidden = a->hidden; p.n_tokens = a->n_tokens;
+  p.batch = batch; p.max_entries = a->max_entries; p.cache_stride_b = a->cache_stride_b;
+  p.w = static_cast<const __nv_bfloat16*>(a->w);
+  p.scale_rule = a->scale_rule; p.first_entry = a->first_entry; p.cache = a->cache;
+  p.hdr = static_cast<uint32_t*>(ws);
+  if (cudaError_t e = launch_project_pack(p, stream)) return cuda_fail(e, "project_pack");
+  return CSA_OK;
+}
+
 // ------------------------------------------------------------------------------------------------
 }  // extern "C"
 

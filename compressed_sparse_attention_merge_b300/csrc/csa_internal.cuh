@@ -25,6 +25,7 @@ enum KernelId : uint32_t {
   KID_TOPK = 5,
   KID_ATTN = 6,
   KID_COMBINE = 7,
+  KID_PROJECT = 8,
 };
 
 __device__ __forceinline__ void report(uint32_t* hdr, uint32_t code, uint32_t kernel, uint32_t detail) {
@@ -306,6 +307,18 @@ cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 cudaError_t launch_pack(const PackParams& p, cudaStream_t s);
 cudaError_t launch_pack_multi(const PackParams* jobs, int n, cudaStream_t s);
 cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s);
+
+// Fused latent projection + pair-merge + FP4 pack (csa_project_pack).
+struct ProjectParams {
+  const __nv_bfloat16* h;
+  int64_t h_stride_b, h_stride_t, hidden, n_tokens, batch, max_entries, cache_stride_b;
+  const __nv_bfloat16* w;
+  int scale_rule;
+  const int32_t* first_entry;
+  uint8_t* cache;
+  uint32_t* hdr;
+};
+cudaError_t launch_project_pack(const ProjectParams& p, cudaStream_t s);
 cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s, bool pdl);
 cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s, bool pdl);

@@ -341,31 +341,76 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
       const int64_t e = blk * kBlockEntries + (m & 7);
       const bool row_ok = id0 >= 0 && blk < u.n_b && e < u.n_e;
       const int64_t slot = slot0 + (m >> 3);
+      if constexpr (NQ >= 8) {
+        // Many positions per unit: all N columns in one round of loads, then the block maximum of every
+        // position at once by a transposing reduction over the 8 lanes of a block. At the step with offset
+        // o a lane keeps the half of its positions selected by (lane & o) and takes the maximum with its
+        // partner's copy of that half; after offsets 1, 2, 4, lane j of a block holds positions
+        // (j & 1) NQ/2 + (j >> 1 & 1) NQ/4 + (j >> 2) NQ/8 + i, i < NQ/8. The maximum is exact, so the result
+        // equals the per-position shuffles of the path below.
+        uint32_t r[N];
 #pragma unroll
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        if (c0 >= u.nq * HI) break;
-        uint32_t r[16];
-        ld_32x16(tbase + lane_base + C::kColD + db * N + c0, r);
+        for (int c0 = 0; c0 < N; c0 += 16) ld_32x16(tbase + lane_base + C::kColD + db * N + c0, r + c0);
         tc::wait_ld();
+        float v[NQ];
 #pragma unroll
-        for (int qq = 0; qq < 16 / HI; ++qq) {
-          const int q = c0 / HI + qq;
-          if (q >= NQ || q >= u.nq) break;
+        for (int q = 0; q < NQ; ++q) {
           float sum = 0.0f;
 #pragma unroll
           for (int h = 0; h < HI; ++h) {
-            const float dot = __uint_as_float(r[qq * HI + h]);
+            const float dot = __uint_as_float(r[q * HI + h]);
             const float t = __fmul_rn(w[h], p.relu ? fmaxf(dot, 0.0f) : dot);
             sum = h == 0 ? t : __fadd_rn(sum, t);
           }
-          const bool okq = row_ok && 2 * e + 1 <= (int64_t)pos_sh[q];
-          float mx = okq ? __fadd_rn(sum, 0.0f) : -INFINITY;
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          if ((lane & 7) == 0 && slot < p.n_slots) {
-            const int64_t row = hier ? u.row0 : u.row0 + q;
-            p.scores[row * p.score_stride + slot] = mx;
+          const bool okq = row_ok && q < u.nq && 2 * e + 1 <= (int64_t)pos_sh[q];
+          v[q] = okq ? __fadd_rn(sum, 0.0f) : -INFINITY;
+        }
+#pragma unroll
+        for (int o = 1, n = NQ / 2; o <= 4; o <<= 1, n >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < n; ++i) {
+            const float keep = up ? v[n + i] : v[i];
+            const float give = up ? v[i] : v[n + i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, o));
+          }
+        }
+        const int j = lane & 7;
+        const int qb = (j & 1) * (NQ / 2) + ((j >> 1) & 1) * (NQ / 4) + (j >> 2) * (NQ / 8);
+        if (slot < p.n_slots) {
+#pragma unroll
+          for (int i = 0; i < NQ / 8; ++i) {
+            const int q = qb + i;
+            if (q < u.nq) p.scores[(u.row0 + q) * p.score_stride + slot] = v[i];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          if (c0 >= u.nq * HI) break;
+          uint32_t r[16];
+          ld_32x16(tbase + lane_base + C::kColD + db * N + c0, r);
+          tc::wait_ld();
+#pragma unroll
+          for (int qq = 0; qq < 16 / HI; ++qq) {
+            const int q = c0 / HI + qq;
+            if (q >= NQ || q >= u.nq) break;
+            float sum = 0.0f;
+#pragma unroll
+            for (int h = 0; h < HI; ++h) {
+              const float dot = __uint_as_float(r[qq * HI + h]);
+              const float t = __fmul_rn(w[h], p.relu ? fmaxf(dot, 0.0f) : dot);
+              sum = h == 0 ? t : __fadd_rn(sum, t);
+            }
+            const bool okq = row_ok && 2 * e + 1 <= (int64_t)pos_sh[q];
+            float mx = okq ? __fadd_rn(sum, 0.0f) : -INFINITY;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            if ((lane & 7) == 0 && slot < p.n_slots) {
+              const int64_t row = hier ? u.row0 : u.row0 + q;
+              p.scores[row * p.score_stride + slot] = mx;
+            }
           }
         }
       }

@@ -32,6 +32,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn, int
          ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with bf16 A and B (format code 1 in both operand fields; the two operands of one product always
+// have the same type).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+  return idesc_f16_f32(M, N, a_mn, b_mn) | (1u << 7) | (1u << 10);
+}
+
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"

@@ -9,6 +9,7 @@ Value recipes (the pages publish no workload data; these follow the shapes they 
   index queries      fp32 integers uniform in [-4, 4]
   needle blocks      a fraction of blocks whose 8 key rows are 4 * sign(first index query, head 0), so the
                      Top-K has structure to find
+  hidden rows        bf16 N(0, 1), projected by a bf16 N(0, 1 / hidden) weight (latents about N(0, 1))
 Every generator takes an explicit seed and device; large tensors are generated one sequence at a
 time to bound the temporary fp32 memory.
 """
@@ -178,6 +179,28 @@ def make_prefill(case, device):
 
 
 # The five workloads of the method's decode/prefill path, named by what they are.
+@dataclass
+class ProjectCase:
+    """The cache write path: hidden rows of `batch` sequences of `tokens` tokens, projected to the latent by a
+    [512][hidden] weight and packed (merge 2)."""
+    name: str
+    batch: int = 1
+    tokens: int = 131072
+    hidden: int = 4096
+    seed: int = 30000
+
+
+def make_project(case, device):
+    """Hidden rows bf16 N(0, 1) [batch, tokens, hidden] and a weight bf16 N(0, 1 / hidden) [512, hidden], so
+    that the latents are about N(0, 1)."""
+    g = generator(case.seed, device)
+    h = torch.empty(case.batch, case.tokens, case.hidden, dtype=torch.bfloat16, device=device)
+    for b in range(case.batch):
+        h[b] = torch.randn(case.tokens, case.hidden, generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn(LATENT, case.hidden, generator=g, device=device) / case.hidden ** 0.5).to(torch.bfloat16)
+    return {"h": h, "w": w}
+
+
 TINY_DECODE_4K = DecodeCase("tiny_decode_4k_b1_h16", tokens=[4096], heads=16, idx_heads=1, idx_dim=64, top_k=64,
                             seed=20261)
 DECODE_64K_B32 = DecodeCase("decode_64k_b32_h64", tokens=[65536] * 32, outlier_frac=0.01, needle_frac=0.01,
@@ -191,3 +214,7 @@ PREFILL_2K_AT_128K = PrefillCase("prefill_2048_at_128k_h64", context=131072, chu
 # last four tokens of each sequence, causal among themselves.
 DECODE_64K_B32_Q4 = DecodeCase("decode_64k_b32_h64_q4", tokens=[65536] * 32, n_query=4, outlier_frac=0.01,
                                needle_frac=0.01, causal_drafts=True, seed=20266)
+
+# The cache write path over one 128K-token sequence with a 4,096-wide hidden state (the pages give no hidden
+# width; 4,096 is a common one for a model of this size class).
+PROJECT_128K_H4096 = ProjectCase("project_pack_128k_h4096", batch=1, tokens=131072, hidden=4096, seed=30001)

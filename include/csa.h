@@ -156,6 +156,51 @@ typedef struct csa_pack_args {
 csa_status csa_pack_fp4(int64_t batch, const csa_pack_args* args, void* ws, size_t ws_bytes,
                         cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------------------
+ * csa_project_pack -- project hidden rows to 512-d latents, then pair-merge and FP4-pack them, in one
+ * kernel (the latents never reach memory).
+ *
+ * Follows [card] Key ideas ("Causal Encoder-Decoder (CED)": the upper layers' global KV is projected from
+ * the hidden state of a middle layer) and csa_pack_fp4 for the merge and the format.
+ *
+ * For every sequence b and token t in [0, n_tokens):
+ *   x[t][j] = sum over k of h[b][t][k] * w[j][k]     (j < 512; bf16 inputs, fp32 accumulation on the tensor
+ *                                                   cores, in an order of their own: the result equals the
+ *                                                   exactly rounded sum whenever every partial sum is exact in
+ *                                                   fp32, such as for small-integer inputs)
+ * then the rows x go through csa_pack_fp4 with merge 2, dim 512 and scale_rule (an odd trailing token is
+ * not packed): entry first_entry[b] + i holds the merged pair (2i, 2i + 1).
+ *
+ * Arguments (strides in elements):
+ *   h            device bf16 [batch][n_tokens][hidden], rows contiguous; 16-byte aligned, with h_stride_t and
+ *                h_stride_b multiples of 8 (h_stride_t >= hidden).
+ *   hidden       64 .. 16,384, a multiple of 64.
+ *   w            device bf16 [512][hidden] (output-major, like a linear layer's weight), contiguous,
+ *                16-byte aligned.
+ *   scale_rule, first_entry, max_entries, cache, cache_stride_b: as csa_pack_fp4 with dim 512.
+ *   ws           workspace of at least CSA_WS_HEADER_BYTES (status word only).
+ * Errors: CSA_ERR_INVALID_ARG / CSA_ERR_ALIGNMENT before any launch; a sequence whose first_entry[b] +
+ * n_tokens / 2 exceeds max_entries is skipped and CSA_ERR_DEVICE_CHECK recorded; a bounded wait that runs
+ * out records CSA_ERR_TIMEOUT.
+ * ------------------------------------------------------------------------------------------------ */
+typedef struct csa_project_args {
+  const void* h;
+  int64_t h_stride_b;
+  int64_t h_stride_t;
+  int64_t hidden;
+  const void* w;
+  int64_t n_tokens;
+  int32_t scale_rule;
+  int32_t reserved;          /* must be 0 */
+  const int32_t* first_entry;
+  int64_t max_entries;
+  uint8_t* cache;
+  int64_t cache_stride_b;
+} csa_project_args;
+
+csa_status csa_project_pack(int64_t batch, const csa_project_args* args, void* ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
 /* csa_pack_fp4_multi -- n_jobs csa_pack_fp4 calls (job j: batch[j] sequences, args[j]) in as few
  * launches as their sizes allow. A decode step appends to the latent cache and to the index-key cache, and
  * this call does both in one launch. The result equals the calls made one after another in job order,

@@ -43,6 +43,36 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n)
 
 
+def test_project_pack_rejects_bad_arguments_before_any_device_call(lib):
+    # pointers that are never dereferenced on the host
+    from compressed_sparse_attention_merge_b300 import binding as b
+    good = 0x10000
+    pa = b.ProjectArgs()
+    pa.h, pa.w, pa.cache = good, good, good
+    pa.h_stride_b, pa.h_stride_t, pa.hidden, pa.n_tokens = 4 * 640, 640, 640, 4
+    pa.scale_rule, pa.max_entries, pa.cache_stride_b = b.SCALE_AMAX, 8, 2304
+    call = lambda batch: lib.csa_project_pack(batch, ctypes.byref(pa), None, 0, None)
+    for field, bad, want in [("hidden", 600, b.ERR_INVALID_ARG),          # not a multiple of 64
+                             ("hidden", 16448, b.ERR_INVALID_ARG),        # above 16,384
+                             ("scale_rule", 7, b.ERR_INVALID_ARG),
+                             ("reserved", 1, b.ERR_INVALID_ARG),
+                             ("n_tokens", -1, b.ERR_INVALID_ARG),
+                             ("h", good + 8, b.ERR_ALIGNMENT),
+                             ("w", good + 4, b.ERR_ALIGNMENT),
+                             ("h_stride_t", 644, b.ERR_ALIGNMENT),        # rows not 16-byte aligned
+                             ("h_stride_t", 576, b.ERR_INVALID_ARG),      # shorter than a row
+                             ("cache_stride_b", 2312, b.ERR_ALIGNMENT)]:
+        old = getattr(pa, field)
+        setattr(pa, field, bad)
+        assert call(2) == want, field
+        setattr(pa, field, old)
+    pa.h_stride_b = 640                                  # sequences overlapping rows
+    assert call(2) == b.ERR_INVALID_ARG
+    pa.h = None                                          # a null pointer is fine when nothing is packed
+    pa.n_tokens = 1
+    assert call(2) not in (b.ERR_INVALID_ARG, b.ERR_ALIGNMENT)  # validation passes (device checks follow)
+
+
 def test_constants_and_strings(lib):
     assert lib.csa_abi_version() == 1
     assert lib.csa_entry_bytes(512) == 288 and lib.csa_block_bytes(512) == 2304
