@@ -341,8 +341,15 @@ def shard_case(name, shard):
     return dataclasses.replace(case, seed=case.seed + 1000 * shard) if shard else case
 
 
-def make_workload(name, device, replicas, keep_inputs=False, shard=0):
+def make_workload(name, device, replicas, keep_inputs=False, shard=0, batch=None):
+    """The named workload; `batch` (decode workloads only) replaces the number of sequences, each as long as
+    the workload's first."""
+    import dataclasses
     case = shard_case(name, shard)
+    if batch is not None:
+        if not hasattr(case, "tokens") or not isinstance(case.tokens, list):
+            raise ValueError("--batch applies to decode workloads")
+        case = dataclasses.replace(case, tokens=[case.tokens[0]] * batch, swa_len=None)
     if name.startswith("project"):
         return ProjectWorkload(case, device, replicas, keep_inputs)
     if name.startswith("prefill"):
@@ -449,7 +456,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     csa.lib()
 
-    w = make_workload(args.workload, device, args.replicas, shard=rank)
+    w = make_workload(args.workload, device, args.replicas, shard=rank, batch=args.batch)
     R = args.replicas
     stream = torch.cuda.current_stream(device)
 
@@ -594,7 +601,8 @@ def run_ours(args):
         achieved = kernels[dom].get("achieved_gbs")
         roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": None if achieved is None else round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": TRAFFIC.get((args.workload, dom)), "peak_source": peaks["source"] + " copy"}
+                "traffic": None if args.batch else TRAFFIC.get((args.workload, dom)),
+                "peak_source": peaks["source"] + " copy"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -962,6 +970,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(_cases().keys()), default=DEFAULT_WORKLOAD)
     ap.add_argument("--replicas", type=int, default=4)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="decode workloads: number of sequences (each as long as the workload's first)")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--min-seconds", type=float, default=2.5,
                     help="the K-step timed window is repeated until this many seconds have passed")
