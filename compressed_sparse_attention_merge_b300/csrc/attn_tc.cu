@@ -11,20 +11,22 @@
 // both products are taken with the rows as the 128-wide M side and the heads as N:
 //   S^T [rows x heads]  = C [rows x 512] . Q^T                   (logits)
 //   O^T [512 x heads]  += C^T [512 x rows] . P^T [rows x heads]  (values)
-// S and O accumulate in tensor memory; the row sums l are added up by one warp from the fp16
-// probabilities in shared memory (the same values the tensor core multiplies).
+// Both read the same dequantised tile in shared memory: 128-byte-swizzled rows of 64 latent columns are the
+// K-major layout of C and the MN-major layout of C^T. S and O accumulate in tensor memory; the row sums l
+// are added up by one warp from the fp16 probabilities in shared memory (the same values the tensor core
+// multiplies).
 //   Every tile is dequantised once. Eight converter warps (thread = tensor-memory lane = tile row) read
 //   their row's FP4 codes and scales straight from global memory (the gather warp prefetches each cache
 //   tile's blocks into L2 three tiles ahead; a converter keeps the codes of its next two panels in flight in
 //   registers, one 32-byte load each, and loads a tile's scale bytes once), convert a 64-column panel to
-//   fp16 and write it twice: into the logits
-//   operand ring in tensor memory, and into the values buffer in shared memory, a whole tile of C^T in the
-//   128-byte-swizzled MN-major layout, recycled per 128-latent chunk as the value products finish with it.
-//   Window tiles come first: their bf16 rows are copied by tensor map straight into the values buffer and
-//   converted to fp16 in place by the same threads, which also write the logits panels.
-// Pipelining: S and P are double-buffered, so the logits and softmax of tile t+1 run while the values of
-// tile t are multiplied; the converters of tile t+1 wait only for the value products of the chunk they
-// overwrite. Both products are issued by whole warps (one elected lane issues).
+//   fp16 and write it into the tile buffer in shared memory. The buffer holds one whole tile and is recycled
+//   per 128-latent chunk as the value products finish with it; both products wait for a chunk on the same
+//   barrier. Window tiles come first: their bf16 rows are copied by tensor map straight into the buffer and
+//   converted to fp16 in place by the same threads.
+// Pipelining: S and P are double-buffered, so the softmax of tile t+1 can run while the values of tile t are
+// multiplied; the converters of tile t+1 wait only for the value products of the chunk they overwrite (which
+// complete after the same tile's logits). Both products are issued by whole warps (one elected lane
+// issues).
 //
 // Warp roles: 0-3 softmax and epilogue (thread = tile row), 4-11 converters (warp 4 + 4 h + s covers
 // subpartition s, panels of parity h), 12 gather (window copies, L2 prefetch, block-id checks), 13 logits
@@ -76,11 +78,8 @@ constexpr int kSmemBytes = kQMaxOff + 64 * 4;
 static_assert(kVOff % 1024 == 0 && kPOff % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
-constexpr int kTRing = 4;
 enum Bar {
-  TRING_FULL = 0,                       // logits operand panels in tensor memory: converters <-> logits issuer
-  TRING_EMPTY = TRING_FULL + kTRing,
-  V_FULL = TRING_EMPTY + kTRing,        // values buffer chunks: converters <-> values issuer
+  V_FULL = 0,                           // tile buffer chunks: converters <-> logits and values issuers
   V_EMPTY = V_FULL + kChunks,
   S_FULL = V_EMPTY + kChunks,           // logits buffers: logits issuer <-> softmax
   S_EMPTY = S_FULL + 2,
@@ -96,9 +95,9 @@ constexpr int kConv0 = 4, kConvWarps = 8;      // converter warps 4..11
 constexpr int kGatherWarp = 12, kLogitsWarp = 13, kValuesWarp = 14, kSumWarp = 15;
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColA = 128, kColO = 256;   // S: two buffers of 64 columns; A: four panels
+constexpr uint32_t kColS = 0, kColO = 256;   // S: two buffers of 64 columns; O^T: 4 x 64 columns
 
-constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major (tensor memory), Q K-major
+constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
 constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
 
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
@@ -329,10 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   // ---------------- setup ----------------
   if (warp == kLogitsWarp) tc::alloc(tmem_ptr, kTmemCols);
   if (tid == 0) {
-    for (int i = 0; i < kTRing; ++i) {
-      mbar_init(&bars[TRING_FULL + i], 4);
-      mbar_init(&bars[TRING_EMPTY + i], 1);
-    }
     for (int i = 0; i < kChunks; ++i) {
       mbar_init(&bars[V_FULL + i], kConvWarps);
       mbar_init(&bars[V_EMPTY + i], 1);
@@ -496,7 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     }
   } else if (is_conv) {
     // ---------------- converters: one 64-column panel of every chunk of every tile ----------------
-    const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
     volatile int* progress = flag + 4;
     bool stop = false;
     for (int it = 0; it < n_tiles && !stop; ++it) {
@@ -550,29 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           stop = true;
           break;
         }
-        // logits operand: panel pnl of tile it goes to ring slot pnl & 3, use 2 it + c / 2 of that slot. A slot
-        // written for chunks 0 and 1 was last read by tile it - 1's logits products, which are complete once
-        // that tile's values have freed a chunk (or its window copy has landed): only chunks 2 and 3 wait for
-        // the ring.
-        const uint32_t slot = pnl & 3, use = 2u * it + (c >> 1);
-        if (c >= 2 &&
-            !__all_sync(0xffffffffu, wait_bar(&bars[TRING_EMPTY + slot], (use - 1) & 1u, abort_flag, p.hdr, 3, p.spin_limit))) {
-          stop = true;
-          break;
-        }
-        tc::fence_after();
-        tc::st_32x32(tbase + lane_base + kColA + 32 * slot, h);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           *reinterpret_cast<uint4*>(vrow + ((j ^ (row & 7)) << 4)) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        tc::wait_st();          // no tensor-memory store may be in flight past this point
-        tc::fence_before();
         tc::fence_proxy_async();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars[TRING_FULL + slot]);
-          mbar_arrive(&bars[V_FULL + c]);
-        }
+        if (lane == 0) mbar_arrive(&bars[V_FULL + c]);
       }
       if (!win) {
         // the scales of tile k + 2 are loaded a tile before the queue reaches it, its id one more tile earlier
@@ -592,16 +569,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       const int sb = it & 1;
       if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4, p.spin_limit)) break;
       const uint32_t d = tbase + kColS + 64 * sb;
-      for (int pnl = 0; pnl < kPanels; ++pnl) {
-        const uint32_t slot = pnl & 3, use = 2u * it + (pnl >> 2);
-        if (!wait_bar_warp(&bars[TRING_FULL + slot], use & 1u, abort_flag, p.hdr, 4, p.spin_limit)) { ok = false; break; }
+      for (int c = 0; c < kChunks; ++c) {
+        if (!wait_bar_warp(&bars[V_FULL + c], it & 1, abort_flag, p.hdr, 4, p.spin_limit)) { ok = false; break; }
         tc::fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bq = tc::smem_desc(q_addr + pnl * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
-          tc::mma_f16_ts_warp(d, tbase + kColA + 32 * slot + 8 * ks, bq, kIdescS, (pnl | ks) != 0);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int pnl = 2 * c + hh;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = tc::smem_desc(s_base + kVOff + c * kChunkBytes + hh * kHalfBytes + ks * 32, 16, 1024,
+                                             tc::kSwizzle128B);
+            const uint64_t bq = tc::smem_desc(q_addr + pnl * kQPanel + ks * 32, 16, 1024, tc::kSwizzle128B);
+            tc::mma_f16_warp(d, a, bq, kIdescS, (pnl | ks) != 0);
+          }
         }
-        tc::commit_warp(&bars[TRING_EMPTY + slot]);
       }
       if (ok) tc::commit_warp(&bars[S_FULL + sb]);
     }
