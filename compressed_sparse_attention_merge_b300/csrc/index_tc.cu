@@ -14,7 +14,7 @@
 // positions of one sequence, all indexer heads) are rounded to the same FP4 format with power-of-two
 // scales (exact for integer values in [-4, 4]) and form the N side. Each product lands in tensor memory;
 // four epilogue warps (thread = entry) write the keys' scale factors into tensor memory before the product
-// and afterwards apply ReLU, the head weights, the ordered head sum and the causal mask, and take the block
+// (as soon as a stage's copy has landed, between the epilogues of earlier stages) and afterwards apply ReLU, the head weights, the ordered head sum and the causal mask, and take the block
 // maximum across the 8 lanes that hold one block. The accumulator is double-buffered so that the epilogue
 // of one stage overlaps the product of the next, and the copy warp starts the first stages before the
 // queries are prepared.
@@ -57,7 +57,6 @@ struct Cfg {
   // stages ahead of the product that reads them)
   static constexpr int kND = N <= 16 ? 4 : 2;
   static constexpr int kNSF = 4;
-  static constexpr int kLook = 2;
   // tensor memory columns
   static constexpr uint32_t kColD = 0;                              // kND x N
   static constexpr uint32_t kColSFA = kND * N;                      // kNSF x (4 per MMA)
@@ -307,10 +306,10 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
     float w[HI];
 #pragma unroll
     for (int h = 0; h < HI; ++h) w[h] = p.head_w ? __ldg(p.head_w + h) : 1.0f;
-    // key scale factors of stage k into scale buffer k % kNSF (lane m, column base + 4 s + m / 32)
-    auto write_scales = [&](int k) -> bool {
+    // key scale factors of stage k (whose copy has landed) into scale buffer k % kNSF (lane m, column
+    // base + 4 s + m / 32)
+    auto put_scales = [&](int k) {
       const int slot = k % C::kStages;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&full[slot], (k / C::kStages) & 1, abort_flag, p.hdr))) return false;
       const uint8_t* sc = smem + C::kScalesOff + slot * C::kScalesStage + (m >> 3) * (8 * C::kRowScales) +
                           (m & 7) * C::kRowScales;
 #pragma unroll
@@ -321,14 +320,35 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfr[slot]);
-      return true;
     };
+    int ks = 0;                                    // the next stage whose scale factors are written
     bool ok = true;
-    for (int k = 0; k < C::kLook && k < n && ok; ++k) ok = write_scales(k);
     for (int k = 0; k < n && ok; ++k) {
-      if (k + C::kLook < n && !write_scales(k + C::kLook)) break;
       const int db = k % C::kND;
-      if (!__all_sync(0xffffffffu, wait_or_abort(&dfull[db], (k / C::kND) & 1, abort_flag, p.hdr))) break;
+      // Until stage k's product is complete, write the scale factors of every stage whose copy has landed and
+      // whose scale buffer the products of stage ks - kNSF have finished with (their epilogue has begun), so
+      // the products never wait for this loop to come round to them. Both barriers are polled; a round that
+      // finds neither ready sleeps briefly.
+      uint32_t spins = 0;
+      for (;;) {
+        if (ks < n && ks < k + C::kNSF &&
+            __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&full[ks % C::kStages]), (ks / C::kStages) & 1))) {
+          put_scales(ks++);
+          continue;
+        }
+        if (ks > k && __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&dfull[db]), (k / C::kND) & 1))) break;
+        if (++spins >= kSpinLimit * 8u) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            report(p.hdr, CSA_ERR_TIMEOUT, KID_INDEX_SCORE, blockIdx.x);
+          }
+          ok = false;
+          break;
+        }
+        if ((spins & 7u) == 7u && __any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+        __nanosleep(32);
+      }
+      if (!ok) break;
       tc::fence_after();
       const int64_t st = k0 + k;
       const int64_t slot0 = st * kStageBlocks;
