@@ -710,9 +710,6 @@ def e2e_pipelined(w, host_in, args, world, device, comp):
 # reports traffic as null.
 TRAFFIC = {
     ("decode_64k_b32_h64", "sparse_attn"): 25_287_168 + 6_912,
-    # python bench.py --workload project_pack_128k_h4096 --steps 1 --warmup 3 --no-cpu-baseline --min-seconds 0
-    #   --replicas 1 (ncu reports these in GB / MB with six digits)
-    ("project_pack_128k_h4096", "project_pack"): 1_108_507_000 + 20_185_856,
 }
 
 
