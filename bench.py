@@ -709,6 +709,9 @@ def e2e_pipelined(w, host_in, args, world, device, comp):
 # under ncu -k regex:<kernel> -s 2 -c 1. An entry is removed when its kernel changes; the roofline then
 # reports traffic as null.
 TRAFFIC = {
+    # python bench.py --workload project_pack_128k_h4096 --steps 1 --warmup 3 --no-cpu-baseline --min-seconds 0
+    #   --replicas 1 (ncu reports these in GB / MB with six digits)
+    ("project_pack_128k_h4096", "project_pack"): 1_102_514_000 + 19_863_808,
     ("decode_64k_b32_h64", "sparse_attn"): 25_287_168 + 6_912,
 }
 
