@@ -53,6 +53,7 @@ def _cases():
         "chain20_128k_b64_h64": synth.CHAIN_128K_B64,
         "prefill_2048_at_128k_h64": synth.PREFILL_2K_AT_128K,
         "decode_64k_b32_h64_q4": synth.DECODE_64K_B32_Q4,
+        "decode_64k_b32_h64_nvfp4q": synth.DECODE_64K_B32_NVFP4Q,
         "project_pack_128k_h4096": synth.PROJECT_128K_H4096,
     }
 
@@ -166,7 +167,7 @@ class DecodeWorkload:
         # every layer (indexer for Full / Reindex, attention) through the library's multi-layer entry point
         layers, n_idx = [], 0
         for layer, mode in enumerate(self.modes):
-            ent = {"mode": mode, "q": q[layer], "swa": self.swa[layer],
+            ent = {"mode": mode, "q": q[layer], "swa": self.swa[layer], "nvfp4q": c.nvfp4q,
                    "out": out if layer_outs is None else layer_outs[layer]}
             if mode != "reuse":
                 ent["q_idx"] = q_idx[n_idx % q_idx.shape[0]]

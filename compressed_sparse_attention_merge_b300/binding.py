@@ -70,7 +70,7 @@ class AttnArgs(ctypes.Structure):
 
 
 class LayerArgs(ctypes.Structure):
-    _fields_ = [("mode", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("q_idx", ctypes.c_void_p),
+    _fields_ = [("mode", ctypes.c_int32), ("flags", ctypes.c_int32), ("q_idx", ctypes.c_void_p),
                 ("idx", ctypes.c_void_p), ("q", ctypes.c_void_p), ("swa", ctypes.c_void_p), ("out", ctypes.c_void_p),
                 ("out_lse", ctypes.c_void_p)]
 
@@ -115,7 +115,8 @@ def lib():
         L.csa_index_topk_static.argtypes = [I64, ctypes.POINTER(IndexArgs), P, P]
         L.csa_sparse_attn_workspace_size.restype = SZ
         L.csa_sparse_attn_workspace_size.argtypes = [I64, ctypes.POINTER(AttnArgs)]
-        for name in ("csa_sparse_attn_decode", "csa_sparse_attn_prefill"):
+        for name in ("csa_sparse_attn_decode", "csa_sparse_attn_prefill", "csa_sparse_attn_decode_nvfp4q",
+                     "csa_sparse_attn_prefill_nvfp4q"):
             f = getattr(L, name)
             f.restype = I32
             f.argtypes = [I64, ctypes.POINTER(AttnArgs), P, SZ, P]
@@ -399,19 +400,40 @@ def sparse_attn_prefill(q, cache, n_entries, idx, out, *, q_pos, max_entries, wi
            "csa_sparse_attn_prefill")
 
 
+def sparse_attn_decode_nvfp4q(q, cache, n_entries, idx, out, *, max_entries, window, scale, ws, swa=None,
+                              swa_len=None, out_lse=None, stream=None):
+    """csa_sparse_attn_decode_nvfp4q: sparse_attn_decode with the logits on the block-scaled FP4 tensor cores
+    (query heads and window keys rounded to FP4 inside the logits; values exact)."""
+    a = attn_args(q, cache, n_entries, idx, out, max_entries=max_entries, window=window, scale=scale, swa=swa,
+                  swa_len=swa_len, out_lse=out_lse)
+    _check(lib().csa_sparse_attn_decode_nvfp4q(q.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(), _stream(stream)),
+           "csa_sparse_attn_decode_nvfp4q")
+
+
+def sparse_attn_prefill_nvfp4q(q, cache, n_entries, idx, out, *, q_pos, max_entries, window, scale, ws, swa=None,
+                               swa_first_pos=None, out_lse=None, stream=None):
+    """csa_sparse_attn_prefill_nvfp4q: sparse_attn_prefill with the NVFP4-query logits."""
+    a = attn_args(q, cache, n_entries, idx, out, max_entries=max_entries, window=window, scale=scale, swa=swa,
+                  swa_first_pos=swa_first_pos, q_pos=q_pos, out_lse=out_lse)
+    _check(lib().csa_sparse_attn_prefill_nvfp4q(q.shape[0], ctypes.byref(a), _ptr(ws), ws.numel(),
+                                                _stream(stream)), "csa_sparse_attn_prefill_nvfp4q")
+
+
 LAYER_FULL, LAYER_REINDEX, LAYER_REUSE = 0, 1, 2
+LAYER_ATTN_NVFP4Q = 1
 _LAYER_MODES = {"full": LAYER_FULL, "reindex": LAYER_REINDEX, "reuse": LAYER_REUSE}
 
 
 def decode_layers(layers, *, index_tmpl, attn_tmpl, ws_index, ws_attn, stream=None):
     """csa_decode_layers: a step of several layers over one cache. layers: list of dicts with keys mode
     ("full" | "reindex" | "reuse"), q_idx and idx (Full / Reindex), q, swa (or None), out, out_lse (or
-    None). index_tmpl / attn_tmpl: IndexArgs / AttnArgs (from index_args / attn_args) holding the shared
+    None), and optionally nvfp4q (True: the layer's attention is the NVFP4-query variant). index_tmpl / attn_tmpl: IndexArgs / AttnArgs (from index_args / attn_args) holding the shared
     fields; a set q_pos in attn_tmpl makes the attention causal. The batch is taken from the first layer's q."""
     n = len(layers)
     arr = (LayerArgs * n)()
     for i, layer in enumerate(layers):
         arr[i].mode = _LAYER_MODES[layer["mode"]]
+        arr[i].flags = LAYER_ATTN_NVFP4Q if layer.get("nvfp4q") else 0
         if layer["mode"] != "reuse":
             arr[i].q_idx = _need(layer["q_idx"], "q_idx", torch.float32).data_ptr()
             arr[i].idx = _need(layer["idx"], "idx", torch.int32).data_ptr()

@@ -76,6 +76,14 @@ constexpr int kQScaleOff = kLsumOff + 64 * 4;              // float qscale[64]: 
 constexpr int kQMaxOff = kQScaleOff + 64 * 4;              // uint qmax[64]: bits of each head's largest |q|
 constexpr int kSmemBytes = kQMaxOff + 64 * 4;
 static_assert(kVOff % 1024 == 0 && kPOff % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
+// NVFP4-query mode: the query region holds the FP4 query (B operand of the block-scaled logits), its scale
+// bytes, and one stage of a tile's FP4 codes (A operand): block b of the tile at kRawOff + 2048 b, its 8 rows'
+// first 128 code bytes (latent 0-255) then their last 128, each an 8-row 128-byte-swizzled atom.
+constexpr int kQ4Off = 0;                                  // 2 K-halves x [64 heads x 128 B]: 16 KB
+constexpr int kQ4ScOff = kQ4Off + 2 * kHeadsPad * 128;     // 64 heads x 32 scale bytes: 2 KB
+constexpr int kRawOff = kQ4ScOff + kHeadsPad * 32;         // 16 blocks x 2 KB
+constexpr int kRawBytes = kTileBlocks * 2048;
+static_assert(kRawOff % 1024 == 0 && kRawOff + kRawBytes <= kVOff, "NVFP4-query operands fit the query region");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 enum Bar {
@@ -86,6 +94,10 @@ enum Bar {
   P_FULL = S_EMPTY + 2,                 // P buffers: softmax <-> values issuer and row sums
   P_EMPTY = P_FULL + 2,
   WIN_FULL = P_EMPTY + 2,               // a window tile's rows have landed in the values buffer
+  SFX_FULL,                             // NVFP4-query mode: a tile's key scale factors are in tensor memory
+                                        // (and a window tile's FP4 codes in the raw stage); one per parity
+  RAW_FULL = SFX_FULL + 2,              // NVFP4-query mode: a cache tile's codes have landed in the raw stage
+  RAW_DONE,                             // NVFP4-query mode: the logits of the tile in the raw stage are complete
   FIN_L, FIN_V, NUM_BARS
 };
 
@@ -96,9 +108,12 @@ constexpr int kGatherWarp = 12, kLogitsWarp = 13, kValuesWarp = 14, kSumWarp = 1
 constexpr int kThreads = 16 * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;   // S: two buffers of 64 columns; O^T: 4 x 64 columns
+// NVFP4-query mode: key scale factors, two buffers of 8 products x 4 columns; query scale factors, 8 x 4
+constexpr uint32_t kColSFA = 128, kColSFB = 192;
 
 constexpr uint32_t kIdescS = tc::idesc_f16_f32(128, kHeadsPad, 0, 0);   // C K-major, Q K-major
 constexpr uint32_t kIdescPV = tc::idesc_f16_f32(128, kHeadsPad, 1, 1);  // C^T MN-major, P^T MN-major
+constexpr uint32_t kIdescS4 = tc::idesc_mxf4(128, kHeadsPad);            // FP4 codes, FP4 query
 
 // Bounded wait that also gives up as soon as another role of the CTA has given up.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -150,6 +165,42 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
                " [%0], [%1, {%2, %3, %4}], [%5];"
                :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
                   "r"(smem_addr(bar)) : "memory");
+}
+
+// Tensor-map copy of one [8 x 128-byte] box (the code bytes of one cache block's 8 rows, one half of each
+// row) into shared memory, 128-byte swizzled.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w, uint64_t* bar) {
+  asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+               :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
+                  "r"(smem_addr(bar)) : "memory");
+}
+
+// One 16-element group rounded with the AMAX rule of the cache format (the rule csa_pack_fp4 applies): the
+// E4M3 scale byte of fl32(amax / 6) is returned, the E2M1 codes of fl32(v / s) go to *lo (elements 0-7) and
+// *hi (8-15), low nibble first; a zero scale gives zero codes.
+__device__ __forceinline__ uint32_t quant16_amax(const float* v, uint32_t* lo, uint32_t* hi) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  const float sf = __fdiv_rn(amax, 6.0f);
+  uint32_t sbyte = 0u;
+  float s = 0.0f;
+  if (sf > 0.0f) {
+    sbyte = float_to_e4m3_satfinite(sf);
+    s = e4m3_to_float(sbyte);
+  }
+  uint32_t c0 = 0u, c1 = 0u;
+  if (s > 0.0f) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      c0 |= e2m1_code(__fdiv_rn(v[k], s)) << (4 * k);
+      c1 |= e2m1_code(__fdiv_rn(v[k + 8], s)) << (4 * k);
+    }
+  }
+  *lo = c0;
+  *hi = c1;
+  return sbyte;
 }
 
 struct UnitCtx {
@@ -272,12 +323,28 @@ __device__ __forceinline__ void load_scales(const uint8_t* seq, int id, bool ok,
   for (int c = 0; c < 4; ++c) sc[c] = hp ? w[2 * c + 1] : w[2 * c];
 }
 
+// NVFP4-query mode: a converter writes the key scale factors of its row and its four panels (panels hp,
+// hp + 2, hp + 4, hp + 6 = block-scaled products of K = 64) of tile t into scale buffer t & 1 (row m's bytes
+// of product s at lane m, column kColSFA + 32 (t & 1) + 4 s + m / 32) and arrives on that buffer's barrier.
+__device__ __forceinline__ void put_key_scales(uint32_t tbase, int sp, int hp, int lane, int t, const uint32_t* sc,
+                                               uint64_t* bars) {
+  const uint32_t lb = (uint32_t)(sp * 32) << 16;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tc::st_32x1(tbase + lb + kColSFA + 32 * (t & 1) + 4 * (2 * c + hp) + sp, sc[c]);
+  tc::wait_st();
+  tc::fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&bars[SFX_FULL + (t & 1)]);
+}
+
 __device__ __forceinline__ uint32_t pick4(const uint32_t* v, int i) {
   return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
 }
 
+template <bool kQ4>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p,
-                                                               const __grid_constant__ CUtensorMap swa_map) {
+                                                               const __grid_constant__ CUtensorMap swa_map,
+                                                               const __grid_constant__ CUtensorMap cache_map) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + kTmemPtrOff);
@@ -339,6 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       mbar_init(&bars[P_EMPTY + i], 2);        // the values' commit and the row-sum warp
     }
     mbar_init(&bars[WIN_FULL], 1);
+    mbar_init(&bars[SFX_FULL], kConvWarps);
+    mbar_init(&bars[SFX_FULL + 1], kConvWarps);
+    mbar_init(&bars[RAW_FULL], 1);
+    mbar_init(&bars[RAW_DONE], 1);
     mbar_init(&bars[FIN_L], 1);
     mbar_init(&bars[FIN_V], 1);
     fence_mbar_init();
@@ -381,57 +452,141 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     const __nv_bfloat16* qg = p.q + u.unit * (int64_t)H * kLatent;
     uint32_t* qmax = reinterpret_cast<uint32_t*>(smem + kQMaxOff);
     float* qscale = reinterpret_cast<float*>(smem + kQScaleOff);
-    uint4 v[kQPer];
+    if constexpr (!kQ4) {
+      uint4 v[kQPer];
 #pragma unroll
-    for (int k = 0; k < kQPer; ++k) {
-      const int i = qt + k * kQThreads;
-      const int h = i >> 6, ch = i & 63;
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (i < kQItems && h < H) v[k] = ld_nc_v4(qg + (int64_t)h * kLatent + ch * 8);
-    }
-#pragma unroll
-    for (int k = 0; k < kQPer; ++k) {
-      const int i = qt + k * kQThreads;
-      if (i < kQItems) {
-        // magnitudes compare as integers: the bits of |x| with the sign cleared
-        // (the 32 lanes of a warp hold 32 consecutive items starting at a multiple of 32, so all lie in one
-        // head's 64 and the warp reduces them before one atomic; the branch is uniform per warp, since
-        // kQItems and kQThreads are multiples of 32)
-        uint32_t m = 0u;
-        const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
-        m = __reduce_max_sync(0xffffffffu, m);
-        if (lane == 0) atomicMax(qmax + (i >> 6), m);
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = qt + k * kQThreads;
+        const int h = i >> 6, ch = i & 63;
+        v[k] = make_uint4(0, 0, 0, 0);
+        if (i < kQItems && h < H) v[k] = ld_nc_v4(qg + (int64_t)h * kLatent + ch * 8);
       }
-    }
-    asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
 #pragma unroll
-    for (int k = 0; k < kQPer; ++k) {
-      const int i = qt + k * kQThreads;
-      if (i < kQItems) {
-        const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
-        const uint32_t mb = qmax[h];
-        int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;    // exponent of the largest |q|, - 14
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = qt + k * kQThreads;
+        if (i < kQItems) {
+          // magnitudes compare as integers: the bits of |x| with the sign cleared
+          // (the 32 lanes of a warp hold 32 consecutive items starting at a multiple of 32, so all lie in one
+          // head's 64 and the warp reduces them before one atomic; the branch is uniform per warp, since
+          // kQItems and kQThreads are multiples of 32)
+          uint32_t m = 0u;
+          const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
+          m = __reduce_max_sync(0xffffffffu, m);
+          if (lane == 0) atomicMax(qmax + (i >> 6), m);
+        }
+      }
+      asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+#pragma unroll
+      for (int k = 0; k < kQPer; ++k) {
+        const int i = qt + k * kQThreads;
+        if (i < kQItems) {
+          const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
+          const uint32_t mb = qmax[h];
+          int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;    // exponent of the largest |q|, - 14
+          sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+          const float f = __int_as_float((127 - sh) << 23);                  // 2^-sh, exact
+          const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[j] = f2_to_h2(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+          *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      if (qt < 64) {
+        const uint32_t mb = qmax[qt];
+        int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;
         sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-        const float f = __int_as_float((127 - sh) << 23);                  // 2^-sh, exact
-        const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = f2_to_h2(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f);
-        *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);      // scale_log2 * 2^sh
       }
-    }
-    if (qt < 64) {
-      const uint32_t mb = qmax[qt];
-      int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;
-      sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-      qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);      // scale_log2 * 2^sh
+    } else {
+      // NVFP4 query: head h is scaled by 2^-k_h, k_h = floor(log2 max|q_h|) - 10 (clamped to [-100, 100]),
+      // which puts every 16-element block's amax / 6 below 342, inside the E4M3 scale range, and each block
+      // is rounded with the cache format's AMAX rule. The codes form the B operand of the block-scaled
+      // logits (two K-halves of [64 heads x 128 bytes], 128-byte swizzle), the scale bytes go to tensor
+      // memory below, and 2^k_h goes into the head's softmax scale. An item is one block of 16 elements.
+      constexpr int kQ4Items = kHeadsPad * 32;
+      constexpr int kQ4Per = (kQ4Items + kQThreads - 1) / kQThreads;
+      static_assert(kQThreads % 32 == 0, "the 32 blocks of a head lie in one warp's items");
+      uint4 v[2 * kQ4Per];
+#pragma unroll
+      for (int k = 0; k < kQ4Per; ++k) {
+        const int i = qt + k * kQThreads;
+        const int h = i >> 5, g = i & 31;
+        v[2 * k] = make_uint4(0, 0, 0, 0);
+        v[2 * k + 1] = make_uint4(0, 0, 0, 0);
+        if (i < kQ4Items && h < H) {
+          v[2 * k] = ld_nc_v4(qg + (int64_t)h * kLatent + g * 16);
+          v[2 * k + 1] = ld_nc_v4(qg + (int64_t)h * kLatent + g * 16 + 8);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kQ4Per; ++k) {
+        const int i = qt + k * kQThreads;
+        if (i < kQ4Items) {
+          uint32_t m = 0u;
+          const uint32_t w8[8] = {v[2 * k].x, v[2 * k].y, v[2 * k].z, v[2 * k].w,
+                                  v[2 * k + 1].x, v[2 * k + 1].y, v[2 * k + 1].z, v[2 * k + 1].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m = max(m, max(w8[j] & 0x7FFFu, (w8[j] >> 16) & 0x7FFFu));
+          m = __reduce_max_sync(0xffffffffu, m);
+          if (lane == 0) atomicMax(qmax + (i >> 5), m);
+        }
+      }
+      asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+#pragma unroll
+      for (int k = 0; k < kQ4Per; ++k) {
+        const int i = qt + k * kQThreads;
+        if (i < kQ4Items) {
+          const int h = i >> 5, g = i & 31;
+          const uint32_t mb = qmax[h];
+          int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 10;
+          sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+          const float f = __int_as_float((127 - sh) << 23);                // 2^-sh, exact
+          const uint32_t w8[8] = {v[2 * k].x, v[2 * k].y, v[2 * k].z, v[2 * k].w,
+                                  v[2 * k + 1].x, v[2 * k + 1].y, v[2 * k + 1].z, v[2 * k + 1].w};
+          float x[16];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            x[2 * j] = __fmul_rn(__uint_as_float(w8[j] << 16), f);
+            x[2 * j + 1] = __fmul_rn(__uint_as_float(w8[j] & 0xFFFF0000u), f);
+          }
+          uint32_t lo, hi;
+          const uint32_t sbyte = quant16_amax(x, &lo, &hi);
+          const int cc = (g & 15) >> 1;                                    // 16-byte chunk within the 128-byte row
+          *reinterpret_cast<uint2*>(smem + kQ4Off + (g >> 4) * (kHeadsPad * 128) + h * 128 + ((cc ^ (h & 7)) << 4) +
+                                    (g & 1) * 8) = make_uint2(lo, hi);
+          smem[kQ4ScOff + h * 32 + g] = (uint8_t)sbyte;
+        }
+      }
+      if (qt < 64) {
+        const uint32_t mb = qmax[qt];
+        int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 10;
+        sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+        qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);    // scale_log2 * 2^sh
+      }
+      asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+      if (warp < 4) {
+        // query scale factors: head n's four bytes of product s at lane 32 j + n % 32 (every subpartition j
+        // holds a copy; warp w writes subpartition w), column kColSFB + 4 s + n / 32
+        const uint32_t lb = (uint32_t)(warp * 32) << 16;
+#pragma unroll
+        for (int s8 = 0; s8 < 8; ++s8) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tc::st_32x1(tbase + lb + kColSFB + 4 * s8 + c,
+                        *reinterpret_cast<const uint32_t*>(smem + kQ4ScOff + (lane + 32 * c) * 32 + 4 * s8));
+        }
+        tc::wait_st();
+      }
     }
     if (qt < 64) msh[qt] = -INFINITY;
     tc::fence_proxy_async();
+    tc::fence_before();
     asm volatile("bar.sync 2, %0;" :: "n"(kThreads) : "memory");
+    tc::fence_after();
     if (is_conv) {
       griddep_wait();                                // the index list comes from the kernel before
       id_c = n_cache > 0 ? cache_id(p, u, c0, row) : -1;
@@ -447,6 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       load_scales(seq, id_n, n_cache > 1 && cache_ok(u, id_n, row), row, hp, sc_n);
       qs0 = sc_c[0];
       qs1 = sc_c[1];
+      // NVFP4-query mode: the key scale factors of the first tile when it is a cache tile (a later cache
+      // tile's are written while the tile before it is converted)
+      if (kQ4 && nw == 0 && n_cache > 0) put_key_scales(tbase, sp, hp, lane, 0, sc_c, bars);
     }
   } else {
     // the gather warp starts its L2 prefetches once the queries have arrived, so that the queries and the
@@ -503,6 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         vr = window_row(p, u, it, row, &oob);
         if (oob && hp == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
         if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], it & 1, abort_flag, p.hdr, 10, p.spin_limit))) break;
+        // NVFP4-query mode: the first cache tile's key scale factors, one tile ahead
+        if (kQ4 && it + 1 == nw && n_cache > 0) put_key_scales(tbase, sp, hp, lane, it + 1, sc_c, bars);
       }
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
@@ -513,9 +673,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           // bf16 -> fp16 of this row's 64 columns, in place; rows that are not attended become zero. A value
           // beyond the fp16 range (|x| > 65504, outside the call's contract) becomes infinite: reported.
           uint32_t inf = 0u;
+          uint4 xw[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint4 x = *reinterpret_cast<const uint4*>(vrow + ((j ^ (row & 7)) << 4));
+            xw[j] = vr ? x : make_uint4(0u, 0u, 0u, 0u);
             h[4 * j] = vr ? bf2_to_h2(x.x) : 0u; h[4 * j + 1] = vr ? bf2_to_h2(x.y) : 0u;
             h[4 * j + 2] = vr ? bf2_to_h2(x.z) : 0u; h[4 * j + 3] = vr ? bf2_to_h2(x.w) : 0u;
 #pragma unroll
@@ -523,6 +685,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
               inf |= ((h[4 * j + e] & 0x7C00u) == 0x7C00u) | ((h[4 * j + e] & 0x7C000000u) == 0x7C000000u);
           }
           if (inf) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
+          if constexpr (kQ4) {
+            // NVFP4-query mode: the window row's keys for the logits, rounded from the exact bf16 values
+            // with the cache format's AMAX rule: four groups of 16 -> 32 code bytes into the raw stage (the
+            // layout of a copied cache tile) and four scale bytes into this tile's scale buffer
+            uint32_t cw[8], sw = 0u;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const uint32_t w8[8] = {xw[2 * g].x, xw[2 * g].y, xw[2 * g].z, xw[2 * g].w,
+                                      xw[2 * g + 1].x, xw[2 * g + 1].y, xw[2 * g + 1].z, xw[2 * g + 1].w};
+              float v[16];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                v[2 * e] = __uint_as_float(w8[e] << 16);
+                v[2 * e + 1] = __uint_as_float(w8[e] & 0xFFFF0000u);
+              }
+              sw |= quant16_amax(v, &cw[2 * g], &cw[2 * g + 1]) << (8 * g);
+            }
+            tc::st_32x1(tbase + ((uint32_t)(sp * 32) << 16) + kColSFA + 32 * (it & 1) + 4 * pnl + sp, sw);
+            uint8_t* rrow = smem + kRawOff + (row >> 3) * 2048 + (pnl >> 2) * 1024 + (row & 7) * 128;
+            const int j0 = (pnl & 3) * 2;
+            *reinterpret_cast<uint4*>(rrow + ((j0 ^ (row & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            *reinterpret_cast<uint4*>(rrow + (((j0 + 1) ^ (row & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+          }
         } else {
           dequant_panel(q0, qs0, h);
 #pragma unroll
@@ -544,12 +729,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           stop = true;
           break;
         }
+        // NVFP4-query mode: the next cache tile's key scale factors go in once the value products of tile it - 1
+        // have begun to free this tile's buffer (its logits, the last reader of that scale buffer, are complete)
+        if (kQ4 && !win && c == 0 && it + 1 < n_tiles) put_key_scales(tbase, sp, hp, lane, it + 1, sc_n, bars);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           *reinterpret_cast<uint4*>(vrow + ((j ^ (row & 7)) << 4)) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
         tc::fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[V_FULL + c]);
+      }
+      if (kQ4 && win && !stop) {
+        // the window tile's FP4 keys and scale factors are written
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[SFX_FULL + (it & 1)]);
       }
       if (!win) {
         // the scales of tile k + 2 are loaded a tile before the queue reaches it, its id one more tile earlier
@@ -561,6 +756,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         id_nn = k + 3 < n_cache ? cache_id(p, u, c0 + k + 3, row) : -1;
       }
     }
+  } else if (kQ4 && warp == kLogitsWarp) {
+    // ---------------- NVFP4-query logits: S^T(t) = C . Q4^T by block-scaled FP4 products ----------------
+    // A cache tile's codes are copied by tensor map into the raw stage (16 blocks, two boxes each) once the
+    // previous tile's logits are complete; a window tile's FP4 keys are written there by the converters.
+    // The key scale factors come from the converters, one tile ahead, so the logits never wait for the
+    // values buffer.
+    griddep_wait();                                  // the index list comes from the kernel before
+    bool ok = true;
+    int raw_issued = 0;
+    int nid = (n_cache > 0 && lane < kTileBlocks) ? cache_id(p, u, c0, lane << 3) : -1;
+    for (int it = 0; it < n_tiles && ok; ++it) {
+      const int sb = it & 1;
+      if (it >= nw) {
+        const int k = it - nw;
+        if (it > 0 && !wait_bar_warp(&bars[RAW_DONE], (it - 1) & 1, abort_flag, p.hdr, 14, p.spin_limit)) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[RAW_FULL], kRawBytes);
+        __syncwarp();
+        if (lane < kTileBlocks) {
+          uint8_t* dst = smem + kRawOff + lane * 2048;
+          tma_load_4d(dst, &cache_map, 0, 0, nid, (int)u.b, &bars[RAW_FULL]);
+          tma_load_4d(dst + 1024, &cache_map, 128, 0, nid, (int)u.b, &bars[RAW_FULL]);
+        }
+        ++raw_issued;
+        nid = (k + 1 < n_cache && lane < kTileBlocks) ? cache_id(p, u, c0 + k + 1, lane << 3) : -1;
+        if (!wait_bar_warp(&bars[RAW_FULL], k & 1, abort_flag, p.hdr, 15, p.spin_limit)) break;
+      }
+      if (!wait_bar_warp(&bars[SFX_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 16, p.spin_limit)) break;
+      if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4, p.spin_limit)) break;
+      tc::fence_after();
+      const uint32_t d = tbase + kColS + 64 * sb;
+#pragma unroll
+      for (int s8 = 0; s8 < 8; ++s8) {
+        const uint64_t a = tc::smem_desc(s_base + kRawOff + (s8 >> 2) * 1024 + (s8 & 3) * 32, 16, 2048, tc::kSwizzle128B);
+        const uint64_t b = tc::smem_desc(s_base + kQ4Off + (s8 >> 2) * (kHeadsPad * 128) + (s8 & 3) * 32, 16, 1024,
+                                         tc::kSwizzle128B);
+        tc::mma_mxf4_warp(d, a, b, kIdescS4, tbase + kColSFA + 32 * sb + 4 * s8, tbase + kColSFB + 4 * s8, s8 > 0 ? 1u : 0u);
+      }
+      tc::commit_warp(&bars[S_FULL + sb]);
+      tc::commit_warp(&bars[RAW_DONE]);
+    }
+    // every MMA issued must be complete before the tensor memory is released, and no copy may still be in
+    // flight into this CTA's shared memory when it exits
+    tc::commit_warp(&bars[FIN_L]);
+    drain_bar(&bars[FIN_L], 0);
+    if (raw_issued > 0) drain_bar(&bars[RAW_FULL], (raw_issued - 1) & 1);
+    __syncwarp();
   } else if (warp == kLogitsWarp) {
     // ---------------- logits MMA issue: S^T(t) = C . Q^T into S buffer t & 1 ----------------
     const uint32_t q_addr = s_base + kQOff;
@@ -700,8 +941,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int h = 8 * c + 2 * k;
-              const float p0 = valid ? ex2(__uint_as_float(sr[h]) * ss[2 * k] - mm[2 * k]) : 0.0f;
-              const float p1 = valid ? ex2(__uint_as_float(sr[h + 1]) * ss[2 * k + 1] - mm[2 * k + 1]) : 0.0f;
+              // the scaled logit is rounded before the maximum is subtracted, as it was when the maximum was
+              // taken, so the largest row gives exactly 2^0 at any magnitude (a fused multiply-add would leave
+              // the product's rounding error in the exponent, which overflows for logits beyond 2^27)
+              const float p0 = valid ? ex2(__fmul_rn(__uint_as_float(sr[h]), ss[2 * k]) - mm[2 * k]) : 0.0f;
+              const float p1 = valid ? ex2(__fmul_rn(__uint_as_float(sr[h + 1]), ss[2 * k + 1]) - mm[2 * k + 1]) : 0.0f;
               over |= !(p0 <= kMaxProb) || !(p1 <= kMaxProb);
               w[k] = f2_to_h2(p0, p1);
             }
@@ -720,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           tc::wait_ld();
           float v[32];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = valid ? __uint_as_float(sr[h]) * qsc[32 * half + h] : -INFINITY;
+          for (int h = 0; h < 32; ++h) v[h] = valid ? __fmul_rn(__uint_as_float(sr[h]), qsc[32 * half + h]) : -INFINITY;
 #pragma unroll
           for (int n = 16, o = 16; n >= 1; n >>= 1, o >>= 1) {
             const bool up = (lane & o) != 0;
@@ -930,12 +1174,38 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  // NVFP4-query mode: the cache's code bytes as a [batch][block][slot][256] byte tensor (block stride 2,304,
+  // the scale bytes after each block's codes are skipped), copied in [8 x 128] boxes, one half of each of a
+  // block's 8 rows, with the 128-byte swizzle of the block-scaled operand; ids outside the tensor read as zero
+  CUtensorMap cmap;
+  std::memset(&cmap, 0, sizeof(cmap));
+  if (p.q4) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const int64_t nb_cap = (p.max_entries + kBlockEntries - 1) / kBlockEntries;
+    const int64_t batch = p.units / p.n_query;
+    const cuuint64_t dims[4] = {256, (cuuint64_t)kBlockEntries, (cuuint64_t)(nb_cap > 0 ? nb_cap : 1), (cuuint64_t)batch};
+    const int64_t sb = batch > 1 ? p.cache_stride_b : (nb_cap > 0 ? nb_cap : 1) * kLatBlk;
+    const cuuint64_t strides[3] = {256, (cuuint64_t)kLatBlk, (cuuint64_t)sb};
+    const cuuint32_t box[4] = {128, (cuuint32_t)kBlockEntries, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(&cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.cache), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   ProfScope prof("sparse_attn", s);
   clear_stale_error();
-  cudaError_t e = ensure_smem_limit(attn_tc_kernel, kSmemBytes);
+  if (p.q4) {
+    cudaError_t e = ensure_smem_limit(attn_tc_kernel<true>, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return launch_ex(attn_tc_kernel<true>, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads),
+                     (size_t)kSmemBytes, s, pdl, p, map, cmap);
+  }
+  cudaError_t e = ensure_smem_limit(attn_tc_kernel<false>, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_ex(attn_tc_kernel, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads), (size_t)kSmemBytes, s,
-                   pdl, p, map);
+  return launch_ex(attn_tc_kernel<false>, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads),
+                   (size_t)kSmemBytes, s, pdl, p, map, cmap);
 }
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s, bool pdl) {

@@ -510,7 +510,7 @@ size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* a) {
 // it, which is only right when that kernel belongs to the same call (the attention loads the call's queries
 // and window rows before it waits).
 static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream,
-                              bool prefill, bool early) {
+                              bool prefill, bool early, bool q4 = false) {
   csa_status st = validate_attn(batch, a, prefill);
   if (st != CSA_OK) return st;
   int num_sms = 0;
@@ -536,6 +536,7 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.part_ml = reinterpret_cast<float*>(w + L.ml_off);
   p.out = a->out; p.out_lse = a->out_lse;
   p.hdr = reinterpret_cast<uint32_t*>(w);
+  p.q4 = q4 ? 1 : 0;
   debug_fault(&p.fault, &p.spin_limit);
   if (cudaError_t e = launch_attn(p, stream, early)) return cuda_fail(e, "attn");
   if (cudaError_t e = launch_combine(p, stream, true)) return cuda_fail(e, "combine");
@@ -552,6 +553,16 @@ csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* a, void* 
   return sparse_attn(batch, a, ws, ws_bytes, stream, true, false);
 }
 
+csa_status csa_sparse_attn_decode_nvfp4q(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream) {
+  return sparse_attn(batch, a, ws, ws_bytes, stream, false, false, true);
+}
+
+csa_status csa_sparse_attn_prefill_nvfp4q(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
+  return sparse_attn(batch, a, ws, ws_bytes, stream, true, false, true);
+}
+
 // ------------------------------------------------------------------------------------------------
 csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* layers,
                              const csa_index_args* index_tmpl, const csa_attn_args* attn_tmpl, void* ws_index,
@@ -565,6 +576,7 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
     const csa_layer_args& L = layers[l];
     if (L.mode != CSA_LAYER_FULL && L.mode != CSA_LAYER_REINDEX && L.mode != CSA_LAYER_REUSE) return CSA_ERR_INVALID_ARG;
     if (L.mode == CSA_LAYER_REUSE && src == nullptr) return CSA_ERR_INVALID_ARG;
+    if ((L.flags & ~CSA_LAYER_ATTN_NVFP4Q) != 0) return CSA_ERR_INVALID_ARG;
     if (L.mode != CSA_LAYER_REUSE) {
       csa_index_args ia = *index_tmpl;
       ia.q_idx = L.q_idx;
@@ -605,7 +617,8 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
     aa.swa = L.swa;
     aa.out = L.out;
     aa.out_lse = L.out_lse;
-    const csa_status st = sparse_attn(batch, &aa, ws_attn, ws_attn_bytes, stream, causal, true);
+    const csa_status st = sparse_attn(batch, &aa, ws_attn, ws_attn_bytes, stream, causal, true,
+                                      (L.flags & CSA_LAYER_ATTN_NVFP4Q) != 0);
     if (st != CSA_OK) return st;
   }
   return CSA_OK;

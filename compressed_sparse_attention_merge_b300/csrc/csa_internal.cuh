@@ -261,6 +261,7 @@ struct AttnParams {
   float* out;                  // used when splits == 1
   float* out_lse;
   uint32_t* hdr;
+  int q4;                      // host side: the NVFP4-query variant (block-scaled FP4 logits)
   // Bounded waits give up after this many polls (kSpinLimit unless a test lowered it), and a nonzero
   // fault makes the kernel withhold one arrival (csa_debug_set_fault).
   uint32_t spin_limit;

@@ -67,6 +67,19 @@ __device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t a, uint64
                :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
+// Instruction descriptor of kind::mxf4nvf4: E2M1 A and B (K-major), UE4M3 scale factors, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Block-scaled FP4 product, K = 64, one UE4M3 scale per 16 elements (scale_vec::4X), issued by one elected
+// lane of a converged warp. The scale factors of A row m for this product are four bytes at tensor-memory
+// lane m, column sfa + m / 32; those of B column n at lane 32 j + n % 32 (every j), column sfb + n / 32.
+__device__ __forceinline__ void mma_mxf4_warp(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                              uint32_t sfb, uint32_t acc) {
+  asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %6, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+               "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+               :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc) : "memory");
+}
 __device__ __forceinline__ void commit_warp(uint64_t* bar) {
   asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
                "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
@@ -156,6 +169,10 @@ __device__ __forceinline__ void st_32x32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// 32 lanes x 1 column of 32 bits.
+__device__ __forceinline__ void st_32x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -83,6 +83,7 @@ class DecodeCase:
     layers: int = 1               # > 1: layer chain with per-layer queries and windows
     distinct_index_queries: int = 1
     causal_drafts: bool = False
+    nvfp4q: bool = False          # attention by the NVFP4-query variant (block-scaled FP4 logits)
     seed: int = 0
     swa_len: list = field(default_factory=list)
 
@@ -214,6 +215,9 @@ PREFILL_2K_AT_128K = PrefillCase("prefill_2048_at_128k_h64", context=131072, chu
 # last four tokens of each sequence, causal among themselves.
 DECODE_64K_B32_Q4 = DecodeCase("decode_64k_b32_h64_q4", tokens=[65536] * 32, n_query=4, outlier_frac=0.01,
                                needle_frac=0.01, causal_drafts=True, seed=20266)
+# The decode workload above with the opt-in NVFP4-query attention (same inputs, same seed).
+DECODE_64K_B32_NVFP4Q = DecodeCase("decode_64k_b32_h64_nvfp4q", tokens=[65536] * 32, outlier_frac=0.01,
+                                   needle_frac=0.01, nvfp4q=True, seed=20262)
 
 # The cache write path over one 128K-token sequence with a 4,096-wide hidden state (the pages give no hidden
 # width; 4,096 is a common one for a model of this size class).

@@ -398,6 +398,30 @@ csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* args, voi
                                    cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * csa_sparse_attn_decode_nvfp4q / csa_sparse_attn_prefill_nvfp4q -- the same attention with the logits taken
+ * on the block-scaled FP4 tensor cores (opt-in; an approximation of the calls above).
+ *
+ * [card] Key ideas, "FP4 global KV, trained that way", stores the global KV in FP4 with one scale per
+ * 16 elements, the operand format of the block-scaled FP4 product, which needs both operands in FP4. The
+ * pages give no query format; this variant is the library's reading. It computes what
+ * csa_sparse_attn_decode / csa_sparse_attn_prefill compute (same rows, eligibility, window, outputs and
+ * workspace) with two roundings inside the logits z_c = scale * (q4_h . k_c):
+ *   q4_h  each query head scaled by 2^-e_h, e_h = floor(log2 max|q_h|) - 10 clamped to [-100, 100] (0 for an
+ *         all-zero head), rounded like csa_pack_fp4 with CSA_SCALE_AMAX (per 16 elements an E4M3 scale of
+ *         amax / 6, E2M1 codes), and scaled back by 2^e_h;
+ *   k_c   a cache row as stored; a window row rounded like csa_pack_fp4 with CSA_SCALE_AMAX (no merge, no
+ *         pre-scale; magnitudes above 2688 saturate).
+ * Values are exact: out[u][h] = sum_c softmax(z)_c * c uses the dequantized cache rows and the bf16 window
+ * rows, as in the exact calls. Logits are accumulated in fp32. The cache's code bytes are read by
+ * tensor-map copies (the cache's 32-byte alignment and stride rule apply, as above); all other argument
+ * rules and error behaviour are those of the exact calls.
+ * ------------------------------------------------------------------------------------------------ */
+csa_status csa_sparse_attn_decode_nvfp4q(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+csa_status csa_sparse_attn_prefill_nvfp4q(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
+                                          cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------------
  * csa_decode_layers -- a step of several layers over one shared cache: for every layer in order, the
  * indexer (Full and Reindex layers) and the sparse attention.
  *
@@ -418,10 +442,13 @@ csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* args, voi
  * anything is launched; the first layer may not be a Reuse layer.
  * ------------------------------------------------------------------------------------------------ */
 enum { CSA_LAYER_FULL = 0, CSA_LAYER_REINDEX = 1, CSA_LAYER_REUSE = 2 };
+/* Layer flags. CSA_LAYER_ATTN_NVFP4Q: the layer's attention is the NVFP4-query variant
+ * (csa_sparse_attn_decode_nvfp4q / csa_sparse_attn_prefill_nvfp4q). Other bits must be 0. */
+enum { CSA_LAYER_ATTN_NVFP4Q = 1 };
 
 typedef struct csa_layer_args {
   int32_t mode;
-  int32_t reserved0;
+  int32_t flags;
   const float* q_idx;   /* indexer queries [batch][n_query][heads][dim] (Full / Reindex) */
   int32_t* idx;         /* Top-K output [batch][n_query][top_k] (Full / Reindex) */
   const void* q;        /* attention queries, bf16 [batch][n_query][heads][512] */

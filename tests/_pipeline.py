@@ -90,28 +90,30 @@ def gpu_index(csa, q_idx, keys_cache, n_entries, max_entries, top_k, coarse=None
     return out, scores
 
 
-def gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, max_entries, window, want_lse=True):
+def gpu_decode_attn(csa, q, cache, n_entries, idx, swa, swa_len, max_entries, window, want_lse=True, nvfp4q=False):
     B, Q, H = q.shape[0], q.shape[1], q.shape[2]
     out = torch.empty(B, Q, H, 512, dtype=torch.float32, device=q.device)
     lse = torch.empty(B, Q, H, dtype=torch.float32, device=q.device) if want_lse else None
     args = csa.attn_args(q, cache, n_entries, idx, out, max_entries=max_entries, window=window, scale=SCALE,
                          swa=swa, swa_len=swa_len, out_lse=lse)
     ws = csa.workspace(csa.sparse_attn_workspace_size(B, args), q.device)
-    csa.sparse_attn_decode(q, cache, n_entries, idx, out, max_entries=max_entries, window=window, scale=SCALE,
-                           ws=ws, swa=swa, swa_len=swa_len, out_lse=lse)
+    fn = csa.sparse_attn_decode_nvfp4q if nvfp4q else csa.sparse_attn_decode
+    fn(q, cache, n_entries, idx, out, max_entries=max_entries, window=window, scale=SCALE, ws=ws, swa=swa,
+       swa_len=swa_len, out_lse=lse)
     assert csa.device_status(ws) == csa.OK
     return out, lse
 
 
-def gpu_prefill_attn(csa, q, cache, n_entries, idx, q_pos, swa, swa_first_pos, max_entries, window):
+def gpu_prefill_attn(csa, q, cache, n_entries, idx, q_pos, swa, swa_first_pos, max_entries, window, nvfp4q=False):
     B, Q, H = q.shape[0], q.shape[1], q.shape[2]
     out = torch.empty(B, Q, H, 512, dtype=torch.float32, device=q.device)
     lse = torch.empty(B, Q, H, dtype=torch.float32, device=q.device)
     args = csa.attn_args(q, cache, n_entries, idx, out, max_entries=max_entries, window=window, scale=SCALE,
                          swa=swa, swa_first_pos=swa_first_pos, q_pos=q_pos, out_lse=lse)
     ws = csa.workspace(csa.sparse_attn_workspace_size(B, args), q.device)
-    csa.sparse_attn_prefill(q, cache, n_entries, idx, out, q_pos=q_pos, max_entries=max_entries, window=window,
-                            scale=SCALE, ws=ws, swa=swa, swa_first_pos=swa_first_pos, out_lse=lse)
+    fn = csa.sparse_attn_prefill_nvfp4q if nvfp4q else csa.sparse_attn_prefill
+    fn(q, cache, n_entries, idx, out, q_pos=q_pos, max_entries=max_entries, window=window, scale=SCALE, ws=ws,
+       swa=swa, swa_first_pos=swa_first_pos, out_lse=lse)
     assert csa.device_status(ws) == csa.OK
     return out, lse
 

@@ -2,6 +2,7 @@
 modes of the chain workload against the oracle's, and the workload table against the shapes the method's
 configurations state."""
 
+import dataclasses
 import bench
 from oracle import chain
 
@@ -43,8 +44,12 @@ def test_workload_table():
     assert (p.chunk, p.max_entries, p.first_pos) == (2048, 65536, 131072 - 2048)
     q = cases["decode_64k_b32_h64_q4"]
     assert (q.batch, q.max_entries, q.n_query) == (32, 32768, 4)
-    # every workload draws from its own seed
-    seeds = [cases[k].seed for k in cases]
+    # the NVFP4-query workload is the decode workload with the other attention: same inputs, same seed
+    v = cases["decode_64k_b32_h64_nvfp4q"]
+    assert v.nvfp4q and not d.nvfp4q
+    assert dataclasses.replace(v, name=d.name, nvfp4q=False) == d
+    # every other workload draws from its own seed
+    seeds = [cases[k].seed for k in cases if k != "decode_64k_b32_h64_nvfp4q"]
     assert len(set(seeds)) == len(seeds)
 
 

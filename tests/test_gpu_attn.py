@@ -357,3 +357,30 @@ def test_queries_beyond_fp16_range_and_window_overflow(csa):
     csa.sparse_attn_decode(q, cache, n_entries, idx, bad, max_entries=E, window=W, scale=SCALE, ws=ws, swa=swa,
                            swa_len=swa_len)
     assert csa.device_status(ws) == csa.ERR_DEVICE_CHECK
+
+
+def test_extreme_query_magnitudes(csa):
+    # heads around 1e30 and 1e-30 (any finite bf16 magnitude): the logits of the large heads reach ~1e31, so the
+    # softmax must subtract its maximum from the same rounded products it took the maximum of
+    g = torch.Generator(device=DEV).manual_seed(63)
+    B, T, H, K, W = 2, 1800, 64, 24, 128
+    E = T // 2
+    x = _latents(g, B, T)
+    mag = torch.tensor([1e30, 1e-30, 3e5, 1.0], device=DEV).repeat(16).view(1, 1, H, 1)
+    q = (torch.randn(B, 1, H, 512, generator=g, device=DEV) * mag).to(torch.bfloat16)
+    swa = torch.randn(B, W, 512, generator=g, device=DEV).to(torch.bfloat16)
+    swa_len = torch.tensor([W, 7], dtype=torch.int32, device=DEV)
+    ws0 = csa.workspace(256, DEV)
+    cache = gpu_pack_sequences(csa, x, [T] * B, E, 512, 2, csa.SCALE_AMAX, ws0)
+    rng = np.random.default_rng(63)
+    idx_np = np.stack([rng.choice(-(-E // 8), K, replace=False) for _ in range(B)]).astype(np.int32)[:, None, :]
+    out, lse = gpu_decode_attn(csa, q, cache, torch.full((B,), E, dtype=torch.int32, device=DEV),
+                               torch.from_numpy(idx_np).to(DEV), swa, swa_len, E, W)
+    out, lse = out.cpu().numpy(), lse.cpu().numpy()
+    xf, qf, sf = to_np(x), to_np(q), to_np(swa)
+    for b in range(B):
+        entries = o_fp4.dequantize(o_fp4.pack(xf[b], 2, "amax", n_blocks=-(-E // 8)), 512, E)
+        ref, ref_lse = o_attn.decode_attention(qf[b, 0].astype(np.float64), entries, E, idx_np[b, 0],
+                                               sf[b, :int(swa_len[b])], SCALE)
+        assert_attn_close(out[b, 0], ref, f"seq {b}")
+        np.testing.assert_allclose(lse[b, 0], ref_lse, rtol=1e-5, atol=2e-3)

@@ -123,7 +123,13 @@ def _decode_case(name, samples, layer_checks=None):
                     swa = o_attn.prefill_window(to_np(d["swa"][layer, b]), int(d["swa_first_pos"][b]), p, c.window)
                     rows = _oracle_rows(tok, ref[j], lambda e, p=p: e < E and 2 * e + 1 <= p)
                 q = to_np(d["q"][layer, b, j]).astype(np.float64)
-                want, _ = o_attn.attend(q, np.concatenate([rows, swa]), SCALE)
+                if c.nvfp4q:
+                    # the NVFP4-query attention: rounded query heads and window keys in the logits, exact values
+                    keys = np.concatenate([rows, o_fp4.round_trip(np.asarray(swa, np.float32), "amax")])
+                    want, _ = o_attn.attend_kv(o_attn.nvfp4_query(q.astype(np.float32)), keys,
+                                               np.concatenate([rows, swa]), SCALE)
+                else:
+                    want, _ = o_attn.attend(q, np.concatenate([rows, swa]), SCALE)
                 assert_attn_close(outs[layer][b, j, :c.heads].cpu().numpy(), want[:c.heads],
                                   f"{name} seq {b} layer {layer} ({w.modes[layer]})")
     return w
@@ -139,6 +145,10 @@ def test_decode_64k_batch32():
 
 def test_decode_64k_batch32_four_query_positions():
     _decode_case("decode_64k_b32_h64_q4", samples=[0, 31])
+
+
+def test_decode_64k_batch32_nvfp4q():
+    _decode_case("decode_64k_b32_h64_nvfp4q", samples=[0, 31])
 
 
 def test_decode_1m_hierarchical():
