@@ -176,6 +176,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
                   "r"(smem_addr(bar)) : "memory");
 }
 
+// Two E2M1 codes (lo in the low nibble): the nearest E2M1 value, ties to the even code, saturating at 6, the
+// sign kept (the hardware conversion with round-to-nearest-even and finite saturation).
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tmov.b32 %0, {t, t, t, t};\n\t}"
+      : "=r"(r) : "f"(lo), "f"(hi));
+  return r & 0xFFu;
+}
+
 // One 16-element group rounded with the AMAX rule of the cache format (the rule csa_pack_fp4 applies): the
 // E4M3 scale byte of fl32(amax / 6) is returned, the E2M1 codes of fl32(v / s) go to *lo (elements 0-7) and
 // *hi (8-15), low nibble first; a zero scale gives zero codes.
@@ -193,9 +202,9 @@ __device__ __forceinline__ uint32_t quant16_amax(const float* v, uint32_t* lo, u
   uint32_t c0 = 0u, c1 = 0u;
   if (s > 0.0f) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      c0 |= e2m1_code(__fdiv_rn(v[k], s)) << (4 * k);
-      c1 |= e2m1_code(__fdiv_rn(v[k + 8], s)) << (4 * k);
+    for (int k = 0; k < 4; ++k) {
+      c0 |= e2m1x2_rn(__fdiv_rn(v[2 * k], s), __fdiv_rn(v[2 * k + 1], s)) << (8 * k);
+      c1 |= e2m1x2_rn(__fdiv_rn(v[8 + 2 * k], s), __fdiv_rn(v[9 + 2 * k], s)) << (8 * k);
     }
   }
   *lo = c0;
@@ -323,6 +332,17 @@ __device__ __forceinline__ void load_scales(const uint8_t* seq, int id, bool ok,
   for (int c = 0; c < 4; ++c) sc[c] = hp ? w[2 * c + 1] : w[2 * c];
 }
 
+// NVFP4-query mode: the scale words of the four panels of parity hp of row `row` of window tile tw, from the
+// window rows the prepare kernel rounded; zeros for a row that is not attended.
+__device__ __forceinline__ void load_window_scales(const AttnParams& p, const UnitCtx& u, int tw, int row, int hp,
+                                                   uint32_t* sc) {
+  bool oob;
+  uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  if (window_row(p, u, tw, row, &oob)) ld_nc_v8(p.w4_sc + ((int64_t)u.b * p.swa_rows + window_row0(p, u, tw) + row) * 32, w);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) sc[c] = hp ? w[2 * c + 1] : w[2 * c];
+}
+
 // NVFP4-query mode: a converter writes the key scale factors of its row and its four panels (panels hp,
 // hp + 2, hp + 4, hp + 6 = block-scaled products of K = 64) of tile t into scale buffer t & 1 (row m's bytes
 // of product s at lane m, column kColSFA + 32 (t & 1) + 4 s + m / 32) and arrives on that buffer's barrier.
@@ -341,10 +361,69 @@ __device__ __forceinline__ uint32_t pick4(const uint32_t* v, int i) {
   return i == 0 ? v[0] : (i == 1 ? v[1] : (i == 2 ? v[2] : v[3]));
 }
 
+// NVFP4-query variant, first step: rounds every query head and every window row once per call. One warp per
+// 512-element row, lane = one 16-element group. A query head is scaled by 2^-e, e = floor(log2 max|q_h|) - 10
+// clamped to [-100, 100], which puts every block's amax / 6 below 342 (inside the E4M3 scale range); rows
+// beyond the call's heads are zero so that each unit has 64 rows. Window rows are rounded as they are.
+__global__ void __launch_bounds__(256) attn_prep_kernel(const AttnParams p) {
+  griddep_launch();                                // the attention kernel may start its setup
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t qrows = p.units * 64;
+  const int64_t wrows = p.window > 0 ? (p.units / p.n_query) * p.swa_rows : 0;
+  float x[16];
+  uint32_t w8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  if (r < qrows) {
+    const int64_t unit = r >> 6;
+    const int h = (int)(r & 63);
+    if (h < p.heads) {
+      const __nv_bfloat16* src = p.q + (unit * p.heads + h) * kLatent + lane * 16;
+      const uint4 a = ld_nc_v4(src), b = ld_nc_v4(src + 8);
+      w8[0] = a.x; w8[1] = a.y; w8[2] = a.z; w8[3] = a.w; w8[4] = b.x; w8[5] = b.y; w8[6] = b.z; w8[7] = b.w;
+    }
+    uint32_t m = 0u;                               // |x| bits: magnitudes compare as integers
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, max(w8[j] & 0x7FFFu, (w8[j] >> 16) & 0x7FFFu));
+    m = __reduce_max_sync(0xffffffffu, m);
+    int sh = m == 0u ? 0 : (int)((m >> 7) & 0xFFu) - 127 - 10;
+    sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+    const float f = __int_as_float((127 - sh) << 23);               // 2^-sh, exact
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      x[2 * j] = __fmul_rn(__uint_as_float(w8[j] << 16), f);
+      x[2 * j + 1] = __fmul_rn(__uint_as_float(w8[j] & 0xFFFF0000u), f);
+    }
+    uint32_t lo, hi;
+    const uint32_t sb = quant16_amax(x, &lo, &hi);
+    *reinterpret_cast<uint2*>(p.q4_codes + r * 256 + lane * 8) = make_uint2(lo, hi);
+    p.q4_sc[r * 32 + lane] = (uint8_t)sb;
+    if (lane == 0) p.q4_mult[r] = __int_as_float((127 + sh) << 23);  // 2^sh
+  } else if (r < qrows + wrows) {
+    const int64_t wr = r - qrows;
+    const int64_t b = wr / p.swa_rows, row = wr % p.swa_rows;
+    const __nv_bfloat16* src = p.swa + b * p.swa_stride_b + row * kLatent + lane * 16;
+    const uint4 a = ld_nc_v4(src), c = ld_nc_v4(src + 8);
+    w8[0] = a.x; w8[1] = a.y; w8[2] = a.z; w8[3] = a.w; w8[4] = c.x; w8[5] = c.y; w8[6] = c.z; w8[7] = c.w;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      x[2 * j] = __uint_as_float(w8[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w8[j] & 0xFFFF0000u);
+    }
+    uint32_t lo, hi;
+    const uint32_t sb = quant16_amax(x, &lo, &hi);
+    *reinterpret_cast<uint2*>(p.w4 + wr * 256 + lane * 8) = make_uint2(lo, hi);
+    p.w4_sc[wr * 32 + lane] = (uint8_t)sb;
+  }
+  // completes only after the kernel before it, so that its dependent, which waits for this kernel alone,
+  // also sees everything before (the index list)
+  griddep_wait();
+}
+
 template <bool kQ4>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap swa_map,
-                                                               const __grid_constant__ CUtensorMap cache_map) {
+                                                               const __grid_constant__ CUtensorMap cache_map,
+                                                               const __grid_constant__ CUtensorMap win4_map) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + kTmemPtrOff);
@@ -502,82 +581,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);      // scale_log2 * 2^sh
       }
     } else {
-      // NVFP4 query: head h is scaled by 2^-k_h, k_h = floor(log2 max|q_h|) - 10 (clamped to [-100, 100]),
-      // which puts every 16-element block's amax / 6 below 342, inside the E4M3 scale range, and each block
-      // is rounded with the cache format's AMAX rule. The codes form the B operand of the block-scaled
-      // logits (two K-halves of [64 heads x 128 bytes], 128-byte swizzle), the scale bytes go to tensor
-      // memory below, and 2^k_h goes into the head's softmax scale. An item is one block of 16 elements.
-      constexpr int kQ4Items = kHeadsPad * 32;
-      constexpr int kQ4Per = (kQ4Items + kQThreads - 1) / kQThreads;
-      static_assert(kQThreads % 32 == 0, "the 32 blocks of a head lie in one warp's items");
-      uint4 v[2 * kQ4Per];
-#pragma unroll
-      for (int k = 0; k < kQ4Per; ++k) {
-        const int i = qt + k * kQThreads;
-        const int h = i >> 5, g = i & 31;
-        v[2 * k] = make_uint4(0, 0, 0, 0);
-        v[2 * k + 1] = make_uint4(0, 0, 0, 0);
-        if (i < kQ4Items && h < H) {
-          v[2 * k] = ld_nc_v4(qg + (int64_t)h * kLatent + g * 16);
-          v[2 * k + 1] = ld_nc_v4(qg + (int64_t)h * kLatent + g * 16 + 8);
-        }
+      // NVFP4 query, rounded by the prepare kernel (this kernel's predecessor): the codes form the B operand of
+      // the block-scaled logits (two K-halves of [64 heads x 128 bytes], 128-byte swizzle), the scale bytes go
+      // to tensor memory, and the head's power of two goes into its softmax scale
+      griddep_wait();
+      const uint8_t* qsrc = p.q4_codes + u.unit * 64 * 256;
+      for (int i = qt; i < 64 * 16; i += kQThreads) {
+        const int n = i >> 4, j = i & 15, cc = j & 7;
+        *reinterpret_cast<uint4*>(smem + kQ4Off + (j >> 3) * (kHeadsPad * 128) + n * 128 + ((cc ^ (n & 7)) << 4)) =
+            ld_nc_v4(qsrc + i * 16);
       }
-#pragma unroll
-      for (int k = 0; k < kQ4Per; ++k) {
-        const int i = qt + k * kQThreads;
-        if (i < kQ4Items) {
-          uint32_t m = 0u;
-          const uint32_t w8[8] = {v[2 * k].x, v[2 * k].y, v[2 * k].z, v[2 * k].w,
-                                  v[2 * k + 1].x, v[2 * k + 1].y, v[2 * k + 1].z, v[2 * k + 1].w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) m = max(m, max(w8[j] & 0x7FFFu, (w8[j] >> 16) & 0x7FFFu));
-          m = __reduce_max_sync(0xffffffffu, m);
-          if (lane == 0) atomicMax(qmax + (i >> 5), m);
-        }
-      }
-      asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
-#pragma unroll
-      for (int k = 0; k < kQ4Per; ++k) {
-        const int i = qt + k * kQThreads;
-        if (i < kQ4Items) {
-          const int h = i >> 5, g = i & 31;
-          const uint32_t mb = qmax[h];
-          int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 10;
-          sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-          const float f = __int_as_float((127 - sh) << 23);                // 2^-sh, exact
-          const uint32_t w8[8] = {v[2 * k].x, v[2 * k].y, v[2 * k].z, v[2 * k].w,
-                                  v[2 * k + 1].x, v[2 * k + 1].y, v[2 * k + 1].z, v[2 * k + 1].w};
-          float x[16];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            x[2 * j] = __fmul_rn(__uint_as_float(w8[j] << 16), f);
-            x[2 * j + 1] = __fmul_rn(__uint_as_float(w8[j] & 0xFFFF0000u), f);
-          }
-          uint32_t lo, hi;
-          const uint32_t sbyte = quant16_amax(x, &lo, &hi);
-          const int cc = (g & 15) >> 1;                                    // 16-byte chunk within the 128-byte row
-          *reinterpret_cast<uint2*>(smem + kQ4Off + (g >> 4) * (kHeadsPad * 128) + h * 128 + ((cc ^ (h & 7)) << 4) +
-                                    (g & 1) * 8) = make_uint2(lo, hi);
-          smem[kQ4ScOff + h * 32 + g] = (uint8_t)sbyte;
-        }
-      }
-      if (qt < 64) {
-        const uint32_t mb = qmax[qt];
-        int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 10;
-        sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-        qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);    // scale_log2 * 2^sh
-      }
-      asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+      if (qt < 64) qscale[qt] = p.scale_log2 * __ldg(p.q4_mult + u.unit * 64 + qt);
       if (warp < 4) {
         // query scale factors: head n's four bytes of product s at lane 32 j + n % 32 (every subpartition j
         // holds a copy; warp w writes subpartition w), column kColSFB + 4 s + n / 32
         const uint32_t lb = (uint32_t)(warp * 32) << 16;
 #pragma unroll
-        for (int s8 = 0; s8 < 8; ++s8) {
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sc[8];
+          ld_nc_v8(p.q4_sc + (u.unit * 64 + lane + 32 * c) * 32, sc);
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tc::st_32x1(tbase + lb + kColSFB + 4 * s8 + c,
-                        *reinterpret_cast<const uint32_t*>(smem + kQ4ScOff + (lane + 32 * c) * 32 + 4 * s8));
+          for (int s8 = 0; s8 < 8; ++s8) tc::st_32x1(tbase + lb + kColSFB + 4 * s8 + c, sc[s8]);
         }
         tc::wait_st();
       }
@@ -602,9 +626,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       load_scales(seq, id_n, n_cache > 1 && cache_ok(u, id_n, row), row, hp, sc_n);
       qs0 = sc_c[0];
       qs1 = sc_c[1];
-      // NVFP4-query mode: the key scale factors of the first tile when it is a cache tile (a later cache
-      // tile's are written while the tile before it is converted)
-      if (kQ4 && nw == 0 && n_cache > 0) put_key_scales(tbase, sp, hp, lane, 0, sc_c, bars);
+      // NVFP4-query mode: the key scale factors of the first tile (a later tile's are written while the tile
+      // before it is converted)
+      if (kQ4 && n_tiles > 0) {
+        uint32_t sw[4] = {sc_c[0], sc_c[1], sc_c[2], sc_c[3]};
+        if (nw > 0) load_window_scales(p, u, 0, row, hp, sw);
+        put_key_scales(tbase, sp, hp, lane, 0, sw, bars);
+      }
     }
   } else {
     // the gather warp starts its L2 prefetches once the queries have arrived, so that the queries and the
@@ -661,8 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         vr = window_row(p, u, it, row, &oob);
         if (oob && hp == 0) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
         if (!__all_sync(0xffffffffu, wait_bar(&bars[WIN_FULL], it & 1, abort_flag, p.hdr, 10, p.spin_limit))) break;
-        // NVFP4-query mode: the first cache tile's key scale factors, one tile ahead
-        if (kQ4 && it + 1 == nw && n_cache > 0) put_key_scales(tbase, sp, hp, lane, it + 1, sc_c, bars);
+        // NVFP4-query mode: the next tile's key scale factors, one tile ahead
+        if (kQ4 && it + 1 < n_tiles) {
+          uint32_t sw[4] = {sc_c[0], sc_c[1], sc_c[2], sc_c[3]};
+          if (it + 1 < nw) load_window_scales(p, u, it + 1, row, hp, sw);
+          put_key_scales(tbase, sp, hp, lane, it + 1, sw, bars);
+        }
       }
 #pragma unroll 1
       for (int c = 0; c < kChunks; ++c) {
@@ -673,11 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
           // bf16 -> fp16 of this row's 64 columns, in place; rows that are not attended become zero. A value
           // beyond the fp16 range (|x| > 65504, outside the call's contract) becomes infinite: reported.
           uint32_t inf = 0u;
-          uint4 xw[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint4 x = *reinterpret_cast<const uint4*>(vrow + ((j ^ (row & 7)) << 4));
-            xw[j] = vr ? x : make_uint4(0u, 0u, 0u, 0u);
             h[4 * j] = vr ? bf2_to_h2(x.x) : 0u; h[4 * j + 1] = vr ? bf2_to_h2(x.y) : 0u;
             h[4 * j + 2] = vr ? bf2_to_h2(x.z) : 0u; h[4 * j + 3] = vr ? bf2_to_h2(x.w) : 0u;
 #pragma unroll
@@ -685,29 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
               inf |= ((h[4 * j + e] & 0x7C00u) == 0x7C00u) | ((h[4 * j + e] & 0x7C000000u) == 0x7C000000u);
           }
           if (inf) report(p.hdr, CSA_ERR_DEVICE_CHECK, KID_ATTN, (uint32_t)u.unit);
-          if constexpr (kQ4) {
-            // NVFP4-query mode: the window row's keys for the logits, rounded from the exact bf16 values
-            // with the cache format's AMAX rule: four groups of 16 -> 32 code bytes into the raw stage (the
-            // layout of a copied cache tile) and four scale bytes into this tile's scale buffer
-            uint32_t cw[8], sw = 0u;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const uint32_t w8[8] = {xw[2 * g].x, xw[2 * g].y, xw[2 * g].z, xw[2 * g].w,
-                                      xw[2 * g + 1].x, xw[2 * g + 1].y, xw[2 * g + 1].z, xw[2 * g + 1].w};
-              float v[16];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                v[2 * e] = __uint_as_float(w8[e] << 16);
-                v[2 * e + 1] = __uint_as_float(w8[e] & 0xFFFF0000u);
-              }
-              sw |= quant16_amax(v, &cw[2 * g], &cw[2 * g + 1]) << (8 * g);
-            }
-            tc::st_32x1(tbase + ((uint32_t)(sp * 32) << 16) + kColSFA + 32 * (it & 1) + 4 * pnl + sp, sw);
-            uint8_t* rrow = smem + kRawOff + (row >> 3) * 2048 + (pnl >> 2) * 1024 + (row & 7) * 128;
-            const int j0 = (pnl & 3) * 2;
-            *reinterpret_cast<uint4*>(rrow + ((j0 ^ (row & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-            *reinterpret_cast<uint4*>(rrow + (((j0 + 1) ^ (row & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-          }
         } else {
           dequant_panel(q0, qs0, h);
 #pragma unroll
@@ -739,13 +746,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[V_FULL + c]);
       }
-      if (kQ4 && win && !stop) {
-        // the window tile's FP4 keys and scale factors are written
-        tc::wait_st();
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[SFX_FULL + (it & 1)]);
-      }
       if (!win) {
         // the scales of tile k + 2 are loaded a tile before the queue reaches it, its id one more tile earlier
 #pragma unroll
@@ -758,37 +758,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     }
   } else if (kQ4 && warp == kLogitsWarp) {
     // ---------------- NVFP4-query logits: S^T(t) = C . Q4^T by block-scaled FP4 products ----------------
-    // A cache tile's codes are copied by tensor map into the raw stage (16 blocks, two boxes each) once the
-    // previous tile's logits are complete; a window tile's FP4 keys are written there by the converters.
+    // Each tile's FP4 keys are copied by tensor map into the raw stage once the previous tile's logits are
+    // complete: a cache tile as 16 blocks (two [8 x 128-byte] boxes each, 8-row groups 2,048 bytes apart), a
+    // window tile from the rounded window rows (two [128 x 128-byte] boxes, 8-row groups 1,024 bytes apart).
     // The key scale factors come from the converters, one tile ahead, so the logits never wait for the
     // values buffer.
-    griddep_wait();                                  // the index list comes from the kernel before
+    griddep_wait();                                  // the index list and the rounded window rows
     bool ok = true;
     int raw_issued = 0;
     int nid = (n_cache > 0 && lane < kTileBlocks) ? cache_id(p, u, c0, lane << 3) : -1;
     for (int it = 0; it < n_tiles && ok; ++it) {
       const int sb = it & 1;
-      if (it >= nw) {
+      const bool win = it < nw;
+      if (it > 0 && !wait_bar_warp(&bars[RAW_DONE], (it - 1) & 1, abort_flag, p.hdr, 14, p.spin_limit)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[RAW_FULL], kRawBytes);
+      __syncwarp();
+      if (win) {
+        if (lane == 0) {
+          const int64_t y0 = window_row0(p, u, it);
+          const int y = (int)(y0 < -(int64_t)kRows ? -kRows : (y0 > p.swa_rows ? p.swa_rows : y0));
+          tma_load_3d(smem + kRawOff, &win4_map, 0, y, (int)u.b, &bars[RAW_FULL]);
+          tma_load_3d(smem + kRawOff + kRawBytes / 2, &win4_map, 128, y, (int)u.b, &bars[RAW_FULL]);
+        }
+      } else {
         const int k = it - nw;
-        if (it > 0 && !wait_bar_warp(&bars[RAW_DONE], (it - 1) & 1, abort_flag, p.hdr, 14, p.spin_limit)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars[RAW_FULL], kRawBytes);
-        __syncwarp();
         if (lane < kTileBlocks) {
           uint8_t* dst = smem + kRawOff + lane * 2048;
           tma_load_4d(dst, &cache_map, 0, 0, nid, (int)u.b, &bars[RAW_FULL]);
           tma_load_4d(dst + 1024, &cache_map, 128, 0, nid, (int)u.b, &bars[RAW_FULL]);
         }
-        ++raw_issued;
         nid = (k + 1 < n_cache && lane < kTileBlocks) ? cache_id(p, u, c0 + k + 1, lane << 3) : -1;
-        if (!wait_bar_warp(&bars[RAW_FULL], k & 1, abort_flag, p.hdr, 15, p.spin_limit)) break;
       }
+      ++raw_issued;
+      if (!wait_bar_warp(&bars[RAW_FULL], it & 1, abort_flag, p.hdr, 15, p.spin_limit)) break;
       if (!wait_bar_warp(&bars[SFX_FULL + sb], (it >> 1) & 1, abort_flag, p.hdr, 16, p.spin_limit)) break;
       if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4, p.spin_limit)) break;
       tc::fence_after();
       const uint32_t d = tbase + kColS + 64 * sb;
+      const uint32_t half_off = win ? kRawBytes / 2 : 1024, sbo = win ? 1024 : 2048;
 #pragma unroll
       for (int s8 = 0; s8 < 8; ++s8) {
-        const uint64_t a = tc::smem_desc(s_base + kRawOff + (s8 >> 2) * 1024 + (s8 & 3) * 32, 16, 2048, tc::kSwizzle128B);
+        const uint64_t a = tc::smem_desc(s_base + kRawOff + (s8 >> 2) * half_off + (s8 & 3) * 32, 16, sbo,
+                                         tc::kSwizzle128B);
         const uint64_t b = tc::smem_desc(s_base + kQ4Off + (s8 >> 2) * (kHeadsPad * 128) + (s8 & 3) * 32, 16, 1024,
                                          tc::kSwizzle128B);
         tc::mma_mxf4_warp(d, a, b, kIdescS4, tbase + kColSFA + 32 * sb + 4 * s8, tbase + kColSFB + 4 * s8, s8 > 0 ? 1u : 0u);
@@ -1194,18 +1205,43 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  // NVFP4-query mode: the window rows rounded by the prepare kernel as a [batch][swa_rows][256] byte tensor,
+  // copied in [128 x 128] boxes (one half of each of a window tile's rows) with the 128-byte swizzle; rows
+  // outside the tensor read as zero
+  CUtensorMap wmap;
+  std::memset(&wmap, 0, sizeof(wmap));
+  if (p.q4 && p.n_wt > 0) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {256, (cuuint64_t)p.swa_rows, (cuuint64_t)(p.units / p.n_query)};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)p.swa_rows * 256};
+    const cuuint32_t box[3] = {128, (cuuint32_t)kRows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p.w4, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   ProfScope prof("sparse_attn", s);
   clear_stale_error();
   if (p.q4) {
     cudaError_t e = ensure_smem_limit(attn_tc_kernel<true>, kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_ex(attn_tc_kernel<true>, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads),
-                     (size_t)kSmemBytes, s, pdl, p, map, cmap);
+                     (size_t)kSmemBytes, s, pdl, p, map, cmap, wmap);
   }
   cudaError_t e = ensure_smem_limit(attn_tc_kernel<false>, kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_ex(attn_tc_kernel<false>, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads),
-                   (size_t)kSmemBytes, s, pdl, p, map, cmap);
+                   (size_t)kSmemBytes, s, pdl, p, map, cmap, wmap);
+}
+
+cudaError_t launch_attn_prep(const AttnParams& p, cudaStream_t s, bool pdl) {
+  if (p.units == 0) return cudaSuccess;
+  const int64_t rows = p.units * 64 + (p.window > 0 ? (p.units / p.n_query) * p.swa_rows : 0);
+  ProfScope prof("attn_prep", s);
+  clear_stale_error();
+  return launch_ex(attn_prep_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, pdl, p);
 }
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s, bool pdl) {

@@ -74,7 +74,7 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 struct AttnLayout {
   int64_t units;
   int n_ct, n_wt, splits, cache_splits, win_split, last_ct;
-  size_t o_off, ml_off, total;
+  size_t o_off, ml_off, q4_off, q4sc_off, q4m_off, w4_off, w4sc_off, total;
 };
 
 // One CTA per SM: the selected blocks of a query are cut into 128-row tiles (16 blocks) shared by the
@@ -103,7 +103,15 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   L.o_off = CSA_WS_HEADER_BYTES;
   const size_t parts = L.splits > 1 ? (size_t)L.units * L.splits * a->heads : 0;
   L.ml_off = round_up(L.o_off + parts * kLatent * 4, 256);
-  L.total = round_up(L.ml_off + parts * 2 * 4, 256);
+  // the NVFP4-query variant's rounded queries (64 head rows per unit) and window rows
+  const size_t qrows = (size_t)L.units * 64;
+  const size_t wrows = a->window > 0 && a->swa_rows > 0 ? (size_t)batch * a->swa_rows : 0;
+  L.q4_off = round_up(L.ml_off + parts * 2 * 4, 256);
+  L.q4sc_off = round_up(L.q4_off + qrows * 256, 256);
+  L.q4m_off = round_up(L.q4sc_off + qrows * 32, 256);
+  L.w4_off = round_up(L.q4m_off + qrows * 4, 256);
+  L.w4sc_off = round_up(L.w4_off + wrows * 256, 256);
+  L.total = round_up(L.w4sc_off + wrows * 32, 256);
   return L;
 }
 
@@ -538,7 +546,17 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.hdr = reinterpret_cast<uint32_t*>(w);
   p.q4 = q4 ? 1 : 0;
   debug_fault(&p.fault, &p.spin_limit);
-  if (cudaError_t e = launch_attn(p, stream, early)) return cuda_fail(e, "attn");
+  if (q4) {
+    // the NVFP4-query variant rounds the queries and the window rows once, in a kernel of its own; the
+    // attention kernel, its programmatic dependent, copies the rounded operands in
+    p.q4_codes = w + L.q4_off;
+    p.q4_sc = w + L.q4sc_off;
+    p.q4_mult = reinterpret_cast<float*>(w + L.q4m_off);
+    p.w4 = w + L.w4_off;
+    p.w4_sc = w + L.w4sc_off;
+    if (cudaError_t e = launch_attn_prep(p, stream, early)) return cuda_fail(e, "attn_prep");
+  }
+  if (cudaError_t e = launch_attn(p, stream, early || q4)) return cuda_fail(e, "attn");
   if (cudaError_t e = launch_combine(p, stream, true)) return cuda_fail(e, "combine");
   return CSA_OK;
 }

@@ -262,6 +262,14 @@ struct AttnParams {
   float* out_lse;
   uint32_t* hdr;
   int q4;                      // host side: the NVFP4-query variant (block-scaled FP4 logits)
+  // NVFP4-query variant: operands rounded by the prepare kernel (workspace). Per unit, 64 head rows (zero
+  // beyond heads) of 256 code bytes, 32 scale bytes and the head's power of two 2^e; per sequence, swa_rows
+  // window rows of 256 code bytes and 32 scale bytes.
+  uint8_t* q4_codes;           // [units][64][256]
+  uint8_t* q4_sc;              // [units][64][32]
+  float* q4_mult;              // [units][64]
+  uint8_t* w4;                 // [batch][swa_rows][256]
+  uint8_t* w4_sc;              // [batch][swa_rows][32]
   // Bounded waits give up after this many polls (kSpinLimit unless a test lowered it), and a nonzero
   // fault makes the kernel withhold one arrival (csa_debug_set_fault).
   uint32_t spin_limit;
@@ -324,6 +332,7 @@ cudaError_t launch_index_score(const ScoreParams& p, int num_sms, cudaStream_t s
 cudaError_t launch_coarse_score(const CoarseScoreParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_topk(const TopkParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_attn_prep(const AttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s, bool pdl);
 
 // Clears an error that an earlier runtime call of another component left in this thread's last-error

@@ -386,11 +386,12 @@ typedef struct csa_attn_args {
   float* out_lse;
 } csa_attn_args;
 
-/* Workspace bytes for one call with these arguments on the current device. A query's rows are cut into
- * 128-row tiles shared by several CTAs (splits), as many as fill the device's SMs. With more than one split
- * the workspace holds every split's partial (o, m, l), which a second kernel merges; with one split it is only
- * the status header. The answer depends on the device's SM count, so query it with the device current that
- * will run the call. */
+/* Workspace bytes for one call with these arguments on the current device (the same for the NVFP4-query
+ * calls below). A query's rows are cut into 128-row tiles shared by several CTAs (splits), as many as fill the
+ * device's SMs. With more than one split the workspace holds every split's partial (o, m, l), which a second
+ * kernel merges. It also holds the NVFP4-query variant's rounded operands: 64 head rows per query of 288 bytes
+ * plus a 4-byte power of two, and 288 bytes per window row. The answer depends on the device's SM count, so
+ * query it with the device current that will run the call. */
 size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* args);
 csa_status csa_sparse_attn_decode(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,
                                   cudaStream_t stream);
@@ -412,8 +413,9 @@ csa_status csa_sparse_attn_prefill(int64_t batch, const csa_attn_args* args, voi
  *   k_c   a cache row as stored; a window row rounded like csa_pack_fp4 with CSA_SCALE_AMAX (no merge, no
  *         pre-scale; magnitudes above 2688 saturate).
  * Values are exact: out[u][h] = sum_c softmax(z)_c * c uses the dequantized cache rows and the bf16 window
- * rows, as in the exact calls. Logits are accumulated in fp32. The cache's code bytes are read by
- * tensor-map copies (the cache's 32-byte alignment and stride rule apply, as above); all other argument
+ * rows, as in the exact calls. Logits are accumulated in fp32. A first kernel rounds every query head and
+ * every window row once per call into the workspace; the attention kernel copies those and the cache's code
+ * bytes in by tensor map (the cache's 32-byte alignment and stride rule apply, as above). All other argument
  * rules and error behaviour are those of the exact calls.
  * ------------------------------------------------------------------------------------------------ */
 csa_status csa_sparse_attn_decode_nvfp4q(int64_t batch, const csa_attn_args* args, void* ws, size_t ws_bytes,

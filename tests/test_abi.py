@@ -175,8 +175,10 @@ def test_attention_workspace_size_is_host_only(lib):
     # one cache tile and one window tile: two splits, so partials; no window: one split, no partials
     aa.top_k = 16
     assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) >= 256 + 2 * 64 * (512 * 4 + 2 * 4)
+    # no window: one split, no partials; the header and the NVFP4-query variant's rounded query (64 head rows
+    # of 256 code bytes, 32 scale bytes and a 4-byte power of two)
     aa.swa_rows, aa.window = 0, 0
-    assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) == 256
+    assert lib.csa_sparse_attn_workspace_size(1, ctypes.byref(aa)) == 256 + 64 * 256 + 64 * 32 + 256
 
 
 def test_static_index_validates_before_sizing(lib):
