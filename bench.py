@@ -709,7 +709,7 @@ def e2e_pipelined(w, host_in, args, world, device, comp):
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernels, from one ncu
 # capture of the same workload with one cache replica (still larger than L2):
-#   python bench.py --steps 2 --warmup 3 --no-cpu-baseline --min-seconds 0 --replicas 1
+#   python bench.py [--workload <name>] --steps 2 --warmup 3 --no-cpu-baseline --min-seconds 0 --replicas 1
 # under ncu -k regex:<kernel> -s 2 -c 1. An entry is removed when its kernel changes; the roofline then
 # reports traffic as null.
 TRAFFIC = {
@@ -717,6 +717,7 @@ TRAFFIC = {
     #   --replicas 1 (ncu reports these in GB / MB with six digits)
     ("project_pack_128k_h4096", "project_pack"): 1_102_514_000 + 19_863_808,
     ("decode_64k_b32_h64", "sparse_attn"): 25_297_408 + 0,
+    ("decode_64k_b32_h64_nvfp4q", "sparse_attn"): 24_989_952 + 256,
     ("decode_64k_b32_h64", "index_score"): 75_610_368 + 1_088_256,
 }
 
