@@ -934,9 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       if (tid == 0) flag[sb] = 0;
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
-        bool over = false;
+        // on the CTA's first tile every reference maximum is still -inf, so a first pass could only report an
+        // overflow: it goes straight to the maxima (a tile without attended rows then leaves them at -inf and
+        // the second pass writes zeros, as the first would have)
+        const bool first = it == 0 && pass == 0;
+        bool over = first;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < 2 && !first; ++half) {
           uint32_t sr[32];
           tc::ld_32x32(s_col + 32 * half, sr);
           tc::wait_ld();
