@@ -98,6 +98,7 @@ enum Bar {
                                         // (and a window tile's FP4 codes in the raw stage); one per parity
   RAW_FULL = SFX_FULL + 2,              // NVFP4-query mode: a cache tile's codes have landed in the raw stage
   RAW_DONE,                             // NVFP4-query mode: the logits of the tile in the raw stage are complete
+  Q_FULL,                               // prepared fp16 queries have landed (exact attention with several splits)
   FIN_L, FIN_V, NUM_BARS
 };
 
@@ -370,10 +371,36 @@ __global__ void __launch_bounds__(256) attn_prep_kernel(const AttnParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int64_t qrows = p.units * 64;
-  const int64_t wrows = p.window > 0 ? (p.units / p.n_query) * p.swa_rows : 0;
+  const int64_t wrows = p.q4 && p.window > 0 ? (p.units / p.n_query) * p.swa_rows : 0;
   float x[16];
   uint32_t w8[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-  if (r < qrows) {
+  if (r < qrows && !p.q4) {
+    // exact attention: the head scaled by 2^-e, e = floor(log2 max|q_h|) - 14, which puts its largest magnitude
+    // in [2^14, 2^15), and rounded to fp16 (exact for every finite bf16 value), as the attention kernel does
+    // when it converts its own queries
+    const int64_t unit = r >> 6;
+    const int h = (int)(r & 63);
+    if (h < p.heads) {
+      const __nv_bfloat16* src = p.q + (unit * p.heads + h) * kLatent + lane * 16;
+      const uint4 a = ld_nc_v4(src), b = ld_nc_v4(src + 8);
+      w8[0] = a.x; w8[1] = a.y; w8[2] = a.z; w8[3] = a.w; w8[4] = b.x; w8[5] = b.y; w8[6] = b.z; w8[7] = b.w;
+    }
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, max(w8[j] & 0x7FFFu, (w8[j] >> 16) & 0x7FFFu));
+    m = __reduce_max_sync(0xffffffffu, m);
+    int sh = m == 0u ? 0 : (int)((m >> 7) & 0xFFu) - 127 - 14;
+    sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+    const float f = __int_as_float((127 - sh) << 23);
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      o[j] = f2_to_h2(__uint_as_float(w8[j] << 16) * f, __uint_as_float(w8[j] & 0xFFFF0000u) * f);
+    uint4* dst = reinterpret_cast<uint4*>(p.qh + r * kLatent + lane * 16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if (lane == 0) p.q4_mult[r] = __int_as_float((127 + sh) << 23);
+  } else if (r < qrows) {
     const int64_t unit = r >> 6;
     const int h = (int)(r & 63);
     if (h < p.heads) {
@@ -423,7 +450,8 @@ template <bool kQ4>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p,
                                                                const __grid_constant__ CUtensorMap swa_map,
                                                                const __grid_constant__ CUtensorMap cache_map,
-                                                               const __grid_constant__ CUtensorMap win4_map) {
+                                                               const __grid_constant__ CUtensorMap win4_map,
+                                                               const __grid_constant__ CUtensorMap qh_map) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(smem + kTmemPtrOff);
@@ -489,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     mbar_init(&bars[SFX_FULL + 1], kConvWarps);
     mbar_init(&bars[RAW_FULL], 1);
     mbar_init(&bars[RAW_DONE], 1);
+    mbar_init(&bars[Q_FULL], 1);
     mbar_init(&bars[FIN_L], 1);
     mbar_init(&bars[FIN_V], 1);
     fence_mbar_init();
@@ -532,53 +561,66 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     uint32_t* qmax = reinterpret_cast<uint32_t*>(smem + kQMaxOff);
     float* qscale = reinterpret_cast<float*>(smem + kQScaleOff);
     if constexpr (!kQ4) {
-      uint4 v[kQPer];
-#pragma unroll
-      for (int k = 0; k < kQPer; ++k) {
-        const int i = qt + k * kQThreads;
-        const int h = i >> 6, ch = i & 63;
-        v[k] = make_uint4(0, 0, 0, 0);
-        if (i < kQItems && h < H) v[k] = ld_nc_v4(qg + (int64_t)h * kLatent + ch * 8);
-      }
-#pragma unroll
-      for (int k = 0; k < kQPer; ++k) {
-        const int i = qt + k * kQThreads;
-        if (i < kQItems) {
-          // magnitudes compare as integers: the bits of |x| with the sign cleared
-          // (the 32 lanes of a warp hold 32 consecutive items starting at a multiple of 32, so all lie in one
-          // head's 64 and the warp reduces them before one atomic; the branch is uniform per warp, since
-          // kQItems and kQThreads are multiples of 32)
-          uint32_t m = 0u;
-          const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
-          m = __reduce_max_sync(0xffffffffu, m);
-          if (lane == 0) atomicMax(qmax + (i >> 6), m);
+      if (p.qh != nullptr) {
+        // the queries were converted by the prepare kernel (this kernel's predecessor): eight tensor-map boxes
+        // of [64 heads x 64 latent] land as the eight 128-byte-swizzled panels
+        griddep_wait();
+        if (warp == kLogitsWarp && lane == 0) {
+          mbar_arrive_expect_tx(&bars[Q_FULL], kPanels * kQPanel);
+#pragma unroll 1
+          for (int pp = 0; pp < kPanels; ++pp)
+            tma_load_3d(smem + kQOff + pp * kQPanel, &qh_map, 64 * pp, 0, (int)u.unit, &bars[Q_FULL]);
         }
-      }
-      asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+        if (qt < 64) qscale[qt] = p.scale_log2 * __ldg(p.q4_mult + u.unit * 64 + qt);
+      } else {
+        uint4 v[kQPer];
 #pragma unroll
-      for (int k = 0; k < kQPer; ++k) {
-        const int i = qt + k * kQThreads;
-        if (i < kQItems) {
-          const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
-          const uint32_t mb = qmax[h];
-          int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;    // exponent of the largest |q|, - 14
+        for (int k = 0; k < kQPer; ++k) {
+          const int i = qt + k * kQThreads;
+          const int h = i >> 6, ch = i & 63;
+          v[k] = make_uint4(0, 0, 0, 0);
+          if (i < kQItems && h < H) v[k] = ld_nc_v4(qg + (int64_t)h * kLatent + ch * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+          const int i = qt + k * kQThreads;
+          if (i < kQItems) {
+            // magnitudes compare as integers: the bits of |x| with the sign cleared
+            // (the 32 lanes of a warp hold 32 consecutive items starting at a multiple of 32, so all lie in one
+            // head's 64 and the warp reduces them before one atomic; the branch is uniform per warp, since
+            // kQItems and kQThreads are multiples of 32)
+            uint32_t m = 0u;
+            const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m = max(m, max(w4[j] & 0x7FFFu, (w4[j] >> 16) & 0x7FFFu));
+            m = __reduce_max_sync(0xffffffffu, m);
+            if (lane == 0) atomicMax(qmax + (i >> 6), m);
+          }
+        }
+        asm volatile("bar.sync 3, %0;" :: "n"(kQThreads) : "memory");
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+          const int i = qt + k * kQThreads;
+          if (i < kQItems) {
+            const int h = i >> 6, ch = i & 63, pp = ch >> 3, c = ch & 7;
+            const uint32_t mb = qmax[h];
+            int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;    // exponent of the largest |q|, - 14
+            sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
+            const float f = __int_as_float((127 - sh) << 23);                  // 2^-sh, exact
+            const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              o[j] = f2_to_h2(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+            *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        if (qt < 64) {
+          const uint32_t mb = qmax[qt];
+          int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;
           sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-          const float f = __int_as_float((127 - sh) << 23);                  // 2^-sh, exact
-          const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-          uint32_t o[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            o[j] = f2_to_h2(__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f);
-          *reinterpret_cast<uint4*>(smem + kQOff + pp * kQPanel + h * 128 + ((c ^ (h & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);      // scale_log2 * 2^sh
         }
-      }
-      if (qt < 64) {
-        const uint32_t mb = qmax[qt];
-        int sh = mb == 0u ? 0 : (int)((mb >> 7) & 0xFFu) - 127 - 14;
-        sh = sh < -100 ? -100 : (sh > 100 ? 100 : sh);
-        qscale[qt] = p.scale_log2 * __int_as_float((127 + sh) << 23);      // scale_log2 * 2^sh
       }
     } else {
       // NVFP4 query, rounded by the prepare kernel (this kernel's predecessor): the codes form the B operand of
@@ -816,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
   } else if (warp == kLogitsWarp) {
     // ---------------- logits MMA issue: S^T(t) = C . Q^T into S buffer t & 1 ----------------
     const uint32_t q_addr = s_base + kQOff;
-    bool ok = true;
+    bool ok = p.qh == nullptr || wait_bar_warp(&bars[Q_FULL], 0, abort_flag, p.hdr, 17, p.spin_limit);
     for (int it = 0; it < n_tiles && ok; ++it) {
       const int sb = it & 1;
       if (it >= 2 && !wait_bar_warp(&bars[S_EMPTY + sb], ((it - 2) >> 1) & 1, abort_flag, p.hdr, 4, p.spin_limit)) break;
@@ -838,9 +880,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
       }
       if (ok) tc::commit_warp(&bars[S_FULL + sb]);
     }
-    // every MMA issued must be complete before the tensor memory is released
+    // every MMA issued must be complete before the tensor memory is released, and the query copy must have
+    // landed before the CTA exits
     tc::commit_warp(&bars[FIN_L]);
     drain_bar(&bars[FIN_L], 0);
+    if (p.qh != nullptr) drain_bar(&bars[Q_FULL], 0);
     __syncwarp();
   } else if (warp == kValuesWarp) {
     // ---------------- values MMA issue: O^T += C^T . P^T, chunk by chunk ----------------
@@ -1226,23 +1270,39 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
+  // exact attention with prepared queries: [units][64][512] fp16, copied in [1 x 64 x 64] boxes (one panel of
+  // 64 latent columns for the 64 head rows) with the 128-byte swizzle of the query panels
+  CUtensorMap qmap;
+  std::memset(&qmap, 0, sizeof(qmap));
+  if (p.qh != nullptr) {
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)kLatent, 64, (cuuint64_t)p.units};
+    const cuuint64_t strides[2] = {(cuuint64_t)kLatent * 2, (cuuint64_t)64 * kLatent * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p.qh, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   ProfScope prof("sparse_attn", s);
   clear_stale_error();
   if (p.q4) {
     cudaError_t e = ensure_smem_limit(attn_tc_kernel<true>, kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_ex(attn_tc_kernel<true>, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads),
-                     (size_t)kSmemBytes, s, pdl, p, map, cmap, wmap);
+                     (size_t)kSmemBytes, s, pdl, p, map, cmap, wmap, qmap);
   }
   cudaError_t e = ensure_smem_limit(attn_tc_kernel<false>, kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_ex(attn_tc_kernel<false>, dim3((unsigned)p.splits, (unsigned)p.units), dim3(kThreads),
-                   (size_t)kSmemBytes, s, pdl, p, map, cmap, wmap);
+                   (size_t)kSmemBytes, s, pdl, p, map, cmap, wmap, qmap);
 }
 
 cudaError_t launch_attn_prep(const AttnParams& p, cudaStream_t s, bool pdl) {
   if (p.units == 0) return cudaSuccess;
-  const int64_t rows = p.units * 64 + (p.window > 0 ? (p.units / p.n_query) * p.swa_rows : 0);
+  const int64_t rows = p.units * 64 + (p.q4 && p.window > 0 ? (p.units / p.n_query) * p.swa_rows : 0);
   ProfScope prof("attn_prep", s);
   clear_stale_error();
   return launch_ex(attn_prep_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s, pdl, p);

@@ -74,7 +74,7 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 struct AttnLayout {
   int64_t units;
   int n_ct, n_wt, splits, cache_splits, win_split, last_ct;
-  size_t o_off, ml_off, q4_off, q4sc_off, q4m_off, w4_off, w4sc_off, total;
+  size_t o_off, ml_off, q4_off, q4sc_off, q4m_off, w4_off, w4sc_off, qh_off, total;
 };
 
 // One CTA per SM: the selected blocks of a query are cut into 128-row tiles (16 blocks) shared by the
@@ -111,7 +111,9 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   L.q4m_off = round_up(L.q4sc_off + qrows * 32, 256);
   L.w4_off = round_up(L.q4m_off + qrows * 4, 256);
   L.w4sc_off = round_up(L.w4_off + wrows * 256, 256);
-  L.total = round_up(L.w4sc_off + wrows * 32, 256);
+  // the exact attention's fp16 queries, converted once a query when several splits would each convert them
+  L.qh_off = round_up(L.w4sc_off + wrows * 32, 256);
+  L.total = round_up(L.qh_off + (L.splits > 1 ? qrows * kLatent * 2 : 0), 256);
   return L;
 }
 
@@ -546,17 +548,23 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.hdr = reinterpret_cast<uint32_t*>(w);
   p.q4 = q4 ? 1 : 0;
   debug_fault(&p.fault, &p.spin_limit);
-  if (q4) {
-    // the NVFP4-query variant rounds the queries and the window rows once, in a kernel of its own; the
-    // attention kernel, its programmatic dependent, copies the rounded operands in
-    p.q4_codes = w + L.q4_off;
-    p.q4_sc = w + L.q4sc_off;
+  // The NVFP4-query variant rounds the queries and the window rows once, in a kernel of its own; the exact
+  // attention converts its queries there too when several splits of a query would each convert them. The
+  // attention kernel, the prepare kernel's programmatic dependent, copies the prepared operands in.
+  const bool prep = q4 || L.splits > 1;
+  if (prep) {
     p.q4_mult = reinterpret_cast<float*>(w + L.q4m_off);
-    p.w4 = w + L.w4_off;
-    p.w4_sc = w + L.w4sc_off;
+    if (q4) {
+      p.q4_codes = w + L.q4_off;
+      p.q4_sc = w + L.q4sc_off;
+      p.w4 = w + L.w4_off;
+      p.w4_sc = w + L.w4sc_off;
+    } else {
+      p.qh = reinterpret_cast<__half*>(w + L.qh_off);
+    }
     if (cudaError_t e = launch_attn_prep(p, stream, early)) return cuda_fail(e, "attn_prep");
   }
-  if (cudaError_t e = launch_attn(p, stream, early || q4)) return cuda_fail(e, "attn");
+  if (cudaError_t e = launch_attn(p, stream, early || prep)) return cuda_fail(e, "attn");
   if (cudaError_t e = launch_combine(p, stream, true)) return cuda_fail(e, "combine");
   return CSA_OK;
 }

@@ -270,6 +270,9 @@ struct AttnParams {
   float* q4_mult;              // [units][64]
   uint8_t* w4;                 // [batch][swa_rows][256]
   uint8_t* w4_sc;              // [batch][swa_rows][32]
+  // Exact attention with several splits a query: the queries converted once by the prepare kernel, each head
+  // scaled by its power of two (q4_mult) and rounded to fp16 (exact), 64 head rows a unit; null otherwise.
+  __half* qh;                  // [units][64][512]
   // Bounded waits give up after this many polls (kSpinLimit unless a test lowered it), and a nonzero
   // fault makes the kernel withhold one arrival (csa_debug_set_fault).
   uint32_t spin_limit;
