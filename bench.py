@@ -54,6 +54,7 @@ def _cases():
         "prefill_2048_at_128k_h64": synth.PREFILL_2K_AT_128K,
         "decode_64k_b32_h64_q4": synth.DECODE_64K_B32_Q4,
         "decode_64k_b32_h64_nvfp4q": synth.DECODE_64K_B32_NVFP4Q,
+        "prefill_2048_at_128k_h64_nvfp4q": synth.PREFILL_2K_AT_128K_NVFP4Q,
         "project_pack_128k_h4096": synth.PROJECT_128K_H4096,
     }
 
@@ -261,9 +262,9 @@ class PrefillWorkload:
             ws=self.ws_pack)
         csa.index_topk(q_idx, kcache, self.n_entries, self.idx, max_entries=self.E, top_k=c.top_k,
                        ws=self.ws_index, q_pos=self.q_pos)
-        csa.sparse_attn_prefill(q, cache, self.n_entries, self.idx, out, q_pos=self.q_pos, max_entries=self.E,
-                                window=c.window, scale=SCALE, ws=self.ws_attn, swa=self.swa,
-                                swa_first_pos=self.swa_first_pos)
+        attn = csa.sparse_attn_prefill_nvfp4q if c.nvfp4q else csa.sparse_attn_prefill
+        attn(q, cache, self.n_entries, self.idx, out, q_pos=self.q_pos, max_entries=self.E, window=c.window,
+             scale=SCALE, ws=self.ws_attn, swa=self.swa, swa_first_pos=self.swa_first_pos)
         return out
 
     def flops(self):

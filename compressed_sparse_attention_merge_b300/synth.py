@@ -147,6 +147,7 @@ class PrefillCase:
     top_k: int = 256
     window: int = 128
     outlier_frac: float = 0.0
+    nvfp4q: bool = False          # attention by the NVFP4-query variant (block-scaled FP4 logits)
     seed: int = 0
 
     @property
@@ -211,6 +212,9 @@ DECODE_1M_B4_HIER = DecodeCase("decode_1m_b4_h64_hier2048", tokens=[1 << 20] * 4
 CHAIN_128K_B64 = DecodeCase("chain20_128k_b64_h64", tokens=[131072] * 64, outlier_frac=0.01, needle_frac=0.01,
                             layers=20, distinct_index_queries=5, seed=20264)
 PREFILL_2K_AT_128K = PrefillCase("prefill_2048_at_128k_h64", context=131072, chunk=2048, seed=20265)
+# The prefill workload above with the opt-in NVFP4-query attention (same inputs, same seed).
+PREFILL_2K_AT_128K_NVFP4Q = PrefillCase("prefill_2048_at_128k_h64_nvfp4q", context=131072, chunk=2048, nvfp4q=True,
+                                        seed=20265)
 # Multi-token decode at the 64K shape: four draft positions per sequence (speculative verification), the
 # last four tokens of each sequence, causal among themselves.
 DECODE_64K_B32_Q4 = DecodeCase("decode_64k_b32_h64_q4", tokens=[65536] * 32, n_query=4, outlier_frac=0.01,

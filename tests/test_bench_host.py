@@ -48,8 +48,11 @@ def test_workload_table():
     v = cases["decode_64k_b32_h64_nvfp4q"]
     assert v.nvfp4q and not d.nvfp4q
     assert dataclasses.replace(v, name=d.name, nvfp4q=False) == d
+    w = cases["prefill_2048_at_128k_h64_nvfp4q"]
+    assert w.nvfp4q and not p.nvfp4q
+    assert dataclasses.replace(w, name=p.name, nvfp4q=False) == p
     # every other workload draws from its own seed
-    seeds = [cases[k].seed for k in cases if k != "decode_64k_b32_h64_nvfp4q"]
+    seeds = [cases[k].seed for k in cases if not k.endswith("_nvfp4q")]
     assert len(set(seeds)) == len(seeds)
 
 

@@ -162,7 +162,15 @@ def test_chain_20_layers_128k_batch64():
 
 
 def test_prefill_2048_at_128k():
-    w = bench.make_workload("prefill_2048_at_128k_h64", DEV, replicas=1, keep_inputs=True)
+    _prefill_case("prefill_2048_at_128k_h64")
+
+
+def test_prefill_2048_at_128k_nvfp4q():
+    _prefill_case("prefill_2048_at_128k_h64_nvfp4q")
+
+
+def _prefill_case(name):
+    w = bench.make_workload(name, DEV, replicas=1, keep_inputs=True)
     c = w.case
     w.step(0)
     torch.cuda.synchronize()
@@ -186,8 +194,14 @@ def test_prefill_2048_at_128k():
         p = int(pos[k])
         rows = _oracle_rows(tok, ref[k], lambda e: e < E and 2 * e + 1 <= p)
         win = o_attn.prefill_window(swa, first, p, c.window)
-        want, _ = o_attn.attend(to_np(d["q"][0, j]).astype(np.float64), np.concatenate([rows, win]), SCALE)
-        assert_attn_close(out[j], want, f"prefill position {p}")
+        qj = to_np(d["q"][0, j]).astype(np.float64)
+        if c.nvfp4q:
+            keys = np.concatenate([rows, o_fp4.round_trip(np.asarray(win, np.float32), "amax")])
+            want, _ = o_attn.attend_kv(o_attn.nvfp4_query(qj.astype(np.float32)), keys, np.concatenate([rows, win]),
+                                       SCALE)
+        else:
+            want, _ = o_attn.attend(qj, np.concatenate([rows, win]), SCALE)
+        assert_attn_close(out[j], want, f"{name} position {p}")
 
 
 def test_chain_step_as_one_graph_replays_the_eager_step():
