@@ -74,6 +74,7 @@ IndexLayout index_layout(int64_t batch, const csa_index_args* a) {
 struct AttnLayout {
   int64_t units;
   int n_ct, n_wt, splits, cache_splits, win_split, last_ct;
+  bool exact_prep;
   size_t o_off, ml_off, q4_off, q4sc_off, q4m_off, w4_off, w4sc_off, qh_off, total;
 };
 
@@ -111,9 +112,13 @@ AttnLayout attn_layout(int64_t batch, const csa_attn_args* a, int num_sms) {
   L.q4m_off = round_up(L.q4sc_off + qrows * 32, 256);
   L.w4_off = round_up(L.q4m_off + qrows * 4, 256);
   L.w4sc_off = round_up(L.w4_off + wrows * 256, 256);
-  // the exact attention's fp16 queries, converted once a query when several splits would each convert them
+  // The exact attention's fp16 queries, converted once a query by the prepare kernel when several splits would
+  // each convert them and there are enough queries for the conversions to crowd the attention's start; with a
+  // few queries the extra launch costs more than it saves (measured: tiny and 1M decode lose 1-2 %, the 64K
+  // decode and the 20-layer chain gain).
+  L.exact_prep = L.splits > 1 && L.units >= 16;
   L.qh_off = round_up(L.w4sc_off + wrows * 32, 256);
-  L.total = round_up(L.qh_off + (L.splits > 1 ? qrows * kLatent * 2 : 0), 256);
+  L.total = round_up(L.qh_off + (L.exact_prep ? qrows * kLatent * 2 : 0), 256);
   return L;
 }
 
@@ -549,9 +554,9 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
   p.q4 = q4 ? 1 : 0;
   debug_fault(&p.fault, &p.spin_limit);
   // The NVFP4-query variant rounds the queries and the window rows once, in a kernel of its own; the exact
-  // attention converts its queries there too when several splits of a query would each convert them. The
+  // attention converts its queries there too when many queries have several splits each (see attn_layout). The
   // attention kernel, the prepare kernel's programmatic dependent, copies the prepared operands in.
-  const bool prep = q4 || L.splits > 1;
+  const bool prep = q4 || L.exact_prep;
   if (prep) {
     p.q4_mult = reinterpret_cast<float*>(w + L.q4m_off);
     if (q4) {
