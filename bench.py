@@ -796,6 +796,9 @@ class OracleDecodeSample:
                 if self.q_pos is not None:
                     out, _ = o_attn.prefill_attention(qj, entries, E, idx[j], self.swa[layer], self.swa_first_pos,
                                                       int(self.q_pos[j]), c.window, SCALE)
+                elif c.nvfp4q:
+                    out, _ = o_attn.decode_attention_nvfp4q(self.q[layer, j], entries, E, idx[j], self.swa[layer],
+                                                            SCALE)
                 else:
                     out, _ = o_attn.decode_attention(qj, entries, E, idx[j], self.swa[layer], SCALE)
                 outs.append(out)
@@ -834,9 +837,10 @@ class OraclePrefillSample:
         pos = np.array(self.positions)
         idx, _ = o_idx.flat_topk(self.q_idx, keys, E, c.top_k, q_pos=pos)
         outs = []
+        attend = o_attn.prefill_attention_nvfp4q if c.nvfp4q else o_attn.prefill_attention
         for j, p in enumerate(self.positions):
-            out, _ = o_attn.prefill_attention(self.q[j].astype(np.float64), entries, E, idx[j], self.swa,
-                                              P - c.window + 1, int(p), c.window, SCALE)
+            qj = self.q[j] if c.nvfp4q else self.q[j].astype(np.float64)
+            out, _ = attend(qj, entries, E, idx[j], self.swa, P - c.window + 1, int(p), c.window, SCALE)
             outs.append(out)
         return outs
 
