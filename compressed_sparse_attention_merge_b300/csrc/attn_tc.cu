@@ -724,6 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
     for (int it = 0; it < n_tiles && !stop; ++it) {
       if (warp == kConv0 && lane == 0) *progress = it;
       const bool win = it < nw;
+      // NVFP4-query mode: the converters set the tile cadence and usually find the previous tile's value
+      // products long complete; they complete in issue order, so one test of the last chunk's barrier stands in
+      // for the four per-chunk waits
+      bool prev_done = kQ4 && !win && it > 0 &&
+                       __all_sync(0xffffffffu, mbar_test_wait(smem_addr(&bars[V_EMPTY + kChunks - 1]), (it - 1) & 1));
       const int k = it - nw;                       // cache tile index within this CTA
       bool vr = false;
       if (win) {
@@ -773,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
         }
         // values operand: the chunk must have been consumed by the previous tile's value products (a window
         // tile's chunks were, before its copy was issued)
-        if (!win && it > 0 &&
+        if (!win && it > 0 && !prev_done &&
             !__all_sync(0xffffffffu, wait_bar(&bars[V_EMPTY + c], (it - 1) & 1, abort_flag, p.hdr, 6, p.spin_limit))) {
           stop = true;
           break;
