@@ -789,9 +789,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const AttnParams p
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           *reinterpret_cast<uint4*>(vrow + ((j ^ (row & 7)) << 4)) = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        tc::fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[V_FULL + c]);
+        // publish the chunk to the value products; in NVFP4-query mode, where the converters set the cadence,
+        // two chunks at a time (one proxy fence and round of arrivals per pair)
+        if (!kQ4 || (c & 1)) {
+          tc::fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            if (kQ4) mbar_arrive(&bars[V_FULL + c - 1]);
+            mbar_arrive(&bars[V_FULL + c]);
+          }
+        }
       }
       if (!win) {
         // the scales of tile k + 2 are loaded a tile before the queue reaches it, its id one more tile earlier
