@@ -524,8 +524,12 @@ size_t csa_sparse_attn_workspace_size(int64_t batch, const csa_attn_args* a) {
 // The attention's launches; `early` makes the attention kernel a programmatic dependent of the kernel before
 // it, which is only right when that kernel belongs to the same call (the attention loads the call's queries
 // and window rows before it waits).
+// Which launches of the call: all of them, only the prepare kernel, or everything after it (a caller that
+// launched the prepare kernel earlier on the same stream, as csa_decode_layers does).
+enum AttnPhase { ATTN_ALL = 0, ATTN_PREP_ONLY = 1, ATTN_AFTER_PREP = 2 };
+
 static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, size_t ws_bytes, cudaStream_t stream,
-                              bool prefill, bool early, bool q4 = false) {
+                              bool prefill, bool early, bool q4 = false, int phase = ATTN_ALL) {
   csa_status st = validate_attn(batch, a, prefill);
   if (st != CSA_OK) return st;
   int num_sms = 0;
@@ -567,8 +571,11 @@ static csa_status sparse_attn(int64_t batch, const csa_attn_args* a, void* ws, s
     } else {
       p.qh = reinterpret_cast<__half*>(w + L.qh_off);
     }
-    if (cudaError_t e = launch_attn_prep(p, stream, early)) return cuda_fail(e, "attn_prep");
+    if (phase != ATTN_AFTER_PREP) {
+      if (cudaError_t e = launch_attn_prep(p, stream, early)) return cuda_fail(e, "attn_prep");
+    }
   }
+  if (phase == ATTN_PREP_ONLY) return CSA_OK;
   if (cudaError_t e = launch_attn(p, stream, early || prep)) return cuda_fail(e, "attn");
   if (cudaError_t e = launch_combine(p, stream, true)) return cuda_fail(e, "combine");
   return CSA_OK;
@@ -633,6 +640,20 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
   src = nullptr;
   for (int l = 0; l < n_layers; ++l) {
     const csa_layer_args& L = layers[l];
+    const bool q4 = (L.flags & CSA_LAYER_ATTN_NVFP4Q) != 0;
+    // The layer's prepare kernel (queries and window rows, when the attention uses one) goes first: it reads
+    // only the layer's inputs, so it runs beside the end of the previous layer and ahead of the indexer; the
+    // attention, launched after the Top-K, implies its completion.
+    {
+      csa_attn_args aa = *attn_tmpl;
+      aa.q = L.q;
+      aa.idx = L.mode != CSA_LAYER_REUSE ? L.idx : src;
+      aa.swa = L.swa;
+      aa.out = L.out;
+      aa.out_lse = L.out_lse;
+      const csa_status st = sparse_attn(batch, &aa, ws_attn, ws_attn_bytes, stream, causal, true, q4, ATTN_PREP_ONLY);
+      if (st != CSA_OK) return st;
+    }
     if (L.mode != CSA_LAYER_REUSE) {
       csa_index_args ia = *index_tmpl;
       ia.q_idx = L.q_idx;
@@ -648,8 +669,7 @@ csa_status csa_decode_layers(int64_t batch, int n_layers, const csa_layer_args* 
     aa.swa = L.swa;
     aa.out = L.out;
     aa.out_lse = L.out_lse;
-    const csa_status st = sparse_attn(batch, &aa, ws_attn, ws_attn_bytes, stream, causal, true,
-                                      (L.flags & CSA_LAYER_ATTN_NVFP4Q) != 0);
+    const csa_status st = sparse_attn(batch, &aa, ws_attn, ws_attn_bytes, stream, causal, true, q4, ATTN_AFTER_PREP);
     if (st != CSA_OK) return st;
   }
   return CSA_OK;
