@@ -718,7 +718,7 @@ TRAFFIC = {
     #   --replicas 1 (ncu reports these in GB / MB with six digits)
     ("project_pack_128k_h4096", "project_pack"): 1_102_514_000 + 19_863_808,
     ("decode_64k_b32_h64", "sparse_attn"): 25_296_640 + 0,
-    ("decode_64k_b32_h64_nvfp4q", "sparse_attn"): 24_989_952 + 256,
+    ("decode_64k_b32_h64_nvfp4q", "sparse_attn"): 24_971_520 + 0,
     ("decode_64k_b32_h64", "index_score"): 75_609_088 + 892_160,
 }
 
