@@ -102,18 +102,16 @@ def flat_topk(q, keys, n_entries, k, head_w=None, relu=True, q_pos=None):
 
 
 def coarse_keys(keys, n_entries):
-    """Super-block coarse keys: float32 [ceil(n_entries / 512), D], each the fp32 sum in ascending
-    entry order of the dequantised keys of its entries below n_entries."""
-    keys = np.asarray(keys, np.float32)[:n_entries]
+    """Super-block coarse keys: float32 [ceil(n_entries / 512), D], each the sum of the dequantised keys of
+    its entries below n_entries ([card] Key ideas, hierarchical indexer; the summary is this library's
+    reading), taken exactly and rounded once to fp32. Dequantised FP4 keys are multiples of 2^-13 below
+    2,688 in magnitude, so the fp64 sum of a super-block (at most 512 of them) is exact."""
+    keys = np.asarray(keys, np.float64)[:n_entries]
     n_super = -(-n_entries // ENTRIES_PER_SUPER)
     d = keys.shape[1]
-    padded = np.zeros((n_super * ENTRIES_PER_SUPER, d), np.float32)
+    padded = np.zeros((n_super * ENTRIES_PER_SUPER, d), np.float64)
     padded[:n_entries] = keys
-    grouped = padded.reshape(n_super, ENTRIES_PER_SUPER, d)
-    acc = np.zeros((n_super, d), np.float32)
-    for i in range(ENTRIES_PER_SUPER):      # sequential fp32 accumulation, ascending entry order
-        acc = acc + grouped[:, i, :]
-    return acc
+    return padded.reshape(n_super, ENTRIES_PER_SUPER, d).sum(axis=1).astype(np.float32)
 
 
 def hierarchical_topk(q, keys, n_entries, k, keep_blocks, head_w=None, relu=True, coarse=None):

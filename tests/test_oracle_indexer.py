@@ -2,6 +2,7 @@
 flat selection."""
 
 import itertools
+import math
 
 import numpy as np
 
@@ -107,12 +108,38 @@ def test_hierarchical_restricts_to_kept_super_blocks():
     assert set(idx2[0].tolist()) <= set(range(128, 192)) | set(range(320, 384))
 
 
-def test_coarse_keys_sum_in_order():
+def test_coarse_keys_per_super_block():
     k = np.ones((1100, 8), np.float32)
     c = indexer.coarse_keys(k, 1100)
     np.testing.assert_array_equal(c[:, 0], [512, 512, 76])
     for a, b in itertools.product(range(2), range(2)):
         assert c[a, b] == 512
+
+
+def test_coarse_keys_are_exact_sums_rounded_once():
+    # 342 keys of 1536 (code 6 x scale 2^8) then 170 of 2^-5 (code 0.5 x 2^-4): a sum in entry order in fp32
+    # loses every 2^-5 (half an ulp at 525,312, a tie that rounds to even), the exact sum keeps them
+    k = np.zeros((512, 2), np.float32)
+    k[:342] = 1536.0
+    k[342:] = 2.0 ** -5
+    c = indexer.coarse_keys(k, 512)
+    assert c[0, 0] == np.float32(525312 + 170 * 2.0 ** -5)
+    ordered = np.float32(0)
+    for v in k[:, 0]:
+        ordered = np.float32(ordered + v)
+    assert ordered == np.float32(525312) != c[0, 0]
+
+
+def test_coarse_keys_match_an_exactly_rounded_sum():
+    # against Python's math.fsum (an exactly rounded sum), on dequantised FP4 keys of every magnitude
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((1100, 16)).astype(np.float32) * np.exp2(rng.integers(-12, 9, (1100, 1)))
+    deq = fp4.dequantize(fp4.pack(x, 1, "pow2"), 16, 1100)
+    c = indexer.coarse_keys(deq, 1100)
+    for g in range(3):
+        rows = deq[512 * g:min(512 * g + 512, 1100)]
+        want = [np.float32(math.fsum(rows[:, j])) for j in range(16)]
+        np.testing.assert_array_equal(c[g], want)
 
 
 def test_query_rounding_is_identity_on_small_integers():
