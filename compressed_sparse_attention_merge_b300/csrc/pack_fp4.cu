@@ -132,20 +132,30 @@ __global__ void __launch_bounds__(256) pack_fp4_multi_kernel(const __grid_consta
   pack_thread<TPG>(m.job[j], ((int64_t)blockIdx.x - m.cta_begin[j]) * blockDim.x + threadIdx.x);
 }
 
-// coarse_sum[b][g][d] = fp32 sum, ascending entry order, of the dequantised element d of entries
+// coarse_sum[b][g][d] = the exact sum, rounded once to fp32, of the dequantised element d of entries
 // [512 g, min(512 (g + 1), first + n_new)), for every super-block g touched by this call. One CTA per
-// (super-block, sequence), one thread per element d: the super-block's packed bytes are staged through
-// shared memory in chunks, each one bulk copy, and each thread then sums its element over the chunk's
-// entries in ascending order.
+// (super-block, 32 columns, sequence): the super-block's packed bytes are staged through shared memory in
+// chunks, each one bulk copy; the 32 warps take slices of the entries, each lane summing its column in int64
+// fixed point (2^13 times a dequantised key is an integer), and the slices' sums are added and rounded at the
+// end.
 constexpr int kCoarseStage = 36864;
 
 __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touched) {
   __shared__ __align__(16) uint8_t stage[kCoarseStage];
+  __shared__ long long part[1024];
   __shared__ __align__(8) uint64_t bar;
   griddep_wait();                                // before any access: the packed entries come from the kernel before
   griddep_launch();
-  const int d = threadIdx.x;                     // blockDim.x == dim
-  const int gl = blockIdx.x;
+  // thread = (column d, slice of the entries): a dequantised key is a multiple of 2^-13 below 2,688 in
+  // magnitude, so 2^13 times it is an integer and the slices' int64 sums add up to the exact sum in any order,
+  // rounded once to fp32 at the end
+  // a CTA takes 32 columns of one super-block (grid.x = touched super-blocks x dim / 32): lane = column,
+  // warp = slice of the entries
+  const int ncg = p.dim / 32;
+  const int d = (blockIdx.x % ncg) * 32 + (threadIdx.x & 31);
+  const int sl = threadIdx.x >> 5;
+  const int slices = blockDim.x >> 5;
+  const int gl = blockIdx.x / ncg;
   const int64_t b = blockIdx.y;
   const int64_t first = p.first_entry ? (int64_t)p.first_entry[b] : 0;
   if (first < 0 || first + p.n_new > p.max_entries || p.n_new == 0) return;
@@ -159,24 +169,24 @@ __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touc
   const int half = p.dim / 2, groups = p.dim / kGroup;
   const int chunk_blocks = kCoarseStage / bb < kSuper ? kCoarseStage / bb : kSuper;
   const uint8_t* seq = p.cache + b * p.cache_stride_b;
-  if (d == 0) {
+  if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
-  float acc = 0.0f;
+  long long acc = 0;
   uint32_t phase = 0;
   for (int64_t blk0 = g * kSuper; blk0 * kBlockEntries < e_hi; blk0 += chunk_blocks) {
     const int64_t n_e = e_hi - blk0 * kBlockEntries;
     const int nb = (int)((n_e + kBlockEntries - 1) / kBlockEntries < chunk_blocks
                              ? (n_e + kBlockEntries - 1) / kBlockEntries : chunk_blocks);
     __syncthreads();                             // the previous chunk has been read (and bar initialised)
-    if (d == 0) {
+    if (threadIdx.x == 0) {
       mbar_arrive_expect_tx(&bar, (uint32_t)(nb * bb));
       bulk_g2s(stage, seq + blk0 * bb, (uint32_t)(nb * bb), &bar);
     }
     if (!__syncthreads_and(mbar_wait(&bar, phase))) {
       // give up: report, let the copy land (bounded), leave without writing a sum
-      if (d == 0) {
+      if (threadIdx.x == 0) {
         report(p.hdr, CSA_ERR_TIMEOUT, KID_COARSE_SUM, (uint32_t)b);
         mbar_wait(&bar, phase);
       }
@@ -184,19 +194,29 @@ __global__ void __launch_bounds__(1024) coarse_sum_kernel(PackParams p, int touc
     }
     phase ^= 1u;
     const int ne = (int)(n_e < (int64_t)nb * kBlockEntries ? n_e : (int64_t)nb * kBlockEntries);
-#pragma unroll 8
-    for (int i = 0; i < ne; ++i) {
+#pragma unroll 4
+    for (int i = sl; i < ne; i += slices) {
       const uint8_t* blk = stage + (i >> 3) * bb;
       const int slot = i & 7;
-      // both nibbles of the byte to fp16 (exact), this thread's element, times the group scale (exact in
-      // fp32), added in ascending entry order
-      const uint32_t h2 = e2m1x2_to_f16x2(blk[slot * half + d / 2]);
-      const float x = __half2float(__ushort_as_half((unsigned short)((d & 1) ? (h2 >> 16) : (h2 & 0xFFFFu))));
-      const float sc = e4m3_to_float(blk[kBlockEntries * half + slot * groups + d / kGroup]);
-      acc = __fadd_rn(acc, __fmul_rn(x, sc));
+      // 2^13 times the dequantised element, from the bits: the E2M1 magnitude in halves (0, 1, 2, 3, 4, 6, 8,
+      // 12 for codes 0-7) times 2^12 times the E4M3 scale ((8 + m) 2^(e + 2) for exponent field e > 0, 8 m
+      // for a subnormal), below 2^25
+      const uint32_t code = ((uint32_t)blk[slot * half + d / 2] >> (4 * (d & 1))) & 0xFu;
+      const int c2 = (int)((0xC8643210u >> (4 * (code & 7u))) & 0xFu);
+      const uint32_t sb = blk[kBlockEntries * half + slot * groups + d / kGroup];
+      const uint32_t e = (sb >> 3) & 0xFu, m = sb & 7u;
+      const int s12 = e == 0u ? (int)(m << 3) : (int)((8u + m) << (e + 2u));
+      const int v = c2 * s12;
+      acc += (code & 8u) ? -(long long)v : (long long)v;
     }
   }
-  p.coarse_sum[b * p.coarse_stride_b + g * p.dim + d] = acc;
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  if (sl == 0) {
+    long long sum = 0;
+    for (int k = 0; k < slices; ++k) sum += part[k * 32 + (threadIdx.x & 31)];
+    p.coarse_sum[b * p.coarse_stride_b + g * p.dim + d] = __fmul_rn(__ll2float_rn(sum), 1.0f / 8192.0f);
+  }
 }
 
 }  // namespace
@@ -244,10 +264,11 @@ cudaError_t launch_coarse_sum(const PackParams& p, cudaStream_t s) {
   if (p.coarse_sum == nullptr || p.n_new == 0 || p.batch == 0) return cudaSuccess;
   const int64_t per_super = (int64_t)kSuper * kBlockEntries;
   const int touched = (int)((p.n_new + per_super - 1) / per_super) + 1;
-  dim3 grid((unsigned)touched, (unsigned)p.batch);
+  // dim / 32 CTAs per touched super-block (dim is 64, 128 or 256), 1024 threads: 32 columns x 32 slices
+  dim3 grid((unsigned)(touched * (p.dim / 32)), (unsigned)p.batch);
   ProfScope prof("coarse_sum", s);
   clear_stale_error();
-  return launch_ex(coarse_sum_kernel, grid, dim3((unsigned)p.dim), 0, s, true, p, touched);
+  return launch_ex(coarse_sum_kernel, grid, dim3(1024u), 0, s, true, p, touched);
 }
 
 }  // namespace csa

@@ -121,10 +121,10 @@ csa_status csa_get_device_status(void* ws, cudaStream_t stream);
  *   code byte j of an entry holds element 2j in its low nibble and 2j+1 in its high nibble.
  *
  * If coarse_sum is not NULL, after packing every super-block (64 blocks = 512 entries) that received a
- * new entry is recomputed: coarse_sum[b][g][d] = sum, in ascending entry order in fp32, of the dequantized
+ * new entry is recomputed: coarse_sum[b][g][d] = the exact sum, rounded once to fp32, of the dequantized
  * element d over entries [512 g, min(512 (g+1), first_entry[b] + n_new)). This assumes entries are appended
- * in order, so that [0, first_entry[b] + n_new) is the valid prefix. The sums are exact when the dequantized
- * values are integers (index keys under CSA_SCALE_POW2 with integer inputs).
+ * in order, so that [0, first_entry[b] + n_new) is the valid prefix. (Dequantized values are multiples of
+ * 2^-13 below 2,688 in magnitude, so the sum is taken exactly in 64-bit fixed point.)
  *
  * Arguments (all strides in elements unless stated):
  *   x            device, [batch][n_tokens][dim] rows of x_dtype; each row contiguous; 16-byte aligned rows.

@@ -21,8 +21,8 @@ no score function, tie rule or hierarchy shape; the readings taken here:
     candidate (score -inf here).
   * Top-K: the min(K, #candidates) candidates with the largest scores, ties to the lower block id,
     listed in ascending block id and padded with -1.
-  * hierarchical: super-block g covers blocks [64 g, 64 g + 64); its coarse key is the fp32 sum, in
-    ascending entry order, of the dequantised keys of its entries below n_entries; super-blocks are
+  * hierarchical: super-block g covers blocks [64 g, 64 g + 64); its coarse key is the sum of the
+    dequantised keys of its entries below n_entries, taken exactly and rounded once to fp32; super-blocks are
     scored with the same score function, the best keep_blocks / 64 are kept (ties to the lower id), and
     the block Top-K runs over their blocks only.
 """

@@ -80,6 +80,28 @@ def test_pow2_keys_and_coarse_sums(csa):
             np.testing.assert_array_equal(coarse[b, :c_ref.shape[0]].cpu().numpy(), c_ref)
 
 
+def test_coarse_sums_are_exact_sums(csa):
+    # real-valued keys over a wide range of magnitudes, and a super-block whose sum in entry order in fp32 would
+    # lose 170 half-ulp increments: the coarse sums equal the exact sum rounded once, bit for bit
+    g = torch.Generator(device=DEV).manual_seed(4)
+    for dim in (64, 128, 256):
+        E = 512 * 2 + 300
+        x = torch.randn(1, E, dim, generator=g, device=DEV)
+        x = x * torch.exp2(torch.randint(-12, 9, (1, E, 1), generator=g, device=DEV).float())
+        x[0, :342] = 1536.0
+        x[0, 342:512] = 2.0 ** -5
+        ws = csa.workspace(256, DEV)
+        coarse = csa.empty_coarse(1, E, dim, DEV)
+        cache = csa.empty_cache(1, E, dim, DEV)
+        csa.pack_fp4(x, cache, merge=1, scale_rule=csa.SCALE_POW2, max_entries=E, ws=ws, coarse_sum=coarse)
+        assert csa.device_status(ws) == csa.OK
+        ref = o_fp4.pack(x[0].cpu().numpy(), 1, "pow2", n_blocks=cache.shape[1])
+        np.testing.assert_array_equal(cache[0].cpu().numpy(), ref)
+        c_ref = o_idx.coarse_keys(o_fp4.dequantize(ref, dim, E), E)
+        assert c_ref[0, 0] == np.float32(525312 + 170 * 2.0 ** -5)
+        np.testing.assert_array_equal(coarse[0, :c_ref.shape[0]].cpu().numpy(), c_ref)
+
+
 def test_append_at_first_entry(csa):
     g = torch.Generator(device=DEV).manual_seed(4)
     E = 3000
