@@ -450,8 +450,9 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
 // to FP4 once (16-element groups, power-of-two scales: the rounding the block products use) into shared
 // memory, then each warp scores its super-blocks with lanes over the feature index (per-lane fused
 // multiply-adds in feature order, then a butterfly sum), the ReLU, the head weights and the ordered head
-// sum.
-constexpr int kCoarsePerWarp = 8;
+// sum. Two super-blocks a warp: with a few queries (the 1M decode has 4 x 1,024 super-blocks) more CTAs
+// spread the latency-bound scoring over the SMs (16.1 -> 11.1 us against eight a warp).
+constexpr int kCoarsePerWarp = 2;
 constexpr int kCoarsePerCta = 8 * kCoarsePerWarp;
 
 __global__ void __launch_bounds__(256) coarse_score_kernel(CoarseScoreParams p) {
