@@ -36,6 +36,17 @@
 // split over several CTAs, every split writes its unnormalised partial (o, m, l) and the combine kernel
 // merges them in split order (measured faster than merging inside the kernel across a thread-block
 // cluster, through distributed shared memory or through L2 copies).
+//
+// Prepared operands. A prepare kernel (attn_prep_kernel, the attention's predecessor) converts each query
+// once into the workspace when many queries have several splits each, so that the splits copy the fp16
+// panels in by tensor map instead of each converting them.
+//
+// NVFP4-query mode (attn_tc_kernel<true>, opt-in). The logits are taken on the block-scaled FP4 tensor cores
+// (kind::mxf4nvf4): the prepare kernel rounds the query heads and the window rows to the cache's FP4 format;
+// the logits warp copies each tile's FP4 keys (cache codes, or the rounded window rows) into a raw stage by
+// tensor map as soon as the previous tile's logits are complete, and the converters, which still build the
+// exact fp16 tile for the value products, write the keys' scale factors to tensor memory one tile ahead. The
+// logits then never wait for the values buffer; the converters set the tile cadence.
 #include <cuda.h>
 
 #include <cstring>

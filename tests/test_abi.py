@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("csa_pack_fp4", "csa_pack_fp4_multi", "csa_index_topk", "csa_sparse_attn_decode",
-              "csa_sparse_attn_prefill"):
+              "csa_sparse_attn_prefill", "csa_sparse_attn_decode_nvfp4q", "csa_sparse_attn_prefill_nvfp4q",
+              "csa_project_pack", "csa_decode_layers"):
         assert n in names
 
 
@@ -197,3 +198,26 @@ def test_static_index_validates_before_sizing(lib):
     ia.heads, ia.n_query, ia.max_entries = 4, 1, 64
     ia.q_idx, ia.keys, ia.n_entries, ia.out_idx, ia.keys_stride_b = 0x10008, 0x10000, 0x10000, 0x10000, 8 * 576
     assert lib.csa_index_topk_static(1, ctypes.byref(ia), None, None) == b.ERR_ALIGNMENT
+
+
+def test_nvfp4q_attention_and_layer_flags_reject_before_any_device_call(lib):
+    # the NVFP4-query calls share the exact calls' validation; csa_decode_layers checks every layer's flags
+    # before anything is launched (none of this needs a device)
+    from compressed_sparse_attention_merge_b300 import binding as b
+    assert lib.csa_sparse_attn_decode_nvfp4q(1, None, None, 0, None) == b.ERR_INVALID_ARG
+    assert lib.csa_sparse_attn_prefill_nvfp4q(1, None, None, 0, None) == b.ERR_INVALID_ARG
+    aa = b.AttnArgs()
+    aa.n_query, aa.heads, aa.top_k, aa.window, aa.scale = 1, 20, 8, 128, 0.04      # 20 heads
+    assert lib.csa_sparse_attn_decode_nvfp4q(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
+    aa.heads, aa.window = 64, 2048                                                 # window beyond 1,024
+    assert lib.csa_sparse_attn_prefill_nvfp4q(1, ctypes.byref(aa), None, 0, None) == b.ERR_INVALID_ARG
+    # a layer flag other than CSA_LAYER_ATTN_NVFP4Q
+    layers = (b.LayerArgs * 1)()
+    layers[0].mode, layers[0].flags = b.LAYER_FULL, 2
+    ia, aa = b.IndexArgs(), b.AttnArgs()
+    assert lib.csa_decode_layers(1, 1, layers, ctypes.byref(ia), ctypes.byref(aa), None, 0, None, 0,
+                                 None) == b.ERR_INVALID_ARG
+    # a first layer in Reuse mode (no indices to reuse)
+    layers[0].mode, layers[0].flags = b.LAYER_REUSE, b.LAYER_ATTN_NVFP4Q
+    assert lib.csa_decode_layers(1, 1, layers, ctypes.byref(ia), ctypes.byref(aa), None, 0, None, 0,
+                                 None) == b.ERR_INVALID_ARG
