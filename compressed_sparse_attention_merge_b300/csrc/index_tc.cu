@@ -165,8 +165,26 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_ptr + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Barriers and tensor memory touch no global memory. With a few query columns (decode) they are set up
+  // before the wait on the kernel before, so that they overlap its end; with many (prefill) the wait comes
+  // first (setting up first slowed prefill, measured).
+  auto setup = [&]() {
+    if (warp == 1) tc::alloc(tmem_ptr, C::kTmemCols);
+    if (tid == 0) {
+      for (int i = 0; i < C::kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); mbar_init(&sfr[i], 4); }
+      for (int i = 0; i < C::kND; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4); }
+      mbar_init(fin, 1);
+      fence_mbar_init();
+      *abort_flag = 0;
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  };
+  if constexpr (N <= 16) setup();
   griddep_wait();                                  // (hierarchical) the kept super-blocks come from the kernel before
   griddep_launch();
+  if constexpr (N > 16) setup();
   const bool hier = p.kept != nullptr;
   const int64_t unit = blockIdx.y;
   IdxUnit u;
@@ -188,19 +206,7 @@ index_tc_kernel(const ScoreParams p, int64_t stages_per_unit, int splits, int gr
   const int64_t k1 = stages_per_unit * (blockIdx.x + 1) / splits;
   const int n = (int)(k1 - k0);
 
-  // ---------------- setup: barriers and tensor memory; then the copies start while the other warps
-  // prepare the unit's FP4 queries ----------------
-  if (warp == 1) tc::alloc(tmem_ptr, C::kTmemCols);
-  if (tid == 0) {
-    for (int i = 0; i < C::kStages; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); mbar_init(&sfr[i], 4); }
-    for (int i = 0; i < C::kND; ++i) { mbar_init(&dfull[i], 1); mbar_init(&dempty[i], 4); }
-    mbar_init(fin, 1);
-    fence_mbar_init();
-    *abort_flag = 0;
-  }
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
+  // ---------------- the copies start while the other warps prepare the unit's FP4 queries ----------------
   const uint32_t tbase = *tmem_ptr;
   const uint32_t s_base = smem_addr(smem);
   if (warp == 0) {
