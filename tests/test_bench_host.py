@@ -60,3 +60,15 @@ def test_shards_draw_other_seeds_with_the_same_shapes():
     a, b = bench.shard_case("decode_64k_b32_h64", 0), bench.shard_case("decode_64k_b32_h64", 1)
     assert a.seed != b.seed
     assert (a.batch, a.max_entries, a.top_k) == (b.batch, b.max_entries, b.top_k)
+
+
+def test_nvfp4q_workloads_share_the_byte_and_flop_models():
+    # the NVFP4-query workloads move the same algorithmic bytes (and do the same attention work) as the exact
+    # ones: the roofline lines of the two variants are comparable
+    import dataclasses as dc
+    cases = bench._cases()
+    d, v = cases["decode_64k_b32_h64"], cases["decode_64k_b32_h64_nvfp4q"]
+    per = bench.attn_bytes_per_query(d.heads, d.top_k, d.window)
+    assert per == bench.attn_bytes_per_query(v.heads, v.top_k, v.window) == 918_528
+    p, w = cases["prefill_2048_at_128k_h64"], cases["prefill_2048_at_128k_h64_nvfp4q"]
+    assert dc.replace(w, name=p.name, nvfp4q=False) == p
